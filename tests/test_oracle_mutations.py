@@ -1,0 +1,68 @@
+"""Plant plausible mistakes in the oracle (on the CPU) and check the pins catch each.
+
+Every mutation below swaps one helper of ``oracle.sdpa`` for a wrong version
+-- a dropped term, a wrong sign or index, a transposed or swapped operand --
+and runs the full pin list of ``test_oracle_pins.py``.  A mutation that no
+pin notices would mean the pins do not fix that part of the oracle.
+"""
+import numpy as np
+import pytest
+
+from oracle import sdpa as OA
+from tests.test_oracle_pins import PINS
+
+_orig = {name: getattr(OA, name) for name in
+         ("scores", "visible_mask", "kv_head_of", "softmax_two_pass", "log_sum_exp", "attention_head")}
+
+
+def _softmax_wrong_axis(S, visible):
+    Sm = np.where(visible, S, -np.inf)
+    m = np.max(Sm, axis=1, initial=-np.inf)
+    E = np.where(visible, np.exp(Sm - np.where(np.isfinite(m), m, 0.0)[:, None]), 0.0)
+    l = E.sum(axis=1)
+    col = E.sum(axis=0, keepdims=True)
+    return E / np.where(col > 0, col, 1.0), m, l
+
+
+def _softmax_sign(S, visible):
+    Sm = np.where(visible, S, -np.inf)
+    m = np.max(Sm, axis=1, initial=-np.inf)
+    ms = np.where(np.isfinite(m), m, 0.0)[:, None]
+    E = np.where(visible, np.exp(np.where(visible, ms - S, 0.0)), 0.0)
+    l = E.sum(axis=1)
+    return E / np.where(l > 0, l, 1.0)[:, None], m, l
+
+
+def _attention_head_k_for_v(Qh, Kh, Vh, scale, causal, visible=None):
+    return _orig["attention_head"](Qh, Kh, Kh[:, : Vh.shape[1]] if Kh.shape[1] >= Vh.shape[1] else Vh,
+                                   scale, causal, visible)
+
+
+MUTATIONS = {
+    "scale_dropped": ("scores", lambda Qh, Kh, scale: Qh @ Kh.T),
+    "logit_sign": ("scores", lambda Qh, Kh, scale: -scale * (Qh @ Kh.T)),
+    "mask_top_left": ("visible_mask", lambda Lq, Lkv, causal: (np.arange(Lkv)[None, :] <= np.arange(Lq)[:, None])
+                      if causal else np.ones((Lq, Lkv), bool)),
+    "mask_off_by_one": ("visible_mask", lambda Lq, Lkv, causal: (np.arange(Lkv)[None, :] < np.arange(Lq)[:, None]
+                                                                + (Lkv - Lq)) if causal else np.ones((Lq, Lkv), bool)),
+    "mask_ignored": ("visible_mask", lambda Lq, Lkv, causal: np.ones((Lq, Lkv), bool)),
+    "gqa_modulo": ("kv_head_of", lambda hq, Hq, Hkv: hq % Hkv),
+    "softmax_wrong_axis": ("softmax_two_pass", _softmax_wrong_axis),
+    "softmax_exp_sign": ("softmax_two_pass", _softmax_sign),
+    "lse_log2": ("log_sum_exp", lambda m, l: np.where(l > 0, m + np.log2(np.where(l > 0, l, 1.0)), -np.inf)),
+    "lse_drops_max": ("log_sum_exp", lambda m, l: np.where(l > 0, np.log(np.where(l > 0, l, 1.0)), -np.inf)),
+    "k_used_for_v": ("attention_head", _attention_head_k_for_v),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_some_pin_catches(name, monkeypatch):
+    attr, bad = MUTATIONS[name]
+    monkeypatch.setattr(OA, attr, bad)
+    caught = []
+    for pin in PINS:
+        try:
+            pin()
+        except Exception:  # an assertion or a shape error both mean the pin noticed
+            caught.append(pin.__name__)
+    assert caught, f"mutation {name} passed every pin"

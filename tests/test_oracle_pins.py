@@ -1,0 +1,299 @@
+"""Pins of the fp64 oracle against things other than itself (CPU only).
+
+Each pin checks the oracle against a fact fixed by the mathematics or by the
+pages' definition of attention (Operator Fusion, GPU learning diary day 24,
+§3.4: S = QK^T/sqrt(d) + mask, P = softmax(S), O = PV):
+
+* a brute-force pure-Python loop on tiny shapes (independent arithmetic);
+* closed forms: identical keys, a dominant logit, the causal first row, a
+  single key, V = 1 (softmax rows sum to one), hand-worked rational cases;
+* special cases that reduce to library routines: torch's fp64
+  scaled_dot_product_attention for square masks, scipy's softmax and
+  logsumexp for one query;
+* structural reductions: GQA == MHA with repeated K/V heads, decode ==
+  last row of causal prefill, packed sequences == per-sequence dense,
+  scale folded into q, key permutation invariance.
+
+``PINS`` lists every pin; ``tests/test_oracle_mutations.py`` plants mistakes
+in the oracle and checks that some pin fails for each.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import sdpa as OA
+from oracle.brute import attention_loops
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "hand_worked.json")
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+def _qkv(seed, B, Hq, Hkv, Lq, Lkv, D, Dv=None):
+    r = _rng(seed)
+    Dv = D if Dv is None else Dv
+    return (r.standard_normal((B, Hq, Lq, D)), r.standard_normal((B, Hkv, Lkv, D)),
+            r.standard_normal((B, Hkv, Lkv, Dv)))
+
+
+# ----------------------------------------------------------------------------- pins
+
+def pin_brute_force():
+    """Vectorised oracle == literal loops, on shapes covering every mask case."""
+    cases = [
+        (1, 2, 2, 7, 7, 5, False),
+        (1, 2, 2, 9, 9, 4, True),
+        (2, 4, 2, 3, 11, 8, True),   # Lq < Lkv causal: bottom-right offset
+        (1, 2, 1, 12, 6, 3, True),   # Lq > Lkv causal: first rows see nothing
+        (1, 3, 3, 5, 6, 6, False),
+        (1, 1, 1, 6, 6, 6, True),    # square D == L catches a transposed operand
+    ]
+    for n, (B, Hq, Hkv, Lq, Lkv, D, causal) in enumerate(cases):
+        q, k, v = _qkv(10 + n, B, Hq, Hkv, Lq, Lkv, D)
+        scale = 0.37 + 0.1 * n
+        O, lse = OA.attention(q, k, v, scale, causal)
+        Ob, lseb = attention_loops(q, k, v, scale, causal)
+        np.testing.assert_allclose(O, np.array(Ob), rtol=0, atol=1e-12)
+        np.testing.assert_allclose(lse, np.array(lseb), rtol=0, atol=1e-12)
+
+
+def pin_rows_sum_to_one():
+    """softmax rows sum to 1, so V == 1 gives O == 1 on every row that sees a key."""
+    for causal, (Lq, Lkv) in [(False, (9, 13)), (True, (13, 13)), (True, (5, 17))]:
+        q, k, _ = _qkv(20, 1, 2, 2, Lq, Lkv, 6)
+        S = OA.scores(q[0, 0], k[0, 0], 0.8)
+        P, _, _ = OA.softmax_two_pass(S, OA.visible_mask(Lq, Lkv, causal))
+        np.testing.assert_allclose(P.sum(axis=1), 1.0, rtol=0, atol=1e-14)
+        assert (P >= 0).all()
+        ones = np.ones((1, 2, Lkv, 3))
+        O, _ = OA.attention(q, k, ones, 0.8, causal)
+        np.testing.assert_allclose(O, 1.0, rtol=0, atol=1e-14)
+
+
+def pin_identical_keys():
+    """All keys equal c: O_i = mean of the visible V rows, lse_i = scale q_i.c + ln(n_visible)."""
+    r = _rng(30)
+    Lq, Lkv, D = 6, 10, 4
+    c = r.standard_normal(D)
+    q = r.standard_normal((1, 1, Lq, D))
+    k = np.broadcast_to(c, (1, 1, Lkv, D)).copy()
+    v = r.standard_normal((1, 1, Lkv, D))
+    for causal in (False, True):
+        O, lse = OA.attention(q, k, v, 0.5, causal)
+        for i in range(Lq):
+            n = (i + Lkv - Lq + 1) if causal else Lkv
+            np.testing.assert_allclose(O[0, 0, i], v[0, 0, :n].mean(axis=0), atol=1e-13)
+            assert abs(lse[0, 0, i] - (0.5 * q[0, 0, i] @ c + math.log(n))) < 1e-13
+
+
+def pin_dominant_logit():
+    """One key aligned with q and 50x longer dominates: O ~ V[k*], lse ~ its logit."""
+    r = _rng(40)
+    D, Lkv, kstar = 16, 12, 7
+    q = r.standard_normal((1, 1, 1, D))
+    k = 0.01 * r.standard_normal((1, 1, Lkv, D))
+    k[0, 0, kstar] = 50.0 * q[0, 0, 0] / np.linalg.norm(q[0, 0, 0])
+    v = r.standard_normal((1, 1, Lkv, D))
+    O, lse = OA.attention(q, k, v, 1.0, False)
+    logit = q[0, 0, 0] @ k[0, 0, kstar]
+    assert logit > 40
+    np.testing.assert_allclose(O[0, 0, 0], v[0, 0, kstar], atol=1e-9)
+    assert abs(lse[0, 0, 0] - logit) < 1e-9
+
+
+def pin_causal_first_row():
+    """Square causal: row 0 sees only key 0, so O[0] = V[0] and lse[0] = S[0,0]."""
+    q, k, v = _qkv(50, 2, 3, 3, 8, 8, 5)
+    O, lse = OA.attention(q, k, v, 0.3, True)
+    np.testing.assert_allclose(O[:, :, 0], v[:, :, 0], atol=1e-15)
+    np.testing.assert_allclose(lse[:, :, 0], 0.3 * np.einsum("bhd,bhd->bh", q[:, :, 0], k[:, :, 0]), atol=1e-14)
+
+
+def pin_single_key():
+    """Lkv == 1: every row's weight is 1 on the only key."""
+    q, k, v = _qkv(60, 1, 2, 2, 4, 1, 3)
+    O, lse = OA.attention(q, k, v, 0.9, False)
+    np.testing.assert_allclose(O, np.broadcast_to(v, O.shape), atol=1e-15)
+    np.testing.assert_allclose(lse[0, 0], 0.9 * q[0, 0] @ k[0, 0, 0], atol=1e-14)
+
+
+def pin_hand_worked_golden():
+    """Cases worked by hand with rational softmax weights (tests/golden/hand_worked.json)."""
+    with open(GOLDEN) as f:
+        cases = json.load(f)["cases"]
+    for c in cases:
+        O, lse = OA.attention(np.array(c["q"]), np.array(c["k"]), np.array(c["v"]), c["scale"], c["causal"])
+        np.testing.assert_allclose(O, np.array(c["O"]), rtol=0, atol=1e-14, err_msg=c["name"])
+        np.testing.assert_allclose(lse, np.array(c["lse"]), rtol=0, atol=1e-14, err_msg=c["name"])
+
+
+def pin_torch_sdpa():
+    """torch's fp64 CPU scaled_dot_product_attention (library routine), where its
+    causal convention (top-left) coincides with ours: square masks."""
+    F = torch.nn.functional
+    for B, Hq, Hkv, L, D, causal in [(2, 4, 4, 17, 8, False), (1, 4, 2, 23, 16, True), (1, 8, 2, 5, 4, False)]:
+        q, k, v = _qkv(70 + L, B, Hq, Hkv, L, L, D)
+        O, _ = OA.attention(q, k, v, 0.25, causal)
+        tq, tk, tv = (torch.from_numpy(x) for x in (q, k, v))
+        ref = F.scaled_dot_product_attention(tq, tk, tv, is_causal=causal, scale=0.25, enable_gqa=(Hq != Hkv))
+        np.testing.assert_allclose(O, ref.numpy(), atol=1e-12)
+
+
+def pin_scipy_single_query():
+    """One query: O = softmax(scale K q) V and lse = logsumexp(scale K q) (scipy routines)."""
+    from scipy.special import logsumexp, softmax
+
+    r = _rng(80)
+    D, Lkv = 12, 31
+    q = r.standard_normal((1, 1, 1, D))
+    k = r.standard_normal((1, 1, Lkv, D))
+    v = r.standard_normal((1, 1, Lkv, D))
+    O, lse = OA.attention(q, k, v, 0.6, False)
+    z = 0.6 * (k[0, 0] @ q[0, 0, 0])
+    np.testing.assert_allclose(O[0, 0, 0], softmax(z) @ v[0, 0], atol=1e-13)
+    assert abs(lse[0, 0, 0] - logsumexp(z)) < 1e-13
+
+
+def pin_gqa_equals_mha():
+    """Grouped heads == multi-head attention with each K/V head repeated over its query group."""
+    B, Hq, Hkv, L, D = 2, 8, 2, 9, 4
+    q, k, v = _qkv(90, B, Hq, Hkv, L, L + 3, D)
+    g = Hq // Hkv
+    for causal in (False, True):
+        O, lse = OA.attention(q, k, v, 0.5, causal)
+        Om, lsem = OA.attention(q, np.repeat(k, g, axis=1), np.repeat(v, g, axis=1), 0.5, causal)
+        np.testing.assert_allclose(O, Om, atol=1e-14)
+        np.testing.assert_allclose(lse, lsem, atol=1e-14)
+
+
+def pin_decode_is_last_causal_row():
+    """Decode over kv_len keys == the last row of causal prefill over those keys."""
+    r = _rng(100)
+    B, Hq, Hkv, Lmax, D = 3, 4, 2, 16, 8
+    lens = [16, 5, 1]
+    qd = r.standard_normal((B, Hq, D))
+    kc = r.standard_normal((B, Hkv, Lmax, D))
+    vc = r.standard_normal((B, Hkv, Lmax, D))
+    O, lse = OA.decode(qd, kc, vc, lens, 0.4)
+    for b, n in enumerate(lens):
+        qp = r.standard_normal((1, Hq, n, D))
+        qp[0, :, n - 1] = qd[b]
+        Op, lsep = OA.attention(qp, kc[b:b + 1, :, :n], vc[b:b + 1, :, :n], 0.4, True)
+        np.testing.assert_allclose(O[b], Op[0, :, n - 1], atol=1e-14)
+        np.testing.assert_allclose(lse[b], lsep[0, :, n - 1], atol=1e-14)
+
+
+def pin_scale_folds_into_q():
+    """scale s with q == scale 1 with s*q (the scale multiplies the logits)."""
+    q, k, v = _qkv(110, 1, 2, 2, 6, 9, 5)
+    for causal in (False, True):
+        O1, l1 = OA.attention(q, k, v, 0.3, causal)
+        O2, l2 = OA.attention(0.3 * q, k, v, 1.0, causal)
+        np.testing.assert_allclose(O1, O2, atol=1e-14)
+        np.testing.assert_allclose(l1, l2, atol=1e-14)
+
+
+def pin_key_permutation():
+    """Non-causal: permuting K and V rows together leaves O and lse unchanged."""
+    q, k, v = _qkv(120, 1, 2, 2, 5, 11, 4)
+    perm = _rng(121).permutation(11)
+    O1, l1 = OA.attention(q, k, v, 0.7, False)
+    O2, l2 = OA.attention(q, k[:, :, perm], v[:, :, perm], 0.7, False)
+    np.testing.assert_allclose(O1, O2, atol=1e-14)
+    np.testing.assert_allclose(l1, l2, atol=1e-14)
+
+
+def pin_varlen_is_per_sequence_dense():
+    """Packed sequences == dense attention run on each sequence's own slices."""
+    r = _rng(130)
+    lens = [5, 1, 9, 3]
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    Hq, Hkv, D = 4, 2, 6
+    q = r.standard_normal((cu[-1], Hq, D))
+    k = r.standard_normal((cu[-1], Hkv, D))
+    v = r.standard_normal((cu[-1], Hkv, D))
+    for causal in (False, True):
+        O, lse = OA.attention_varlen(q, k, v, cu, cu, 0.5, causal)
+        for s in range(len(lens)):
+            sl = slice(cu[s], cu[s + 1])
+            Od, lsed = OA.attention(q[sl].transpose(1, 0, 2)[None], k[sl].transpose(1, 0, 2)[None],
+                                    v[sl].transpose(1, 0, 2)[None], 0.5, causal)
+            np.testing.assert_allclose(O[sl], Od[0].transpose(1, 0, 2), atol=1e-14)
+            np.testing.assert_allclose(lse[sl], lsed[0].T, atol=1e-14)
+        Ob, lseb = attention_loops(q[:5].transpose(1, 0, 2)[None], k[:5].transpose(1, 0, 2)[None],
+                                   v[:5].transpose(1, 0, 2)[None], 0.5, causal)
+        np.testing.assert_allclose(O[:5], np.array(Ob)[0].transpose(1, 0, 2), atol=1e-12)
+
+
+def pin_rows_equal_full():
+    """Row-sampled helpers reproduce the corresponding rows of the full computation."""
+    q, k, v = _qkv(140, 2, 4, 2, 10, 10, 4)
+    O, lse = OA.attention(q, k, v, 0.5, True)
+    rows = [0, 3, 9]
+    Or, lr = OA.attention_rows(q, k, v, 0.5, True, 1, 3, rows)
+    np.testing.assert_allclose(Or, O[1, 3, rows], atol=1e-15)
+    np.testing.assert_allclose(lr, lse[1, 3, rows], atol=1e-15)
+    r = _rng(141)
+    lens = [4, 7]
+    cu = np.array([0, 4, 11])
+    qv, kv, vv = (r.standard_normal((11, 4, 4)), r.standard_normal((11, 2, 4)), r.standard_normal((11, 2, 4)))
+    Ov, lv = OA.attention_varlen(qv, kv, vv, cu, cu, 0.5, True)
+    Ovr, lvr = OA.attention_varlen_rows(qv, kv, vv, cu, cu, 0.5, True, 1, 2, [0, 6])
+    np.testing.assert_allclose(Ovr, Ov[[4, 10], 2], atol=1e-15)
+    np.testing.assert_allclose(lvr, lv[[4, 10], 2], atol=1e-15)
+
+
+def pin_empty_rows():
+    """Rows that see no key: O = 0 and lse = -inf (causal Lq > Lkv; decode kv_len == 0)."""
+    q, k, v = _qkv(150, 1, 1, 1, 6, 3, 2)
+    O, lse = OA.attention(q, k, v, 1.0, True)
+    assert np.all(O[0, 0, :3] == 0) and np.all(np.isneginf(lse[0, 0, :3]))
+    assert np.all(np.isfinite(lse[0, 0, 3:]))
+    r = _rng(151)
+    Od, lsed = OA.decode(r.standard_normal((2, 2, 4)), r.standard_normal((2, 1, 5, 4)),
+                         r.standard_normal((2, 1, 5, 4)), [0, 5], 0.5)
+    assert np.all(Od[0] == 0) and np.all(np.isneginf(lsed[0]))
+    assert np.all(np.isfinite(lsed[1]))
+
+
+def pin_bf16_inputs_promote_exactly():
+    """bf16 torch inputs reach fp64 unchanged (every bf16 value is exact in fp64)."""
+    t = torch.tensor([1.0 + 2 ** -7, -3.0, 2.0 ** -100], dtype=torch.bfloat16)
+    np.testing.assert_array_equal(OA.to_f64(t), np.array([1.0 + 2 ** -7, -3.0, 2.0 ** -100]))
+
+
+PINS = [
+    pin_brute_force,
+    pin_rows_sum_to_one,
+    pin_identical_keys,
+    pin_dominant_logit,
+    pin_causal_first_row,
+    pin_single_key,
+    pin_hand_worked_golden,
+    pin_torch_sdpa,
+    pin_scipy_single_query,
+    pin_gqa_equals_mha,
+    pin_decode_is_last_causal_row,
+    pin_scale_folds_into_q,
+    pin_key_permutation,
+    pin_varlen_is_per_sequence_dense,
+    pin_rows_equal_full,
+    pin_empty_rows,
+    pin_bf16_inputs_promote_exactly,
+]
+
+
+@pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
+def test_pin(pin):
+    pin()
+
+
+def test_package_exports_match_module():
+    assert oracle.attention is OA.attention and oracle.decode is OA.decode
