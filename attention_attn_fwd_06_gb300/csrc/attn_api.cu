@@ -1,0 +1,358 @@
+// attn_api.cu -- the C ABI declared in include/attn.h.
+//
+// Host side only: argument validation (before anything touches the device),
+// the sm_103 device check, the per-device split-KV workspace and status word,
+// and the kernel launches.  No compute happens here and there is no CPU path.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/attn.h"
+#include "kernels.h"
+
+// Device status word: kernels record the first problem they see (a kv_len out
+// of range, an expired pipeline wait); attn_get_device_status() reads and
+// clears it.  Each device holds its own copy.
+__device__ unsigned g_attn_device_status;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kMaxSplits = 12288;
+
+struct DeviceState {
+  bool probed = false;
+  int support = ATTN_OK;  // ATTN_ERR_UNSUPPORTED when the device is not sm_103
+  int num_sms = 0;
+  unsigned* status = nullptr;
+  void* ws = nullptr;
+  size_t ws_bytes = 0;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+// Looks up (and on first use probes) the current device.  Caller holds g_mu.
+int device_state_locked(DeviceState** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return ATTN_ERR_UNSUPPORTED;
+  }
+  DeviceState& s = g_dev[dev];
+  if (!s.probed) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return ATTN_ERR_CUDA;
+    }
+    s.support = (major == 10 && minor == 3) ? ATTN_OK : ATTN_ERR_UNSUPPORTED;
+    s.num_sms = sms;
+    if (s.support == ATTN_OK) {
+      if (cudaGetSymbolAddress(reinterpret_cast<void**>(&s.status), g_attn_device_status) != cudaSuccess) {
+        cudaGetLastError();
+        return ATTN_ERR_CUDA;
+      }
+    }
+    s.probed = true;
+  }
+  *out = &s;
+  return s.support;
+}
+
+int map_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return ATTN_OK;
+  if (e == cudaErrorNotSupported) return ATTN_ERR_UNSUPPORTED;
+  return ATTN_ERR_CUDA;
+}
+
+// Ensures the workspace of `s` holds `bytes`.  Refuses to allocate while the
+// stream is being captured into a CUDA graph.  Caller holds g_mu.
+int ensure_workspace_locked(DeviceState& s, size_t bytes, cudaStream_t stream) {
+  if (bytes <= s.ws_bytes) return ATTN_OK;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) {
+    cudaGetLastError();
+    return ATTN_ERR_CUDA;
+  }
+  if (cap != cudaStreamCaptureStatusNone) return ATTN_ERR_INVALID_ARG;
+  if (s.ws != nullptr) {
+    cudaFree(s.ws);  // synchronises the device: no earlier decode can still be using it
+    s.ws = nullptr;
+    s.ws_bytes = 0;
+  }
+  if (cudaMalloc(&s.ws, bytes) != cudaSuccess) {
+    cudaGetLastError();
+    s.ws = nullptr;
+    return ATTN_ERR_CUDA;
+  }
+  s.ws_bytes = bytes;
+  return ATTN_OK;
+}
+
+struct DecodeShape {
+  int chunk = 0;
+  int nsplit = 0;
+  size_t part_o_elems = 0;
+  size_t part_ml_elems = 0;
+  size_t bytes = 0;
+};
+
+// Keys per split: aim for about 8 CTAs per SM at the cache's full length, in
+// whole pipeline stages.  The real lengths live on the device, so this is an
+// upper-bound estimate.
+int auto_chunk(int B, int Hq, int Hkv, int Lmax, int D, int num_sms) {
+  const int sk = attn::decode_stage_keys(D);
+  const int group = Hq / Hkv;
+  const long long rows = (long long)B * Hkv * (group / attn::decode_heads_per_cta(group));
+  const long long target = (long long)(num_sms > 0 ? num_sms : 148) * 8;
+  long long chunk = (rows * (long long)Lmax + target - 1) / target;
+  chunk = ((chunk + sk - 1) / sk) * sk;
+  if (chunk < sk) chunk = sk;
+  if (chunk > 64LL * sk) chunk = 64LL * sk;
+  return (int)chunk;
+}
+
+DecodeShape decode_shape(int B, int Hq, int Hkv, int Lmax, int D, int chunk, int num_sms) {
+  DecodeShape s;
+  s.chunk = chunk > 0 ? chunk : auto_chunk(B, Hq, Hkv, Lmax, D, num_sms);
+  s.nsplit = Lmax > 0 ? (Lmax + s.chunk - 1) / s.chunk : 1;
+  const size_t rows = (size_t)B * Hq * s.nsplit;
+  s.part_o_elems = rows * D;
+  s.part_ml_elems = rows * 2;
+  s.bytes = (s.part_o_elems + s.part_ml_elems) * sizeof(float);
+  return s;
+}
+
+int validate_decode(const attn_decode_params* p) {
+  if (p == nullptr) return ATTN_ERR_INVALID_ARG;
+  if (p->B < 0 || p->Hq <= 0 || p->Hkv <= 0 || p->Lmax < 0 || p->D <= 0) return ATTN_ERR_INVALID_ARG;
+  if (p->Hq % p->Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (p->D != 64 && p->D != 128) return ATTN_ERR_UNSUPPORTED;
+  if (p->out_dtype != ATTN_DTYPE_BF16 && p->out_dtype != ATTN_DTYPE_F32) return ATTN_ERR_INVALID_ARG;
+  if (p->chunk < 0 || p->chunk > (1 << 20)) return ATTN_ERR_INVALID_ARG;
+  if (!(p->scale == p->scale)) return ATTN_ERR_INVALID_ARG;  // NaN scale
+  if (p->B == 0) return ATTN_OK;
+  if (p->q == nullptr || p->kcache == nullptr || p->vcache == nullptr || p->kv_lens == nullptr ||
+      p->out == nullptr)
+    return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(p->q) || !aligned16(p->kcache) || !aligned16(p->vcache) || !aligned16(p->out) ||
+      !aligned4(p->kv_lens) || (p->lse != nullptr && !aligned4(p->lse)))
+    return ATTN_ERR_ALIGNMENT;
+  if (p->B > 65535 || p->Hkv > 65535 || (long long)p->B * p->Hq > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+  return ATTN_OK;
+}
+
+int validate_fwd(const attn_fwd_params* p) {
+  if (p == nullptr) return ATTN_ERR_INVALID_ARG;
+  if (p->B < 0 || p->Hq <= 0 || p->Hkv <= 0 || p->Lq < 0 || p->Lkv < 0 || p->D <= 0)
+    return ATTN_ERR_INVALID_ARG;
+  if (p->Hq % p->Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (p->D != 64 && p->D != 128) return ATTN_ERR_UNSUPPORTED;
+  if (p->causal != 0 && p->causal != 1) return ATTN_ERR_INVALID_ARG;
+  if (p->out_dtype != ATTN_DTYPE_BF16 && p->out_dtype != ATTN_DTYPE_F32) return ATTN_ERR_INVALID_ARG;
+  if (!(p->scale == p->scale)) return ATTN_ERR_INVALID_ARG;
+  const bool varlen = p->cu_seqlens_q != nullptr || p->cu_seqlens_k != nullptr;
+  if (varlen) {
+    if (p->cu_seqlens_q == nullptr || p->cu_seqlens_k == nullptr) return ATTN_ERR_INVALID_ARG;
+    if (p->total_q < 0 || p->total_k < 0) return ATTN_ERR_INVALID_ARG;
+    if (!aligned4(p->cu_seqlens_q) || !aligned4(p->cu_seqlens_k)) return ATTN_ERR_ALIGNMENT;
+  }
+  if (p->B == 0 || p->Lq == 0 || (varlen && p->total_q == 0)) return ATTN_OK;
+  if (p->q == nullptr || p->k == nullptr || p->v == nullptr || p->out == nullptr) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(p->q) || !aligned16(p->k) || !aligned16(p->v) || !aligned16(p->out) ||
+      (p->lse != nullptr && !aligned4(p->lse)))
+    return ATTN_ERR_ALIGNMENT;
+  if (p->B > 65535 || (long long)p->B * p->Hq > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+  return ATTN_OK;
+}
+
+bool is_empty_fwd(const attn_fwd_params* p) {
+  const bool varlen = p->cu_seqlens_q != nullptr;
+  return p->B == 0 || p->Lq == 0 || (varlen && p->total_q == 0);
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_version(void) { return 100; }
+
+const char* attn_status_string(int status) {
+  switch (status) {
+    case ATTN_OK: return "ATTN_OK";
+    case ATTN_ERR_INVALID_ARG: return "ATTN_ERR_INVALID_ARG";
+    case ATTN_ERR_UNSUPPORTED: return "ATTN_ERR_UNSUPPORTED";
+    case ATTN_ERR_ALIGNMENT: return "ATTN_ERR_ALIGNMENT";
+    case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA";
+    case ATTN_ERR_DEVICE_TIMEOUT: return "ATTN_ERR_DEVICE_TIMEOUT";
+    case ATTN_ERR_DEVICE_BOUNDS: return "ATTN_ERR_DEVICE_BOUNDS";
+    default: return "ATTN_STATUS_UNKNOWN";
+  }
+}
+
+unsigned long long attn_decode_workspace_bytes(int B, int Hq, int Hkv, int Lmax, int D, int chunk) {
+  attn_decode_params p = {};
+  p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.Lmax = Lmax; p.D = D; p.chunk = chunk;
+  p.q = p.kcache = p.vcache = reinterpret_cast<const void*>(16);
+  p.kv_lens = reinterpret_cast<const int*>(16);
+  p.out = reinterpret_cast<void*>(16);
+  if (validate_decode(&p) != ATTN_OK || B == 0) return 0;
+  int sms = 0;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState* s = nullptr;
+    if (device_state_locked(&s) == ATTN_OK) sms = s->num_sms;
+  }
+  return decode_shape(B, Hq, Hkv, Lmax, D, chunk, sms).bytes;
+}
+
+int attn_decode_ex(const attn_decode_params* p) {
+  int st = validate_decode(p);
+  if (st != ATTN_OK) return st;
+  if (p->B == 0) return ATTN_OK;
+  cudaStream_t stream = static_cast<cudaStream_t>(p->stream);
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState* s = nullptr;
+  st = device_state_locked(&s);
+  if (st != ATTN_OK) return st;
+  const DecodeShape sh = decode_shape(p->B, p->Hq, p->Hkv, p->Lmax, p->D, p->chunk, s->num_sms);
+  if (sh.nsplit > kMaxSplits) return ATTN_ERR_UNSUPPORTED;  // combine keeps one weight per split in smem
+  st = ensure_workspace_locked(*s, sh.bytes, stream);
+  if (st != ATTN_OK) return st;
+  attn::DecodeLaunch L;
+  L.q = p->q;
+  L.kcache = p->kcache;
+  L.vcache = p->vcache;
+  L.kv_lens = p->kv_lens;
+  L.out = p->out;
+  L.lse = p->lse;
+  L.part_o = static_cast<float*>(s->ws);
+  L.part_ml = static_cast<float*>(s->ws) + sh.part_o_elems;
+  L.B = p->B;
+  L.Hq = p->Hq;
+  L.Hkv = p->Hkv;
+  L.Lmax = p->Lmax;
+  L.D = p->D;
+  L.chunk = sh.chunk;
+  L.nsplit = sh.nsplit;
+  L.scale = p->scale;
+  L.out_f32 = p->out_dtype == ATTN_DTYPE_F32;
+  L.status = s->status;
+  L.stream = stream;
+  return map_cuda(attn::launch_decode(L));
+}
+
+int attn_decode(const void* q, const void* kcache, const void* vcache, const int* kv_lens, void* out, float* lse,
+                int B, int Hq, int Hkv, int Lmax, int D, float scale, void* stream) {
+  attn_decode_params p = {};
+  p.q = q;
+  p.kcache = kcache;
+  p.vcache = vcache;
+  p.kv_lens = kv_lens;
+  p.out = out;
+  p.lse = lse;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.Lmax = Lmax;
+  p.D = D;
+  p.scale = scale;
+  p.out_dtype = ATTN_DTYPE_BF16;
+  p.chunk = 0;
+  p.stream = stream;
+  return attn_decode_ex(&p);
+}
+
+int attn_fwd_ex(const attn_fwd_params* p) {
+  int st = validate_fwd(p);
+  if (st != ATTN_OK) return st;
+  if (is_empty_fwd(p)) return ATTN_OK;
+  cudaStream_t stream = static_cast<cudaStream_t>(p->stream);
+  DeviceState* s = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    st = device_state_locked(&s);
+  }
+  if (st != ATTN_OK) return st;
+  attn::PrefillLaunch L;
+  L.q = p->q;
+  L.k = p->k;
+  L.v = p->v;
+  L.out = p->out;
+  L.lse = p->lse;
+  L.B = p->B;
+  L.Hq = p->Hq;
+  L.Hkv = p->Hkv;
+  L.Lq = p->Lq;
+  L.Lkv = p->Lkv;
+  L.D = p->D;
+  L.scale = p->scale;
+  L.causal = p->causal;
+  L.out_f32 = p->out_dtype == ATTN_DTYPE_F32;
+  L.cu_q = p->cu_seqlens_q;
+  L.cu_k = p->cu_seqlens_k;
+  L.total_q = p->total_q;
+  L.total_k = p->total_k;
+  L.status = s->status;
+  L.stream = stream;
+  return map_cuda(attn::launch_prefill(L));
+}
+
+int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq, int Hkv, int Lq,
+             int Lkv, int D, float scale, int causal, void* stream) {
+  attn_fwd_params p = {};
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.out = out;
+  p.lse = lse;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.Lq = Lq;
+  p.Lkv = Lkv;
+  p.D = D;
+  p.scale = scale;
+  p.causal = causal;
+  p.out_dtype = ATTN_DTYPE_BF16;
+  p.stream = stream;
+  return attn_fwd_ex(&p);
+}
+
+int attn_get_device_status(void* stream) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState* s = nullptr;
+  int st = device_state_locked(&s);
+  if (st != ATTN_OK) return st;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return ATTN_ERR_CUDA;
+  }
+  unsigned v = 0;
+  if (cudaMemcpy(&v, s->status, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return ATTN_ERR_CUDA;
+  const unsigned zero = 0;
+  if (cudaMemcpy(s->status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return ATTN_ERR_CUDA;
+  return static_cast<int>(v);
+}
+
+void attn_release_workspace(void) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return;
+  }
+  DeviceState& s = g_dev[dev];
+  if (s.ws != nullptr) cudaFree(s.ws);
+  s.ws = nullptr;
+  s.ws_bytes = 0;
+}
+
+}  // extern "C"

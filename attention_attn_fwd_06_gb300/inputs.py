@@ -89,7 +89,8 @@ def make_decode(B, Hq, Hkv, Lmax, D, seed, kv_lens=None, kv_range=None):
     """Decode inputs: q [B,Hq,D], caches [B,Hkv,Lmax,D] bf16, kv_lens int32 [B].
 
     ``kv_lens`` fixes the lengths; otherwise they are drawn uniformly from the
-    inclusive ``kv_range`` with the same generator (after the tensors).
+    inclusive ``kv_range`` with the same generator (after the tensors); with
+    neither, every sequence uses the whole cache.
     """
     g = _gen(seed)
     q = randn_bf16((B, Hq, D), g)
@@ -97,6 +98,8 @@ def make_decode(B, Hq, Hkv, Lmax, D, seed, kv_lens=None, kv_range=None):
     vc = randn_bf16((B, Hkv, Lmax, D), g)
     if kv_lens is not None and len(kv_lens) > 0:
         lens = torch.tensor(list(kv_lens), dtype=torch.int32)
+    elif kv_range is None:
+        lens = torch.full((B,), int(Lmax), dtype=torch.int32)
     else:
         lo, hi = kv_range
         lens = torch.randint(int(lo), int(hi) + 1, (B,), generator=g, dtype=torch.int64).to(torch.int32)

@@ -1,0 +1,579 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused attention forward library on one GB300 (or N replicas).
+
+Default workload: single-token GQA decode over a KV cache (B=8, Hq=32, Hkv=8,
+D=128, kv_len uniform in [512, 4096], cache Lmax=4096), the configuration the
+decode HBM-bandwidth metric is quoted on.  One step = one ``attn_decode`` call
+(split pass + log-sum-exp combine) over that batch.  Other workloads:
+``--workload decode_long | prefill_causal | prefill_ragged_gqa |
+prefill_noncausal_d64 | tiny_causal``.
+
+Timing: inputs resident in HBM; W untimed warm-up steps; then exactly K
+steps, each bracketed by CUDA events on the launching stream, with a write of
+a 512 MB buffer (> the 129 MB L2) between steps so every step reads K/V from
+HBM; barrier + synchronize on both sides; max over ranks.  ``value`` is
+algorithmic bytes (decode: K/V rows actually attended, plus q, O and lse) or
+algorithmic FLOPs (prefill: 4*D per visible query/key pair) per second.
+``e2e`` repeats the measurement through the same call with the inputs copied
+from pinned host memory and the outputs copied back inside the timed region.
+``cpu_baseline`` times the fp64 oracle on a bounded sample on the host cores.
+
+``--impl reference`` times that oracle alone (the only reference this
+library has) and prints the same JSON line with ``"impl": "reference"``.
+
+With ``--gpus N > 1`` (launched by torch.distributed.run) every rank runs an
+independent replica of the workload; nothing is exchanged ("scaling": "weak").
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decode attn HBM GB/s (% of peak); prefill attn TFLOP/s (% of tensor peak)"
+FLUSH_BYTES = 512 << 20
+HBM_FALLBACK_GBS = 6800.0
+BF16_FALLBACK_TFLOPS = 1900.0
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": HBM_FALLBACK_GBS, "bf16_tflops": BF16_FALLBACK_TFLOPS,
+                "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def read_traffic(kernel: str):
+    """Per-launch DRAM bytes from the committed ncu summary, if it matches the current kernel source."""
+    import hashlib
+
+    path = os.path.join(ROOT, "profiles", f"{kernel}_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    kv = {}
+    for line in open(path):
+        if "=" in line and not line.startswith("#"):
+            k, v = line.strip().split("=", 1)
+            kv[k.strip()] = v.strip()
+    src = os.path.join(ROOT, "attention_attn_fwd_06_gb300", "csrc", kv.get("source", ""))
+    if not os.path.exists(src):
+        return None
+    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    if digest != kv.get("source_sha256_16"):
+        return None  # kernel changed since the counters were taken
+    try:
+        return float(kv["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """Samples nvidia-smi SM clocks and throttle reasons in the background."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.samples = []  # (t, sm, max, power, reasons)
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm, mx = float(parts[0]), float(parts[1])
+            except ValueError:
+                continue
+            reasons = [n for n, v in zip(names, parts[3:7]) if v.lower() == "active"]
+            self.samples.append((time.time(), sm, mx, parts[2], reasons))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        inside = [s for s in self.samples if t0 <= s[0] <= t1]
+        window = "timed"
+        if not inside:
+            inside = [s for s in self.samples if s[0] <= t1 + 0.5]
+            window = "warmup+timed (the timed region was shorter than the sampling interval)"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "window": "none"}
+        sms = sorted(s[1] for s in inside)
+        reasons = sorted({r for s in inside for r in s[4]})
+        return {"sm_mhz": sms[len(sms) // 2], "sm_max_mhz": max(s[2] for s in inside), "reasons": reasons,
+                "samples": len(inside), "window": window}
+
+
+# ----------------------------------------------------------------------------- workloads
+
+class DecodeCase:
+    def __init__(self, w, device):
+        import torch
+
+        from attention_attn_fwd_06_gb300.inputs import make_decode
+
+        self.w = w
+        q, kc, vc, lens = make_decode(w.B, w.Hq, w.Hkv, w.L, w.D, w.seed,
+                                      kv_lens=w.kv_lens or None, kv_range=w.kv_range or None)
+        self.host = [t.pin_memory() for t in (q, kc, vc, lens)]
+        self.dev = [t.to(device) for t in self.host]
+        self.out = torch.empty((w.B, w.Hq, w.D), dtype=torch.bfloat16, device=device)
+        self.lse = torch.empty((w.B, w.Hq), dtype=torch.float32, device=device)
+        self.out_h = torch.empty_like(self.out, device="cpu").pin_memory()
+        self.lse_h = torch.empty_like(self.lse, device="cpu").pin_memory()
+        self.lens = [int(x) for x in lens.tolist()]
+        kv_bytes = sum(self.lens) * w.Hkv * w.D * 2 * 2
+        self.alg_bytes = kv_bytes + w.B * w.Hq * w.D * 2 * 2 + w.B * w.Hq * 4
+        self.work = self.alg_bytes
+        self.unit, self.kind = "GB/s", "hbm"
+        self.launches_per_step = 2
+        self.h2d = sum(t.numel() * t.element_size() for t in self.host)
+        self.d2h = self.out.numel() * 2 + self.lse.numel() * 4
+
+    def step(self):
+        from attention_attn_fwd_06_gb300 import binding as AB
+
+        q, kc, vc, lens = self.dev
+        AB.attn_decode(q, kc, vc, lens, out=self.out, lse=self.lse, scale=self.w.scale)
+
+    def step_e2e(self):
+        from attention_attn_fwd_06_gb300 import binding as AB
+
+        for d, h in zip(self.dev, self.host):
+            d.copy_(h, non_blocking=True)
+        q, kc, vc, lens = self.dev
+        AB.attn_decode(q, kc, vc, lens, out=self.out, lse=self.lse, scale=self.w.scale)
+        self.out_h.copy_(self.out, non_blocking=True)
+        self.lse_h.copy_(self.lse, non_blocking=True)
+
+    def oracle_sample(self, budget_s):
+        """(work units done, seconds, cores, description) for the fp64 oracle on a bounded sample."""
+        return run_oracle_pool(self, budget_s)
+
+
+class PrefillCase:
+    def __init__(self, w, device):
+        import torch
+
+        from attention_attn_fwd_06_gb300.inputs import make_prefill, make_varlen
+
+        self.w = w
+        if w.kind == "varlen":
+            q, k, v, cu = make_varlen(w.B, w.Hq, w.Hkv, w.D, w.seed, seq_range=w.seq_range)
+            self.cu = cu
+            self.seqlens = [int(cu[i + 1] - cu[i]) for i in range(w.B)]
+            self.host = [t.pin_memory() for t in (q, k, v, cu)]
+            total = int(cu[-1])
+            self.out = torch.empty((total, w.Hq, w.D), dtype=torch.bfloat16, device=device)
+            self.lse = torch.empty((total, w.Hq), dtype=torch.float32, device=device)
+        else:
+            q, k, v = make_prefill(w.B, w.Hq, w.Hkv, w.L, w.L, w.D, w.seed)
+            self.seqlens = [w.L] * w.B
+            self.host = [t.pin_memory() for t in (q, k, v)]
+            odt = torch.float32 if w.out_f32 else torch.bfloat16
+            self.out = torch.empty((w.B, w.Hq, w.L, w.D), dtype=odt, device=device)
+            self.lse = torch.empty((w.B, w.Hq, w.L), dtype=torch.float32, device=device)
+        self.dev = [t.to(device) for t in self.host]
+        self.out_h = torch.empty_like(self.out, device="cpu").pin_memory()
+        self.lse_h = torch.empty_like(self.lse, device="cpu").pin_memory()
+        pairs = sum((L * (L + 1)) // 2 if w.causal else L * L for L in self.seqlens)
+        self.work = 4.0 * w.D * w.Hq * pairs
+        self.unit, self.kind = "TFLOP/s", "tensor"
+        self.launches_per_step = 1
+        self.h2d = sum(t.numel() * t.element_size() for t in self.host)
+        self.d2h = self.out.numel() * self.out.element_size() + self.lse.numel() * 4
+
+    def _call(self):
+        import torch
+
+        from attention_attn_fwd_06_gb300 import binding as AB
+
+        w = self.w
+        if w.kind == "varlen":
+            q, k, v, cu = self.dev
+            mx = max(self.seqlens)
+            AB.attn_fwd_varlen(q, k, v, cu, cu, mx, mx, out=self.out, lse=self.lse, causal=w.causal, scale=w.scale)
+        else:
+            q, k, v = self.dev
+            AB.attn_fwd(q, k, v, out=self.out, lse=self.lse, causal=w.causal, scale=w.scale,
+                        out_dtype=torch.float32 if w.out_f32 else torch.bfloat16)
+
+    def step(self):
+        self._call()
+
+    def step_e2e(self):
+        for d, h in zip(self.dev, self.host):
+            d.copy_(h, non_blocking=True)
+        self._call()
+        self.out_h.copy_(self.out, non_blocking=True)
+        self.lse_h.copy_(self.lse, non_blocking=True)
+
+    def oracle_sample(self, budget_s):
+        return run_oracle_pool(self, budget_s)
+
+
+# ----------------------------------------------------------------------------- oracle (CPU) leg
+
+def _oracle_task(args):
+    os.environ.setdefault("OMP_NUM_THREADS", "1")
+    import numpy as np
+
+    import oracle
+
+    kind, payload = args
+    t0 = time.perf_counter()
+    if kind == "decode":
+        q, kc, vc, n, scale = payload
+        oracle.attention_head(q[None, :].astype(np.float64), kc[:n].astype(np.float64), vc[:n].astype(np.float64),
+                              scale, causal=False)
+    else:
+        q, k, v, scale, causal = payload
+        oracle.attention_head(q.astype(np.float64), k.astype(np.float64), v.astype(np.float64), scale, causal)
+    return time.perf_counter() - t0
+
+
+def run_oracle_pool(case, budget_s):
+    """Time the fp64 oracle on a bounded, seeded sample of the case's rows, on all host cores.
+
+    Work units are dealt to a spawn-started process pool (one BLAS thread per
+    process) in rounds of one unit per core until ``budget_s`` seconds have
+    passed; the value counts the algorithmic work of the units finished.
+    Decode units are (b, hq) rows, each worth its share of its kv head's
+    K/V bytes plus its q, O and lse; prefill units are (sequence, head)
+    problems worth 4*D FLOPs per visible pair.
+    """
+    import multiprocessing as mp
+
+    import numpy as np
+
+    w = case.w
+    rng = np.random.default_rng(12345)
+    cores = os.cpu_count() or 1
+    units = []
+    if isinstance(case, DecodeCase):
+        q, kc, vc = (t.float().numpy() for t in case.host[:3])
+        g = w.Hq // w.Hkv
+        for b in range(w.B):
+            for h in range(w.Hq):
+                n = case.lens[b]
+                hk = h // g
+                bytes_ = n * w.D * 2 * 2 / g + w.D * 2 * 2 + 4
+                units.append((("decode", (q[b, h], kc[b, hk], vc[b, hk], n, w.scale)), bytes_))
+        what = "(b, hq) decode rows"
+    else:
+        hosts = [t.float().numpy() for t in case.host[:3]]
+        cu = case.host[3].numpy() if w.kind == "varlen" else None
+        g = w.Hq // w.Hkv
+        for a in range(w.B):
+            for h in range(w.Hq):
+                hk = h // g
+                if cu is not None:
+                    s0, s1 = int(cu[a]), int(cu[a + 1])
+                    qh, kh, vh = hosts[0][s0:s1, h], hosts[1][s0:s1, hk], hosts[2][s0:s1, hk]
+                    L = s1 - s0
+                else:
+                    qh, kh, vh = hosts[0][a, h], hosts[1][a, hk], hosts[2][a, hk]
+                    L = w.L
+                f = 4.0 * w.D * ((L * (L + 1)) // 2 if w.causal else L * L)
+                units.append((("prefill", (qh, kh, vh, w.scale, w.causal)), f))
+        what = "(sequence, head) prefill problems"
+    order = rng.permutation(len(units))
+    units = [units[i] for i in order]
+    ctx = mp.get_context("spawn")
+    saved = {k: os.environ.get(k) for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS")}
+    os.environ["OMP_NUM_THREADS"] = "1"
+    os.environ["OPENBLAS_NUM_THREADS"] = "1"
+    done, work, passes = 0, 0.0, 0
+    try:
+        with ctx.Pool(cores) as pool:
+            pool.map(_oracle_task, [units[0][0]] * cores)  # spawn + import cost stays outside the timing
+            t0 = time.perf_counter()
+            i = 0
+            while True:
+                batch = [units[(i + j) % len(units)] for j in range(cores)]
+                pool.map(_oracle_task, [u[0] for u in batch], chunksize=1)
+                i += cores
+                done += len(batch)
+                work += sum(u[1] for u in batch)
+                if time.perf_counter() - t0 >= budget_s or done >= 50 * len(units):
+                    break
+            dt = time.perf_counter() - t0
+    finally:
+        for k, v in saved.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+    desc = (f"{done} {what} (of {len(units)} in the workload; seeded order, repeating if all done), "
+            f"fp64 numpy oracle, {cores} spawn worker processes x 1 BLAS thread, {dt:.1f} s")
+    return work, dt, cores, desc
+
+
+# ----------------------------------------------------------------------------- main
+
+def make_case(name, device):
+    from attention_attn_fwd_06_gb300.inputs import WORKLOADS
+
+    w = WORKLOADS[name]
+    return DecodeCase(w, device) if w.kind == "decode" else PrefillCase(w, device)
+
+
+def workload_config(case):
+    w = case.w
+    cfg = {"workload": w.name, "kind": w.kind, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
+           "l2": "512 MB buffer written between timed steps (inputs may fit in the 129 MB L2)"}
+    if w.kind == "decode":
+        cfg.update({"Lmax": w.L, "kv_lens": "uniform [%d, %d]" % w.kv_range if w.kv_range else list(w.kv_lens),
+                    "kv_tokens_total": sum(case.lens)})
+    elif w.kind == "varlen":
+        cfg.update({"nseq": w.B, "seq_range": list(w.seq_range), "total_tokens": sum(case.seqlens),
+                    "causal": w.causal})
+    else:
+        cfg.update({"L": w.L, "causal": w.causal})
+    return cfg
+
+
+def time_steps(case, steps, warmup, flush, e2e=False):
+    import torch
+
+    fn = case.step_e2e if e2e else case.step
+    for _ in range(warmup):
+        flush.zero_()
+        fn()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    for i in range(steps):
+        flush.zero_()
+        starts[i].record(stream)
+        fn()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    t_wall1 = time.time()
+    ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    return sum(ms), ms, t_wall0, t_wall1
+
+
+_dist = None
+
+
+def barrier():
+    if _dist is not None:
+        _dist.barrier()
+
+
+def max_over_ranks(x: float) -> float:
+    if _dist is None:
+        return x
+    import torch
+
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    _dist.all_reduce(t, op=_dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_ours(args):
+    global _dist
+    import torch
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+        _dist = dist
+    device = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(device)
+
+    from attention_attn_fwd_06_gb300 import binding as AB
+
+    AB.load()
+    pk = peaks()
+    case = make_case(args.workload, device)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+
+    clocks = ClockSampler(device.index if device.index is not None else 0)
+    clocks.start()
+    time.sleep(0.2)
+    total_ms, per, tw0, tw1 = time_steps(case, args.steps, args.warmup, flush)
+    if AB.attn_get_device_status() != AB.ATTN_OK:
+        raise RuntimeError("device status reported an error during the timed steps")
+    clk = clocks.summary(tw0, tw1)
+    e2e_ms, _, _, _ = time_steps(case, max(3, args.steps // 4), 2, flush, e2e=True)
+    clocks.stop()
+
+    total_ms = max_over_ranks(total_ms)
+    e2e_ms = max_over_ranks(e2e_ms)
+    n_e2e = max(3, args.steps // 4)
+    sec_per_step = total_ms / 1e3 / args.steps
+    scale_unit = 1e9 if case.unit == "GB/s" else 1e12
+    value = world * case.work / sec_per_step / scale_unit
+    per_gpu = case.work / sec_per_step / scale_unit
+    e2e_value = world * case.work / (e2e_ms / 1e3 / n_e2e) / scale_unit
+    if case.kind == "hbm":
+        peak, peak_src = pk["hbm_gbs"], pk["source"]
+        roof = {"bound": "hbm", "achieved": per_gpu, "peak": peak, "unit": "GB/s", "frac": per_gpu / peak,
+                "traffic": read_traffic("decode_split"), "peak_source": peak_src,
+                "kernel": "decode_split_kernel + decode_combine_kernel (one attn_decode call, event-timed)"}
+    else:
+        peak, peak_src = pk["bf16_tflops"], pk["source"]
+        roof = {"bound": "tensor", "achieved": per_gpu, "peak": peak, "unit": "TFLOP/s", "frac": per_gpu / peak,
+                "traffic": read_traffic("prefill_fwd"), "peak_source": peak_src,
+                "kernel": "prefill_fwd_kernel (one attn_fwd call, event-timed)"}
+
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": case.unit,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": sec_per_step * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) rounded to bf16)",
+        "config": dict(workload_config(case), parallelism=f"replicas x{world}" if world > 1 else "single GPU"),
+        "e2e": {"value": e2e_value, "unit": case.unit, "h2d_bytes_per_step": case.h2d,
+                "d2h_bytes_per_step": case.d2h},
+        "gpu_launches": case.launches_per_step * args.steps,
+        "roofline": roof,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        work, dt, cores, desc = case.oracle_sample(args.cpu_budget)
+        line["cpu_baseline"] = {"value": work / dt / scale_unit, "unit": case.unit, "cores": cores,
+                                "kind": "oracle", "sample": desc, "seconds": dt}
+    if rank == 0 and args.also:
+        also = {}
+        for name in args.also.split(","):
+            if not name or name == args.workload:
+                continue
+            try:
+                c2 = make_case(name, device)
+                t_ms, _, _, _ = time_steps(c2, max(3, args.steps // 4), 3, flush)
+                s_step = t_ms / 1e3 / max(3, args.steps // 4)
+                su = 1e9 if c2.unit == "GB/s" else 1e12
+                v2 = c2.work / s_step / su
+                pkv = pk["hbm_gbs"] if c2.kind == "hbm" else pk["bf16_tflops"]
+                also[name] = {"value": v2, "unit": c2.unit, "ms_per_step": s_step * 1e3, "frac": v2 / pkv,
+                              "config": workload_config(c2)}
+                del c2
+            except Exception as e:  # a workload whose kernel is not built yet is reported, not fatal
+                also[name] = {"error": str(e)[:200]}
+        line["also"] = also
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if _dist is not None:
+        _dist.destroy_process_group()
+
+
+def run_reference(args):
+    """The oracle timed as it stands on the host cores (rank 0 only)."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import torch  # noqa: F401
+
+    case = make_case(args.workload, "cpu")
+    per_step = []
+    desc, cores, work = "", 0, 0.0
+    for i in range(args.warmup + args.steps):
+        work, dt, cores, desc = case.oracle_sample(args.ref_budget)
+        if i >= args.warmup:
+            per_step.append(dt)
+    scale_unit = 1e9 if case.unit == "GB/s" else 1e12
+    sec = sum(per_step) / len(per_step)
+    value = work / sec / scale_unit
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": case.unit,
+        "n_gpus": int(os.environ.get("WORLD_SIZE", "1")),
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": sec * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) rounded to bf16)",
+        "config": workload_config(case),
+        "cpu_baseline": {"value": value, "unit": case.unit, "cores": cores, "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": case.unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="decode_gqa")
+    ap.add_argument("--also", default="decode_long,prefill_causal",
+                    help="comma-separated extra workloads measured in the same run (rank 0, N=1 style)")
+    ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of host work for cpu_baseline")
+    ap.add_argument("--ref-budget", type=float, default=5.0, help="seconds of host work per reference step")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,194 @@
+/*
+ * attn.h -- C ABI of the GB300 (sm_103a) fused attention forward library.
+ *
+ * The library computes scaled-dot-product attention forward,
+ *
+ *     S = scale * Q K^T  (+ causal mask),   P = softmax(S),   O = P V,
+ *     lse = m + ln(l)    (per query row: m = max_j S, l = sum_j exp(S - m)),
+ *
+ * as defined by the standard attention chain of "GPU 学习日报 Day 24：Operator
+ * Fusion" (Operator Fusion, GPU learning diary day 24), §3.4 "Attention Fusion:
+ * FlashAttention", computed by the tiled online-softmax recurrence of the same
+ * section's second listing (running row max m, running row sum l, rescaled O
+ * accumulator, one normalisation at the end), so that the Lq x Lkv score matrix
+ * never reaches HBM.  The log-sum-exp output is not on that page; it is the
+ * natural-log normaliser built from the m and l that listing carries.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - All tensor pointers are DEVICE pointers owned by the caller.  The library
+ *    never frees or retains them.  Every pointer must be 16-byte aligned.
+ *  - Element types: q, k, v, kcache, vcache are bf16 (raw 16-bit words, passed
+ *    as void*).  out is bf16 unless an *_ex call asks for fp32.  lse is fp32.
+ *  - Arithmetic: fp32 accumulation everywhere; P is rounded to bf16 before the
+ *    P V product (tensor-core prefill path).
+ *  - Causal masking is aligned to the bottom-right corner: key j is visible to
+ *    query i iff j <= i + (Lkv - Lq).  For Lq == Lkv this is the lower
+ *    triangle.  A query row that sees no key gets O = 0 and lse = -inf.
+ *  - Grouped-query attention: Hq must be a multiple of Hkv; query head h reads
+ *    key/value head h / (Hq / Hkv) (contiguous groups).
+ *  - D (head dimension) must be 64 or 128.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are
+ *    asynchronous with respect to the host: they enqueue kernels and return.
+ *  - Errors the host can see (NULL pointer, bad size, misalignment, wrong GPU)
+ *    are returned synchronously before anything is enqueued.  A CUDA launch
+ *    failure returns ATTN_ERR_CUDA.  Problems only the device can see (a
+ *    kv_len outside [0, Lmax], a pipeline wait that timed out) are recorded in
+ *    a per-device status word read by attn_get_device_status(); the kernels
+ *    never trap.
+ *  - There is no CPU fallback: without an sm_103 device every compute call
+ *    returns ATTN_ERR_UNSUPPORTED or ATTN_ERR_CUDA.
+ */
+#ifndef ATTN_GB300_H
+#define ATTN_GB300_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum attn_status {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1,     /* NULL pointer, non-positive size, Hq % Hkv != 0, ... */
+  ATTN_ERR_UNSUPPORTED = 2,     /* D not in {64,128}, device is not sm_103, ...        */
+  ATTN_ERR_ALIGNMENT = 3,       /* a pointer is not 16-byte aligned                    */
+  ATTN_ERR_CUDA = 4,            /* a CUDA runtime call or launch failed                */
+  ATTN_ERR_DEVICE_TIMEOUT = 5,  /* device status: a bounded pipeline wait expired      */
+  ATTN_ERR_DEVICE_BOUNDS = 6    /* device status: a kv_len was outside [0, Lmax]       */
+} attn_status;
+
+typedef enum attn_dtype { ATTN_DTYPE_BF16 = 0, ATTN_DTYPE_F32 = 1 } attn_dtype;
+
+/*
+ * attn_fwd -- prefill attention over dense [batch, heads, seq_len, head_dim]
+ * tensors (the Q/K/V shape of "Что такое kernel fusion и как он применяется в
+ * LLM serving?", §2, and the chain of Operator Fusion §3.4).
+ *
+ *   q    bf16 [B, Hq,  Lq,  D]  contiguous
+ *   k    bf16 [B, Hkv, Lkv, D]  contiguous
+ *   v    bf16 [B, Hkv, Lkv, D]  contiguous
+ *   out  bf16 [B, Hq,  Lq,  D]  written
+ *   lse  fp32 [B, Hq,  Lq]      written; may be NULL (then not written)
+ *   scale   multiplies the logits (pass 1/sqrt(D) for the standard chain)
+ *   causal  0 = no mask, 1 = bottom-right-aligned causal mask
+ *
+ * Runs on the tensor cores (tcgen05 MMAs with TMEM accumulators, TMA-fed
+ * shared-memory tiles).  Returns an attn_status.
+ */
+int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
+             int B, int Hq, int Hkv, int Lq, int Lkv, int D, float scale, int causal,
+             void* stream);
+
+/*
+ * attn_fwd_params / attn_fwd_ex -- prefill with every option.
+ *
+ * Dense layout (cu_seqlens_q == NULL): as attn_fwd; Lq/Lkv are the lengths.
+ *
+ * Packed variable-length layout (cu_seqlens_q != NULL and cu_seqlens_k != NULL):
+ *   q    bf16 [total_q, Hq,  D]   (token-major, heads, head_dim)
+ *   k/v  bf16 [total_k, Hkv, D]
+ *   out       [total_q, Hq,  D]
+ *   lse  fp32 [total_q, Hq]       may be NULL
+ *   cu_seqlens_q/k  DEVICE int32 [B + 1], non-decreasing, cu[0] = 0,
+ *                   cu_q[B] == total_q, cu_k[B] == total_k; sequence s owns
+ *                   rows cu[s] .. cu[s+1]-1 and is an independent problem.
+ *   Lq, Lkv   upper bounds of the per-sequence query / key lengths.
+ *   B         number of sequences.
+ *
+ * out_dtype selects bf16 (ATTN_DTYPE_BF16) or fp32 (ATTN_DTYPE_F32) output.
+ */
+typedef struct attn_fwd_params {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* out;
+  float* lse;
+  int B, Hq, Hkv, Lq, Lkv, D;
+  float scale;
+  int causal;
+  int out_dtype;
+  const int* cu_seqlens_q;
+  const int* cu_seqlens_k;
+  int total_q, total_k;
+  void* stream;
+} attn_fwd_params;
+
+int attn_fwd_ex(const attn_fwd_params* p);
+
+/*
+ * attn_decode -- single-token decode over a KV cache ("Оптимизация Decoder
+ * Attention для LLM на GPU", section on the structure of attention in decoding
+ * mode: the new token's query against all cached keys, softmax, times V),
+ * split along the KV sequence (Flash-Decoding, Operator Fusion FAQ Q4) and
+ * merged by a log-sum-exp combine.
+ *
+ *   q        bf16 [B, Hq, D]
+ *   kcache   bf16 [B, Hkv, Lmax, D]
+ *   vcache   bf16 [B, Hkv, Lmax, D]
+ *   kv_lens  DEVICE int32 [B]; sequence b attends to cache rows 0..kv_lens[b]-1.
+ *            A value outside [0, Lmax] is clamped into it and flagged as
+ *            ATTN_ERR_DEVICE_BOUNDS in the device status word.  kv_len == 0
+ *            gives O = 0, lse = -inf.
+ *   out      bf16 [B, Hq, D]
+ *   lse      fp32 [B, Hq]  may be NULL
+ *
+ * Uses a library-owned split-KV workspace on the current device, grown on
+ * demand (see attn_release_workspace).  Two kernels are enqueued: the split
+ * pass and the combine.
+ */
+int attn_decode(const void* q, const void* kcache, const void* vcache, const int* kv_lens,
+                void* out, float* lse, int B, int Hq, int Hkv, int Lmax, int D, float scale,
+                void* stream);
+
+/*
+ * attn_decode_params / attn_decode_ex -- decode with every option.
+ *   out_dtype     ATTN_DTYPE_BF16 or ATTN_DTYPE_F32
+ *   chunk         keys per split-KV work item; 0 = choose automatically,
+ *                 otherwise a multiple of 64 in [64, 65536]
+ */
+typedef struct attn_decode_params {
+  const void* q;
+  const void* kcache;
+  const void* vcache;
+  const int* kv_lens;
+  void* out;
+  float* lse;
+  int B, Hq, Hkv, Lmax, D;
+  float scale;
+  int out_dtype;
+  int chunk;
+  void* stream;
+} attn_decode_params;
+
+int attn_decode_ex(const attn_decode_params* p);
+
+/*
+ * attn_decode_workspace_bytes -- bytes of split-KV workspace a decode call
+ * with these sizes needs (0 on invalid sizes).  chunk as in attn_decode_ex.
+ */
+unsigned long long attn_decode_workspace_bytes(int B, int Hq, int Hkv, int Lmax, int D, int chunk);
+
+/*
+ * attn_get_device_status -- synchronises `stream`, then returns and clears the
+ * current device's status word (ATTN_OK if no kernel flagged a problem since
+ * the last read).  Returns ATTN_ERR_CUDA if the synchronisation fails.
+ */
+int attn_get_device_status(void* stream);
+
+/* attn_status_string -- static, NUL-terminated name of a status code. */
+const char* attn_status_string(int status);
+
+/*
+ * attn_release_workspace -- frees the current device's split-KV workspace.
+ * The caller must ensure no decode call using it is still in flight (for
+ * example by synchronising the streams it was used on).
+ */
+void attn_release_workspace(void);
+
+/* attn_version -- library version as major*10000 + minor*100 + patch. */
+int attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_GB300_H */

@@ -1,0 +1,144 @@
+"""Host-side checks of the C ABI that need no GPU.
+
+The library must build for sm_103a, load on a machine without a GPU, export
+every entry point include/attn.h declares, and reject bad arguments with the
+documented status codes before touching the device.  A well-formed compute
+call on a machine without an sm_103 device must fail (no CPU fallback).
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from attention_attn_fwd_06_gb300 import binding as B
+from attention_attn_fwd_06_gb300.build import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build()
+    return B.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_ ]+\**\s*\**(attn_[a-z0-9_]+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_expected_entry_points():
+    assert declared_functions() == sorted(B.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    assert B.status_string(B.ATTN_OK) == "ATTN_OK"
+    assert B.status_string(B.ATTN_ERR_DEVICE_TIMEOUT) == "ATTN_ERR_DEVICE_TIMEOUT"
+    assert B.status_string(99) == "ATTN_STATUS_UNKNOWN"
+    assert lib.attn_version() >= 100
+
+
+FAKE = 1 << 20  # 16-byte aligned, never dereferenced: validation happens first
+
+
+def fwd(lib, **kw):
+    args = dict(q=FAKE, k=FAKE, v=FAKE, out=FAKE, lse=None, B=1, Hq=4, Hkv=2, Lq=8, Lkv=8, D=128,
+                scale=0.1, causal=1, stream=None)
+    args.update(kw)
+    return lib.attn_fwd(args["q"], args["k"], args["v"], args["out"], args["lse"], args["B"], args["Hq"],
+                        args["Hkv"], args["Lq"], args["Lkv"], args["D"], ctypes.c_float(args["scale"]),
+                        args["causal"], args["stream"])
+
+
+def dec(lib, **kw):
+    args = dict(q=FAKE, kc=FAKE, vc=FAKE, lens=FAKE, out=FAKE, lse=None, B=2, Hq=8, Hkv=2, Lmax=64, D=128,
+                scale=0.1, stream=None)
+    args.update(kw)
+    return lib.attn_decode(args["q"], args["kc"], args["vc"], args["lens"], args["out"], args["lse"], args["B"],
+                           args["Hq"], args["Hkv"], args["Lmax"], args["D"], ctypes.c_float(args["scale"]),
+                           args["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), B.ATTN_ERR_INVALID_ARG),
+    (dict(out=None), B.ATTN_ERR_INVALID_ARG),
+    (dict(Hq=3, Hkv=2), B.ATTN_ERR_INVALID_ARG),
+    (dict(Hkv=0), B.ATTN_ERR_INVALID_ARG),
+    (dict(B=-1), B.ATTN_ERR_INVALID_ARG),
+    (dict(Lq=-5), B.ATTN_ERR_INVALID_ARG),
+    (dict(D=96), B.ATTN_ERR_UNSUPPORTED),
+    (dict(D=256), B.ATTN_ERR_UNSUPPORTED),
+    (dict(causal=2), B.ATTN_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), B.ATTN_ERR_INVALID_ARG),
+    (dict(q=FAKE + 8), B.ATTN_ERR_ALIGNMENT),
+    (dict(out=FAKE + 2), B.ATTN_ERR_ALIGNMENT),
+    (dict(lse=FAKE + 2), B.ATTN_ERR_ALIGNMENT),
+])
+def test_fwd_validation(lib, kw, code):
+    assert fwd(lib, **kw) == code
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(kc=None), B.ATTN_ERR_INVALID_ARG),
+    (dict(lens=None), B.ATTN_ERR_INVALID_ARG),
+    (dict(Hq=6, Hkv=4), B.ATTN_ERR_INVALID_ARG),
+    (dict(Lmax=-1), B.ATTN_ERR_INVALID_ARG),
+    (dict(D=80), B.ATTN_ERR_UNSUPPORTED),
+    (dict(vc=FAKE + 4), B.ATTN_ERR_ALIGNMENT),
+    (dict(lens=FAKE + 2), B.ATTN_ERR_ALIGNMENT),
+])
+def test_decode_validation(lib, kw, code):
+    assert dec(lib, **kw) == code
+
+
+def test_varlen_validation(lib):
+    p = B.attn_fwd_params()
+    p.q = p.k = p.v = p.out = FAKE
+    p.B, p.Hq, p.Hkv, p.Lq, p.Lkv, p.D = 2, 4, 4, 16, 16, 64
+    p.scale, p.causal, p.total_q, p.total_k = 0.1, 1, 20, 20
+    p.cu_seqlens_q = FAKE
+    p.cu_seqlens_k = None  # one of the pair missing
+    assert lib.attn_fwd_ex(ctypes.byref(p)) == B.ATTN_ERR_INVALID_ARG
+    p.cu_seqlens_k = FAKE + 2
+    assert lib.attn_fwd_ex(ctypes.byref(p)) == B.ATTN_ERR_ALIGNMENT
+    p.cu_seqlens_k = FAKE
+    p.out_dtype = 7
+    assert lib.attn_fwd_ex(ctypes.byref(p)) == B.ATTN_ERR_INVALID_ARG
+
+
+def test_decode_chunk_validation(lib):
+    p = B.attn_decode_params()
+    p.q = p.kcache = p.vcache = p.kv_lens = p.out = FAKE
+    p.B, p.Hq, p.Hkv, p.Lmax, p.D, p.scale = 1, 4, 4, 128, 128, 0.1
+    p.chunk = -64
+    assert lib.attn_decode_ex(ctypes.byref(p)) == B.ATTN_ERR_INVALID_ARG
+
+
+def test_empty_inputs_are_noops(lib):
+    assert fwd(lib, B=0) == B.ATTN_OK
+    assert fwd(lib, Lq=0) == B.ATTN_OK
+    assert dec(lib, B=0) == B.ATTN_OK
+
+
+def test_no_cpu_fallback(lib):
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert fwd(lib) in (B.ATTN_ERR_UNSUPPORTED, B.ATTN_ERR_CUDA)
+    assert dec(lib) in (B.ATTN_ERR_UNSUPPORTED, B.ATTN_ERR_CUDA)
+
+
+def test_workspace_bytes_formula(lib):
+    assert lib.attn_decode_workspace_bytes(0, 8, 2, 64, 128, 0) == 0
+    assert lib.attn_decode_workspace_bytes(1, 8, 2, 64, 100, 0) == 0
+    # B*Hq*nsplit*(D+2) floats with an explicit chunk
+    assert lib.attn_decode_workspace_bytes(2, 8, 2, 1000, 128, 256) == 2 * 8 * 4 * 130 * 4
