@@ -157,14 +157,14 @@ def attention_rows(q, k, v, scale: float, causal: bool, b: int, h: int, rows):
     key, its mask row, its two-pass softmax), so checking a sample of rows of a
     large problem costs O(rows * Lkv * D).
     """
-    q, k, v = to_f64(q), to_f64(k), to_f64(v)
     Hq, Lq = q.shape[1], q.shape[2]
     Hkv, Lkv = k.shape[1], k.shape[2]
     _check_heads(Hq, Hkv)
     rows = np.asarray(rows, dtype=np.int64)
     hk = kv_head_of(h, Hq, Hkv)
     vis = visible_mask(Lq, Lkv, causal)[rows]
-    return attention_head(q[b, h, rows], k[b, hk], v[b, hk], scale, causal, visible=vis)
+    Qh = to_f64(q[b, h])[rows]  # promote only the slices this row set reads
+    return attention_head(Qh, to_f64(k[b, hk]), to_f64(v[b, hk]), scale, causal, visible=vis)
 
 
 def attention_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, scale: float, causal: bool):
@@ -195,16 +195,16 @@ def attention_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, scale: float, causal: 
 def attention_varlen_rows(q, k, v, cu_seqlens_q, cu_seqlens_k, scale: float, causal: bool,
                           seq: int, h: int, rows):
     """Selected rows (relative to the start of sequence ``seq``) of :func:`attention_varlen`."""
-    q, k, v = to_f64(q), to_f64(k), to_f64(v)
     cq = np.asarray(cu_seqlens_q, dtype=np.int64)
     ck = np.asarray(cu_seqlens_k, dtype=np.int64)
     Hq, Hkv = q.shape[1], k.shape[1]
     _check_heads(Hq, Hkv)
     rows = np.asarray(rows, dtype=np.int64)
-    qs, qe, ks, ke = cq[seq], cq[seq + 1], ck[seq], ck[seq + 1]
+    qs, qe, ks, ke = (int(x) for x in (cq[seq], cq[seq + 1], ck[seq], ck[seq + 1]))
     hk = kv_head_of(h, Hq, Hkv)
     vis = visible_mask(qe - qs, ke - ks, causal)[rows]
-    return attention_head(q[qs + rows, h], k[ks:ke, hk], v[ks:ke, hk], scale, causal, visible=vis)
+    Qh = to_f64(q[qs:qe, h])[rows]
+    return attention_head(Qh, to_f64(k[ks:ke, hk]), to_f64(v[ks:ke, hk]), scale, causal, visible=vis)
 
 
 def decode(q, kcache, vcache, kv_lens, scale: float, heads=None):
@@ -216,18 +216,20 @@ def decode(q, kcache, vcache, kv_lens, scale: float, heads=None):
     lse [B,Hq].  ``heads`` optionally restricts the work to a list of (b, hq)
     pairs; the other entries are left as NaN.
     """
-    q, kc, vc = to_f64(q), to_f64(kcache), to_f64(vcache)
+    q = to_f64(q)
     lens = np.asarray(kv_lens, dtype=np.int64)
     B, Hq, D = q.shape
-    Hkv = kc.shape[1]
+    Hkv = kcache.shape[1]
     _check_heads(Hq, Hkv)
     if heads is None:
         heads = [(b, h) for b in range(B) for h in range(Hq)]
-    O = np.full((B, Hq, vc.shape[3]), np.nan)
+    O = np.full((B, Hq, vcache.shape[3]), np.nan)
     lse = np.full((B, Hq), np.nan)
     for b, h in heads:
         n = int(lens[b])
         hk = kv_head_of(h, Hq, Hkv)
-        o, ls = attention_head(q[b, h][None, :], kc[b, hk, :n], vc[b, hk, :n], scale, causal=False)
+        # promote only the cache rows this sequence attends to
+        o, ls = attention_head(q[b, h][None, :], to_f64(kcache[b, hk, :n]), to_f64(vcache[b, hk, :n]), scale,
+                               causal=False)
         O[b, h], lse[b, h] = o[0], ls[0]
     return O, lse
