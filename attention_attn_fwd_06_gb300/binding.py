@@ -26,6 +26,7 @@ ATTN_ERR_ALIGNMENT = 3
 ATTN_ERR_CUDA = 4
 ATTN_ERR_DEVICE_TIMEOUT = 5
 ATTN_ERR_DEVICE_BOUNDS = 6
+ATTN_ERR_SCRATCH_TOO_SMALL = 7
 ATTN_DTYPE_BF16 = 0
 ATTN_DTYPE_F32 = 1
 
@@ -35,6 +36,7 @@ EXPORTED = (
     "attn_fwd_ex",
     "attn_decode",
     "attn_decode_ex",
+    "attn_decode_noalloc",
     "attn_decode_workspace_bytes",
     "attn_get_device_status",
     "attn_status_string",
@@ -95,6 +97,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.attn_decode.restype = I
         lib.attn_decode_ex.argtypes = [ctypes.POINTER(attn_decode_params)]
         lib.attn_decode_ex.restype = I
+        lib.attn_decode_noalloc.argtypes = [ctypes.POINTER(attn_decode_params)]
+        lib.attn_decode_noalloc.restype = I
         lib.attn_decode_workspace_bytes.argtypes = [I, I, I, I, I, I]
         lib.attn_decode_workspace_bytes.restype = ctypes.c_ulonglong
         lib.attn_get_device_status.argtypes = [P]
@@ -230,6 +234,43 @@ def attn_decode(q, kcache, vcache, kv_lens, out=None, lse=None, scale=None, chun
     p.chunk = int(chunk)
     p.stream = _stream_handle(stream, q.device)
     _check(load().attn_decode_ex(ctypes.byref(p)), "attn_decode")
+    return out, lse
+
+
+def attn_decode_noalloc(q, kcache, vcache, kv_lens, out, lse=None, scale=None, chunk=0, stream=None):
+    """Decode through the entry point that allocates no device memory.
+
+    For callers that cannot allocate (inside CUDA graph capture, engines that
+    hand all of HBM to their own pool, latency paths that cannot take
+    cudaMalloc's synchronisation).  ``out`` (and ``lse`` if wanted) must be
+    passed in; the split-KV partials go to a fixed 4 MiB buffer inside the
+    library, shared by every call on the device, so calls that may overlap on
+    the GPU must be ordered on one stream.  The first call on a device does a
+    one-time address lookup and should not be inside a stream capture.
+    """
+    _need(q, "q", torch.bfloat16, 3)
+    _need(kcache, "kcache", torch.bfloat16, 4)
+    _need(vcache, "vcache", torch.bfloat16, 4)
+    _need(kv_lens, "kv_lens", torch.int32, 1)
+    B, Hq, D = q.shape
+    Hkv, Lmax = kcache.shape[1], kcache.shape[2]
+    if tuple(kcache.shape) != (B, Hkv, Lmax, D) or tuple(vcache.shape) != tuple(kcache.shape):
+        raise ValueError("cache shapes do not match q")
+    if kv_lens.shape[0] != B:
+        raise ValueError("kv_lens must have B entries")
+    if out.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("out must be bf16 or fp32")
+    _need(out, "out", out.dtype, 3)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, 2)
+    p = attn_decode_params()
+    p.q, p.kcache, p.vcache, p.kv_lens, p.out, p.lse = (_ptr(t) for t in (q, kcache, vcache, kv_lens, out, lse))
+    p.B, p.Hq, p.Hkv, p.Lmax, p.D = B, Hq, Hkv, Lmax, D
+    p.scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    p.out_dtype = ATTN_DTYPE_F32 if out.dtype == torch.float32 else ATTN_DTYPE_BF16
+    p.chunk = int(chunk)
+    p.stream = _stream_handle(stream, q.device)
+    _check(load().attn_decode_noalloc(ctypes.byref(p)), "attn_decode_noalloc")
     return out, lse
 
 

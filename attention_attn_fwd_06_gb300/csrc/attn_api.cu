@@ -33,6 +33,14 @@ struct DeviceState {
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
 
+// Fixed split-KV scratch for attn_decode_noalloc: 4 MiB of fp32 partials per
+// device, part of the library's device image (no runtime allocation).
+constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;
+__device__ __align__(256) float g_noalloc_scratch[kNoAllocScratchBytes / sizeof(float)];
+// Device address of g_noalloc_scratch per device (host code cannot use the
+// symbol itself as a pointer), looked up on the first no-alloc call there.
+float* g_noalloc_ptr[kMaxDevices] = {};
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
@@ -193,6 +201,7 @@ const char* attn_status_string(int status) {
     case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA";
     case ATTN_ERR_DEVICE_TIMEOUT: return "ATTN_ERR_DEVICE_TIMEOUT";
     case ATTN_ERR_DEVICE_BOUNDS: return "ATTN_ERR_DEVICE_BOUNDS";
+    case ATTN_ERR_SCRATCH_TOO_SMALL: return "ATTN_ERR_SCRATCH_TOO_SMALL";
     default: return "ATTN_STATUS_UNKNOWN";
   }
 }
@@ -246,6 +255,59 @@ int attn_decode_ex(const attn_decode_params* p) {
   L.out_f32 = p->out_dtype == ATTN_DTYPE_F32;
   L.status = s->status;
   L.stream = stream;
+  return map_cuda(attn::launch_decode(L));
+}
+
+int attn_decode_noalloc(const attn_decode_params* p) {
+  int st = validate_decode(p);
+  if (st != ATTN_OK) return st;
+  if (p->B == 0) return ATTN_OK;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState* s = nullptr;
+  st = device_state_locked(&s);
+  if (st != ATTN_OK) return st;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return ATTN_ERR_CUDA;
+  }
+  if (g_noalloc_ptr[dev] == nullptr) {
+    // One-time set-up on this device (it is current): resolve the scratch array's device address.
+    float* ptr = nullptr;
+    if (cudaGetSymbolAddress(reinterpret_cast<void**>(&ptr), g_noalloc_scratch) != cudaSuccess || ptr == nullptr) {
+      cudaGetLastError();
+      return ATTN_ERR_CUDA;
+    }
+    g_noalloc_ptr[dev] = ptr;
+  }
+  DecodeShape sh = decode_shape(p->B, p->Hq, p->Hkv, p->Lmax, p->D, p->chunk, s->num_sms);
+  if (p->chunk == 0) {
+    // Grow the automatic chunk (fewer splits, smaller partials) until they fit.
+    while (sh.bytes > kNoAllocScratchBytes && sh.chunk < p->Lmax)
+      sh = decode_shape(p->B, p->Hq, p->Hkv, p->Lmax, p->D, sh.chunk * 2, s->num_sms);
+  }
+  if (sh.bytes > kNoAllocScratchBytes) return ATTN_ERR_SCRATCH_TOO_SMALL;
+  if (sh.nsplit > kMaxSplits) return ATTN_ERR_UNSUPPORTED;
+  attn::DecodeLaunch L;
+  L.q = p->q;
+  L.kcache = p->kcache;
+  L.vcache = p->vcache;
+  L.kv_lens = p->kv_lens;
+  L.out = p->out;
+  L.lse = p->lse;
+  L.part_o = g_noalloc_ptr[dev];
+  L.part_ml = g_noalloc_ptr[dev] + sh.part_o_elems;
+  L.B = p->B;
+  L.Hq = p->Hq;
+  L.Hkv = p->Hkv;
+  L.Lmax = p->Lmax;
+  L.D = p->D;
+  L.chunk = sh.chunk;
+  L.nsplit = sh.nsplit;
+  L.scale = p->scale;
+  L.out_f32 = p->out_dtype == ATTN_DTYPE_F32;
+  L.status = s->status;
+  L.stream = static_cast<cudaStream_t>(p->stream);
   return map_cuda(attn::launch_decode(L));
 }
 

@@ -53,7 +53,8 @@ typedef enum attn_status {
   ATTN_ERR_ALIGNMENT = 3,       /* a pointer is not 16-byte aligned                    */
   ATTN_ERR_CUDA = 4,            /* a CUDA runtime call or launch failed                */
   ATTN_ERR_DEVICE_TIMEOUT = 5,  /* device status: a bounded pipeline wait expired      */
-  ATTN_ERR_DEVICE_BOUNDS = 6    /* device status: a kv_len was outside [0, Lmax]       */
+  ATTN_ERR_DEVICE_BOUNDS = 6,   /* device status: a kv_len was outside [0, Lmax]       */
+  ATTN_ERR_SCRATCH_TOO_SMALL = 7 /* attn_decode_noalloc: partials exceed its fixed buffer */
 } attn_status;
 
 typedef enum attn_dtype { ATTN_DTYPE_BF16 = 0, ATTN_DTYPE_F32 = 1 } attn_dtype;
@@ -183,6 +184,40 @@ const char* attn_status_string(int status);
  * example by synchronising the streams it was used on).
  */
 void attn_release_workspace(void);
+
+/*
+ * attn_decode_noalloc -- attn_decode_ex for callers that must not allocate
+ * device memory.  (The source pages have no counterpart: this entry point is
+ * an integration aid, not part of the attention method.)
+ *
+ * Who needs it: code that runs while a CUDA graph is being captured (where a
+ * cudaMalloc is not allowed), serving engines that reserve nearly all of HBM
+ * up front for KV caches and route every allocation through their own pool,
+ * and latency-critical paths that cannot afford the device-wide
+ * synchronisation cudaMalloc/cudaFree can cause.  attn_decode_ex may grow its
+ * workspace with cudaMalloc on the first call with a larger problem; this
+ * call never does.
+ *
+ * Same arguments, layouts and results as attn_decode_ex.  The split-KV
+ * partials live in a fixed 4 MiB buffer compiled into the library
+ * (a file-scope __device__ array): every GPU on which the library's kernels
+ * are loaded holds that buffer until the process exits, whether or not this
+ * call is used.  The partials need B * Hq * nsplit * (D + 2) * 4 bytes, with
+ * nsplit = ceil(Lmax / chunk); with chunk == 0 the chunk is chosen as in
+ * attn_decode_ex and then doubled until the partials fit.  A problem whose
+ * partials cannot fit (even one split per row) returns
+ * ATTN_ERR_SCRATCH_TOO_SMALL before anything is enqueued.
+ *
+ * No call allocates: no cudaMalloc, no cudaFree, no allocating library
+ * routine.  The first call on a device looks up the buffer's device address
+ * (cudaGetSymbolAddress, once per device, with that device current); make
+ * that first call outside any stream capture.  The buffer needs no zeroing:
+ * every partial is written before it is read within the same call.  All calls
+ * share the one buffer and it keeps the last call's contents: two calls that
+ * can overlap on the GPU (different streams with no ordering between them)
+ * race on it and may return wrong results.  Order such calls on one stream.
+ */
+int attn_decode_noalloc(const attn_decode_params* p);
 
 /* attn_version -- library version as major*10000 + minor*100 + patch. */
 int attn_version(void);

@@ -1,0 +1,72 @@
+"""The decode entry point that allocates no device memory (attn_decode_noalloc).
+
+Some callers cannot let a library call cudaMalloc: code running under CUDA
+graph capture, serving engines that hand all of HBM to their own pool, and
+latency paths that cannot absorb cudaMalloc's synchronisation.  For them the
+library offers attn_decode_noalloc, which keeps its split-KV partials in a
+fixed buffer compiled into the library instead of a workspace it allocates.
+
+These tests call it through the C ABI and check its output against the
+regular attn_decode_ex entry point on the same inputs, for two calls in a row
+(the second call finds the buffer holding the first call's contents).  The
+file sorts last so a run that stops at the first failure has already run
+every other test.
+"""
+import ctypes
+
+import pytest
+import torch
+
+from attention_attn_fwd_06_gb300 import binding as AB
+from attention_attn_fwd_06_gb300.build import build
+from attention_attn_fwd_06_gb300.inputs import make_decode
+from tests._parity import assert_attn_close
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build()
+    return AB.load()
+
+
+def test_noalloc_symbol_exported(lib):
+    assert hasattr(lib, "attn_decode_noalloc")
+    assert AB.status_string(AB.ATTN_ERR_SCRATCH_TOO_SMALL) == "ATTN_ERR_SCRATCH_TOO_SMALL"
+
+
+def test_noalloc_rejects_problem_beyond_scratch(lib):
+    # Validation runs before the device is touched, so a bad size is refused
+    # even without a GPU: 4096 rows x 1 split x (128 + 2) floats = 2 MiB fits,
+    # 16384 rows need 8.5 MiB even with one split each.
+    p = AB.attn_decode_params()
+    fake = 1 << 20
+    p.q = p.kcache = p.vcache = p.kv_lens = p.out = fake
+    p.B, p.Hq, p.Hkv, p.Lmax, p.D, p.scale = 512, 32, 8, 64, 128, 0.088
+    rc = lib.attn_decode_noalloc(ctypes.byref(p))
+    if torch.cuda.is_available():
+        assert rc == AB.ATTN_ERR_SCRATCH_TOO_SMALL
+    else:
+        assert rc in (AB.ATTN_ERR_UNSUPPORTED, AB.ATTN_ERR_CUDA)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("B,Hq,Hkv,Lmax,D,kv_range", [
+    (8, 32, 8, 4096, 128, (512, 4096)),   # the GQA decode workload's shape
+    (3, 16, 16, 777, 64, (1, 777)),       # D = 64, MHA, ragged lengths
+])
+def test_noalloc_matches_decode_ex_twice(lib, B, Hq, Hkv, Lmax, D, kv_range):
+    dev = torch.device("cuda:0")
+    results = []
+    for call, seed in enumerate((71, 72)):  # two calls in a row with different data
+        q, kc, vc, lens = make_decode(B, Hq, Hkv, Lmax, D, seed=seed + Lmax, kv_range=kv_range)
+        q, kc, vc, lens = (t.to(dev) for t in (q, kc, vc, lens))
+        ref_o, ref_lse = AB.attn_decode(q, kc, vc, lens)
+        out = torch.empty_like(ref_o)
+        lse = torch.empty_like(ref_lse)
+        AB.attn_decode_noalloc(q, kc, vc, lens, out, lse)
+        torch.cuda.synchronize()
+        assert AB.attn_get_device_status() == AB.ATTN_OK
+        assert_attn_close(out.cpu(), lse.cpu(), ref_o.double().cpu().numpy(), ref_lse.double().cpu().numpy(),
+                          f"call {call}")
+        results.append(out.cpu())
+    assert not torch.equal(results[0], results[1])  # the second call really recomputed
