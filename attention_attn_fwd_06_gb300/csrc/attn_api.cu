@@ -173,7 +173,9 @@ int validate_fwd(const attn_fwd_params* p) {
     if (!aligned4(p->cu_seqlens_q) || !aligned4(p->cu_seqlens_k)) return ATTN_ERR_ALIGNMENT;
   }
   if (p->B == 0 || p->Lq == 0 || (varlen && p->total_q == 0)) return ATTN_OK;
-  if (p->q == nullptr || p->k == nullptr || p->v == nullptr || p->out == nullptr) return ATTN_ERR_INVALID_ARG;
+  const bool no_keys = varlen ? p->total_k == 0 : p->Lkv == 0;  // then k and v are never read
+  if (p->q == nullptr || p->out == nullptr || (!no_keys && (p->k == nullptr || p->v == nullptr)))
+    return ATTN_ERR_INVALID_ARG;
   if (!aligned16(p->q) || !aligned16(p->k) || !aligned16(p->v) || !aligned16(p->out) ||
       (p->lse != nullptr && !aligned4(p->lse)))
     return ATTN_ERR_ALIGNMENT;

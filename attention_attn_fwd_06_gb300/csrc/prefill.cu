@@ -1,6 +1,468 @@
-// prefill.cu -- placeholder until the tcgen05 prefill kernel lands.
+// prefill.cu -- fused attention forward for prefill on the 5th-generation
+// tensor cores (tcgen05 MMAs, TMEM accumulators, TMA-fed shared memory).
+//
+// What it computes: for each query tile Q_i (128 rows), the tiled online
+// softmax of "GPU 学习日报 Day 24：Operator Fusion" §3.4 (second listing):
+// stream K_j, V_j tiles on chip, S_ij = Q_i K_j^T, keep the running row max
+// m and row sum l, rescale the O accumulator, accumulate P V_j, and normalise
+// O by l once at the end, so the S matrix never reaches HBM.  The logits are
+// scaled by `scale` and causally masked (bottom-right aligned) as in the
+// standard chain of the same section; the per-row log-sum-exp is written too.
+//
+// GB300 design (one CTA per 128-row query tile, 6 warps):
+//  * warp 0 (one lane) issues TMA tile loads: Q once, then K_j and V_j into a
+//    shared-memory ring (128-byte swizzled boxes of 64 columns x 128 rows);
+//  * warp 1 owns the TMEM allocation (512 columns) and one lane issues every
+//    tcgen05.mma: S_j = Q K_j^T into one of two TMEM S buffers (fp32,
+//    128 x 128), and O += P_j V_j with P read from TMEM and V_j from shared
+//    memory (MN-major operand, no transpose pass);
+//  * warps 2-5 (128 threads) run the softmax, one thread per query row = one
+//    TMEM lane: load the S row, mask, row max, exp2 on MUFU, row sum, write P
+//    as bf16 back over the S buffer, and rescale the O row in TMEM when the
+//    running max rose by more than 8 (log2 units) -- otherwise the stale max is
+//    kept, which is exact because O and l share it;
+//  * S is double-buffered so Q K_{j+1}^T runs on the tensor cores while the
+//    softmax works on S_j; P V_j runs while the softmax starts on S_{j+1}.
+//  * Heavy (late, causal) query tiles are launched first.
+//
+// Every wait is bounded (common.cuh); on a timeout the CTA records the status,
+// drains its in-flight copies and MMAs, frees TMEM and exits.
+#include <cmath>
+
+#include "common.cuh"
 #include "kernels.h"
+#include "tcgen05.cuh"
+#include "tmap.h"
 
 namespace attn {
-cudaError_t launch_prefill(const PrefillLaunch&) { return cudaErrorNotSupported; }
+namespace {
+
+constexpr int BM = 128;  // query rows per tile (TMEM lanes)
+constexpr int BN = 128;  // keys per K/V tile
+constexpr int kThreads = 192;
+constexpr int kWarpTMA = 0;
+constexpr int kWarpMMA = 1;
+constexpr int kFirstSoftmaxWarp = 2;
+constexpr uint32_t kTmemCols = 512;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: p <= 2^8 between rescales
+
+template <int D>
+struct Cfg {
+  static constexpr int NDB = D / 64;             // 128-byte column blocks per row
+  static constexpr int TILE_BYTES = BM * D * 2;  // one Q, K or V tile (BM == BN)
+  static constexpr int BLOCK_BYTES = BM * 128;   // one 64-column block of a tile
+  static constexpr int NS = (D == 128) ? 2 : 4;  // K/V ring depth
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = OFF_Q + TILE_BYTES;
+  static constexpr int OFF_V = OFF_K + NS * TILE_BYTES;
+  static constexpr int OFF_BAR = OFF_V + NS * TILE_BYTES;
+  // barriers: q_full, k_full[NS], v_full[NS], kv_empty[NS], s_full[2], p_full[2], o_done, drain
+  static constexpr int NBAR = 1 + 3 * NS + 2 + 2 + 1 + 1;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // tmem address, abort flag
+  static constexpr int SMEM_USED = OFF_MISC + 16;
+  static constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // slack to align the base to 1024
+  static constexpr uint32_t TM_S0 = 0, TM_S1 = 128, TM_O = 256;
+  static constexpr uint32_t IDESC_S = tc::idesc_bf16_f32(BM, BN, false);
+  static constexpr uint32_t IDESC_O = tc::idesc_bf16_f32(BM, D, true);
+};
+
+struct PrefillArgs {
+  void* out;
+  float* lse;
+  const int* cu_q;
+  const int* cu_k;
+  int B, Hq, Hkv, Lq, Lkv;
+  int varlen;
+  int causal;
+  int out_f32;
+  float scale_log2;  // scale * log2(e)
+  int ntiles;        // query tiles along the (longest) sequence
+  int total_q, total_k;  // packed layout: rows of q/out and of k/v
+  unsigned* status;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                       const __grid_constant__ CUtensorMap tmv, const PrefillArgs a) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* Qs = smem + C::OFF_Q;
+  uint8_t* Ks = smem + C::OFF_K;
+  uint8_t* Vs = smem + C::OFF_V;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* q_full = bars;
+  uint64_t* k_full = bars + 1;
+  uint64_t* v_full = k_full + C::NS;
+  uint64_t* kv_empty = v_full + C::NS;
+  uint64_t* s_full = kv_empty + C::NS;
+  uint64_t* p_full = s_full + 2;
+  uint64_t* o_done = p_full + 2;
+  uint64_t* drain = o_done + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+
+  // ---------------- which tile: heavy (late) query tiles first ----------------
+  const int h = blockIdx.x;
+  const int bs = blockIdx.y;  // batch index (dense) or sequence index (packed)
+  const int tile = a.ntiles - 1 - (int)blockIdx.z;
+  const int hk = h / (a.Hq / a.Hkv);
+  int q_start = 0, k_start = 0, Lq_s = a.Lq, Lkv_s = a.Lkv;
+  if (a.varlen) {
+    q_start = a.cu_q[bs];
+    Lq_s = a.cu_q[bs + 1] - q_start;
+    k_start = a.cu_k[bs];
+    Lkv_s = a.cu_k[bs + 1] - k_start;
+    if (q_start < 0 || Lq_s < 0 || Lq_s > a.Lq || q_start + Lq_s > a.total_q || k_start < 0 || Lkv_s < 0 ||
+        k_start + Lkv_s > a.total_k) {
+      // malformed cu_seqlens: touch nothing, report it
+      if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.z == 0) record_status(a.status, ATTN_ERR_DEVICE_BOUNDS);
+      return;
+    }
+  }
+  const int q0 = tile * BM;
+  if (q0 >= Lq_s) return;  // whole CTA, before any barrier or TMEM use
+  const int off = Lkv_s - Lq_s;  // causal alignment: key j visible to row i iff j <= i + off
+  int n = 0;
+  if (Lkv_s > 0) {
+    if (a.causal) {
+      const int last_row = min(q0 + BM - 1, Lq_s - 1);
+      const int kmax = min(Lkv_s - 1, last_row + off);
+      n = (kmax < 0) ? 0 : kmax / BN + 1;
+    } else {
+      n = (Lkv_s + BN - 1) / BN;
+    }
+  }
+  // TMA coordinates: dense maps are (d, row, b*H + h); packed maps are (d, h, token)
+  const int qhead = a.varlen ? h : bs * a.Hq + h;
+  const int khead = a.varlen ? hk : bs * a.Hkv + hk;
+  const int qrow = q_start + q0;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::NBAR; ++i) mbar_init(&bars[i], (&bars[i] == &p_full[0] || &bars[i] == &p_full[1]) ? 128 : 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kWarpMMA) {
+    tc::tmem_alloc(tmem_slot, kTmemCols);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tbase = *tmem_slot;
+
+  if (warp == kWarpTMA) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      tc::tma_prefetch_desc(&tmq);
+      tc::tma_prefetch_desc(&tmk);
+      tc::tma_prefetch_desc(&tmv);
+      int issued = 0;
+      if (n > 0) {
+        mbar_arrive_expect_tx(q_full, C::TILE_BYTES);
+        for (int db = 0; db < C::NDB; ++db)
+          tc::tma_load_3d(Qs + db * C::BLOCK_BYTES, &tmq, db * 64, a.varlen ? qhead : qrow, a.varlen ? qrow : qhead,
+                          q_full);
+      }
+      for (int j = 0; j < n; ++j) {
+        const int slot = j % C::NS;
+        if (j >= C::NS && !mbar_wait(&kv_empty[slot], ((j / C::NS) - 1) & 1, a.status, abort_flag)) break;
+        const int krow = k_start + j * BN;
+        mbar_arrive_expect_tx(&k_full[slot], C::TILE_BYTES);
+        for (int db = 0; db < C::NDB; ++db)
+          tc::tma_load_3d(Ks + slot * C::TILE_BYTES + db * C::BLOCK_BYTES, &tmk, db * 64, a.varlen ? khead : krow,
+                          a.varlen ? krow : khead, &k_full[slot]);
+        mbar_arrive_expect_tx(&v_full[slot], C::TILE_BYTES);
+        for (int db = 0; db < C::NDB; ++db)
+          tc::tma_load_3d(Vs + slot * C::TILE_BYTES + db * C::BLOCK_BYTES, &tmv, db * 64, a.varlen ? khead : krow,
+                          a.varlen ? krow : khead, &v_full[slot]);
+        issued = j + 1;
+      }
+      if (*abort_flag) {  // let in-flight copies land before shared memory is released
+        if (n > 0) mbar_wait(q_full, 0, a.status, nullptr);
+        for (int j = (issued > C::NS ? issued - C::NS : 0); j < issued; ++j) {
+          mbar_wait(&k_full[j % C::NS], (j / C::NS) & 1, a.status, nullptr);
+          mbar_wait(&v_full[j % C::NS], (j / C::NS) & 1, a.status, nullptr);
+        }
+      }
+    }
+  } else if (warp == kWarpMMA) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0 && n > 0) {
+      const uint32_t q_addr = smem_u32(Qs);
+      auto issue_s = [&](int j) {
+        const int slot = j % C::NS;
+        const uint32_t k_addr = smem_u32(Ks + slot * C::TILE_BYTES);
+        const uint32_t d_tmem = tbase + ((j & 1) ? C::TM_S1 : C::TM_S0);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t koff = (kk >> 2) * C::BLOCK_BYTES + (kk & 3) * 32;
+          tc::mma_ss(d_tmem, tc::smem_desc_sw128(q_addr + koff, 16, 1024), tc::smem_desc_sw128(k_addr + koff, 16, 1024),
+                     C::IDESC_S, kk > 0);
+        }
+        tc::mma_commit(&s_full[j & 1]);
+      };
+      bool ok = mbar_wait(q_full, 0, a.status, abort_flag) && mbar_wait(&k_full[0], 0, a.status, abort_flag);
+      if (ok) {
+        tc::fence_after_sync();
+        issue_s(0);
+      }
+      for (int j = 0; ok && j < n; ++j) {
+        if (j + 1 < n) {
+          const int slot = (j + 1) % C::NS;
+          if (!mbar_wait(&k_full[slot], ((j + 1) / C::NS) & 1, a.status, abort_flag)) break;
+          tc::fence_after_sync();
+          issue_s(j + 1);
+        }
+        const int slot = j % C::NS;
+        if (!mbar_wait(&p_full[j & 1], (j >> 1) & 1, a.status, abort_flag)) break;
+        if (!mbar_wait(&v_full[slot], (j / C::NS) & 1, a.status, abort_flag)) break;
+        tc::fence_after_sync();
+        const uint32_t v_addr = smem_u32(Vs + slot * C::TILE_BYTES);
+        const uint32_t p_tmem = tbase + ((j & 1) ? C::TM_S1 : C::TM_S0);
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)
+          tc::mma_ts(tbase + C::TM_O, p_tmem + kk * 8, tc::smem_desc_sw128(v_addr + kk * 2048, C::BLOCK_BYTES, 1024),
+                     C::IDESC_O, (j > 0 || kk > 0) ? 1u : 0u);
+        tc::mma_commit(&kv_empty[slot]);
+        tc::mma_commit(o_done);
+      }
+      // Whatever happened, wait for every MMA issued above before TMEM is released.
+      tc::mma_commit(drain);
+      mbar_wait(drain, 0, a.status, nullptr);
+    }
+  } else {
+    // ---------------- softmax + correction + epilogue: one thread per query row ----------------
+    const int quarter = warp & 3;                  // TMEM lane quarter this warp may access
+    const int row = quarter * 32 + lane;           // row of the tile == TMEM lane
+    const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
+    const int qi = q0 + row;                       // query index within its sequence
+    const int horizon = qi + off;                  // last visible key under the causal mask
+    const float c = a.scale_log2;
+    float m_ref = -INFINITY;                       // running max, scaled log2 units
+    float l = 0.f;
+    bool ok = true;
+
+    for (int j = 0; j < n; ++j) {
+      const int buf = j & 1;
+      if (!mbar_wait(&s_full[buf], (j >> 1) & 1, a.status, abort_flag)) {
+        ok = false;
+        break;
+      }
+      tc::fence_after_sync();
+      const uint32_t s_addr = tbase + lane_addr + (buf ? C::TM_S1 : C::TM_S0);
+      uint32_t sr[4][32];
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) tc::tmem_ld32(s_addr + cc * 32, sr[cc]);
+      tc::tmem_ld_wait();
+
+      const int kbase = j * BN;
+      const bool need_mask = (kbase + BN > Lkv_s) || (a.causal && kbase + BN - 1 > q0 + off);
+      if (need_mask) {
+        const int lim = a.causal ? min(Lkv_s - 1, horizon) : (Lkv_s - 1);
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (kbase + cc * 32 + i > lim) sr[cc][i] = __float_as_uint(-INFINITY);
+      }
+      float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        mx0 = fmaxf(mx0, __uint_as_float(sr[0][i]));
+        mx1 = fmaxf(mx1, __uint_as_float(sr[1][i]));
+        mx2 = fmaxf(mx2, __uint_as_float(sr[2][i]));
+        mx3 = fmaxf(mx3, __uint_as_float(sr[3][i]));
+      }
+      const float mt = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c;
+      float alpha = 1.f;
+      if (mt > m_ref + kRescaleThreshold) {
+        alpha = ex2_approx(m_ref - mt);  // 0 when m_ref is still -inf
+        m_ref = mt;
+        l *= alpha;
+      }
+      const float neg = (m_ref == -INFINITY) ? 0.f : -m_ref;
+      const bool live = m_ref != -INFINITY;
+      float rs0 = 0.f, rs1 = 0.f;
+      uint32_t pk[2][32];
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          float p0 = ex2_approx(fmaf(__uint_as_float(sr[cc][2 * i]), c, neg));
+          float p1 = ex2_approx(fmaf(__uint_as_float(sr[cc][2 * i + 1]), c, neg));
+          if (!live) p0 = p1 = 0.f;
+          rs0 += p0;
+          rs1 += p1;
+          pk[cc >> 1][(cc & 1) * 16 + i] = tc::pack_bf16x2(p0, p1);
+        }
+      }
+      l += rs0 + rs1;
+      // P_j (bf16) overwrites the first 64 columns of this S buffer
+      tc::tmem_st32(s_addr, pk[0]);
+      tc::tmem_st32(s_addr + 32, pk[1]);
+      tc::tmem_st_wait();
+
+      if (j > 0) {
+        // O may be touched only once P_{j-1} V_{j-1} has completed
+        if (!mbar_wait(o_done, (j - 1) & 1, a.status, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc::fence_after_sync();
+        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+          const uint32_t o_addr = tbase + lane_addr + C::TM_O;
+#pragma unroll
+          for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t orr[32];
+            tc::tmem_ld32(o_addr + cc * 32, orr);
+            tc::tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
+            tc::tmem_st32(o_addr + cc * 32, orr);
+          }
+          tc::tmem_st_wait();
+        }
+      }
+      tc::fence_before_sync();
+      mbar_arrive(&p_full[buf]);
+    }
+
+    // ---------------- epilogue: O / l, lse ----------------
+    if (ok && n > 0) {
+      ok = mbar_wait(o_done, (n - 1) & 1, a.status, abort_flag);
+      tc::fence_after_sync();
+    }
+    const bool store = qi < Lq_s;
+    const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+    size_t orow;  // element offset of this row in out
+    if (a.varlen)
+      orow = ((size_t)(q_start + qi) * a.Hq + h) * D;
+    else
+      orow = (((size_t)bs * a.Hq + h) * a.Lq + qi) * D;
+    if (ok) {
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t orr[32];
+        if (n > 0) {
+          tc::tmem_ld32(tbase + lane_addr + C::TM_O + cc * 32, orr);
+          tc::tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) orr[i] = 0u;
+        }
+        if (store) {
+          if (a.out_f32) {
+            float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(a.out) + orow + cc * 32);
+#pragma unroll
+            for (int v4 = 0; v4 < 8; ++v4)
+              dst[v4] = make_float4(__uint_as_float(orr[4 * v4]) * inv_l, __uint_as_float(orr[4 * v4 + 1]) * inv_l,
+                                    __uint_as_float(orr[4 * v4 + 2]) * inv_l, __uint_as_float(orr[4 * v4 + 3]) * inv_l);
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.out) + orow + cc * 32);
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4) {
+              uint4 w;
+              w.x = tc::pack_bf16x2(__uint_as_float(orr[8 * v4 + 0]) * inv_l, __uint_as_float(orr[8 * v4 + 1]) * inv_l);
+              w.y = tc::pack_bf16x2(__uint_as_float(orr[8 * v4 + 2]) * inv_l, __uint_as_float(orr[8 * v4 + 3]) * inv_l);
+              w.z = tc::pack_bf16x2(__uint_as_float(orr[8 * v4 + 4]) * inv_l, __uint_as_float(orr[8 * v4 + 5]) * inv_l);
+              w.w = tc::pack_bf16x2(__uint_as_float(orr[8 * v4 + 6]) * inv_l, __uint_as_float(orr[8 * v4 + 7]) * inv_l);
+              dst[v4] = w;
+            }
+          }
+        }
+      }
+      if (store && a.lse != nullptr) {
+        const float lse = (l > 0.f) ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
+        if (a.varlen)
+          a.lse[(size_t)(q_start + qi) * a.Hq + h] = lse;
+        else
+          a.lse[((size_t)bs * a.Hq + h) * a.Lq + qi] = lse;
+      }
+    }
+  }
+
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == kWarpMMA) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tbase, kTmemCols);
+  }
+}
+
+template <int D>
+cudaError_t launch_d(const PrefillLaunch& p) {
+  using C = Cfg<D>;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!attr_set[dev]) {
+    e = cudaFuncSetAttribute(prefill_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  const bool varlen = p.cu_q != nullptr;
+  CUtensorMap tmq, tmk, tmv;
+  const uint64_t row_b = (uint64_t)D * 2;
+  bool ok;
+  if (!varlen) {
+    // (d, row, b*H + h): rows of one head are contiguous
+    const uint64_t Lk = p.Lkv > 0 ? (uint64_t)p.Lkv : 1;
+    const void* kb = p.Lkv > 0 ? p.k : p.q;  // Lkv == 0: never read, any valid map
+    const void* vb = p.Lkv > 0 ? p.v : p.q;
+    ok = make_tmap_bf16_3d(&tmq, p.q, D, p.Lq, (uint64_t)p.B * p.Hq, row_b, row_b * p.Lq, 64, BM, 1) &&
+         make_tmap_bf16_3d(&tmk, kb, D, Lk, (uint64_t)p.B * p.Hkv, row_b, row_b * Lk, 64, BN, 1) &&
+         make_tmap_bf16_3d(&tmv, vb, D, Lk, (uint64_t)p.B * p.Hkv, row_b, row_b * Lk, 64, BN, 1);
+  } else {
+    // (d, h, token): one box = 128 consecutive tokens of one head
+    const uint64_t tk = p.total_k > 0 ? (uint64_t)p.total_k : 1;
+    const void* kb = p.total_k > 0 ? p.k : p.q;
+    const void* vb = p.total_k > 0 ? p.v : p.q;
+    const uint64_t hk = p.total_k > 0 ? (uint64_t)p.Hkv : 1;
+    ok = make_tmap_bf16_3d(&tmq, p.q, D, p.Hq, p.total_q, row_b, row_b * p.Hq, 64, 1, BM) &&
+         make_tmap_bf16_3d(&tmk, kb, D, hk, tk, row_b, row_b * hk, 64, 1, BN) &&
+         make_tmap_bf16_3d(&tmv, vb, D, hk, tk, row_b, row_b * hk, 64, 1, BN);
+  }
+  if (!ok) return cudaErrorInvalidValue;
+  PrefillArgs a;
+  a.out = p.out;
+  a.lse = p.lse;
+  a.cu_q = p.cu_q;
+  a.cu_k = p.cu_k;
+  a.B = p.B;
+  a.Hq = p.Hq;
+  a.Hkv = p.Hkv;
+  a.Lq = p.Lq;
+  a.Lkv = p.Lkv;
+  a.varlen = varlen ? 1 : 0;
+  a.causal = p.causal;
+  a.out_f32 = p.out_f32;
+  a.scale_log2 = p.scale * kLog2e;
+  a.ntiles = (p.Lq + BM - 1) / BM;
+  a.total_q = p.total_q;
+  a.total_k = p.total_k;
+  a.status = p.status;
+  if (a.ntiles > 65535) return cudaErrorInvalidValue;
+  dim3 grid(p.Hq, p.B, a.ntiles);
+  prefill_fwd_kernel<D><<<grid, kThreads, C::SMEM_ALLOC, p.stream>>>(tmq, tmk, tmv, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prefill(const PrefillLaunch& p) {
+  if (p.D == 64) return launch_d<64>(p);
+  if (p.D == 128) return launch_d<128>(p);
+  return cudaErrorNotSupported;
+}
+
 }  // namespace attn

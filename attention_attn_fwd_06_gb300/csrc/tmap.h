@@ -30,15 +30,16 @@ inline EncodeTiledFn encode_tiled_fn() {
 }
 
 // 3-D bf16 tensor map: extents (e0 innermost, e1, e2) in elements, byte strides
-// of dims 1 and 2 (multiples of 16), box (b0, b1, 1), 128-byte swizzle,
+// of dims 1 and 2 (multiples of 16), box (b0, b1, b2), 128-byte swizzle,
 // out-of-bounds elements read as zero.  Returns false on failure.
 inline bool make_tmap_bf16_3d(CUtensorMap* map, const void* base, uint64_t e0, uint64_t e1, uint64_t e2,
-                              uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t b0, uint32_t b1) {
+                              uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t b0, uint32_t b1,
+                              uint32_t b2 = 1) {
   EncodeTiledFn fn = encode_tiled_fn();
   if (fn == nullptr) return false;
   const cuuint64_t dims[3] = {e0, e1, e2};
   const cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
-  const cuuint32_t box[3] = {b0, b1, 1};
+  const cuuint32_t box[3] = {b0, b1, b2};
   const cuuint32_t elem_strides[3] = {1, 1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
                   elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
