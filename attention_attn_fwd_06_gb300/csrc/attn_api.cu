@@ -19,7 +19,9 @@ __device__ unsigned g_attn_device_status;
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr int kMaxSplits = 12288;
+// Decode workspace layout: [counters: kDecodeCounterSlots x u32][part_o][part_ml].
+// The counter area must be zero before the first call; the kernel leaves it zero.
+constexpr size_t kCounterBytes = size_t(attn::kDecodeCounterSlots) * sizeof(unsigned);
 
 struct DeviceState {
   bool probed = false;
@@ -100,42 +102,40 @@ int ensure_workspace_locked(DeviceState& s, size_t bytes, cudaStream_t stream) {
     s.ws = nullptr;
     return ATTN_ERR_CUDA;
   }
+  if (cudaMemset(s.ws, 0, kCounterBytes) != cudaSuccess) {  // counters start at zero
+    cudaGetLastError();
+    cudaFree(s.ws);
+    s.ws = nullptr;
+    return ATTN_ERR_CUDA;
+  }
   s.ws_bytes = bytes;
   return ATTN_OK;
 }
 
 struct DecodeShape {
-  int chunk = 0;
-  int nsplit = 0;
-  size_t part_o_elems = 0;
-  size_t part_ml_elems = 0;
-  size_t bytes = 0;
+  int grid = 0;               // CTAs of the persistent launch
+  size_t part_o_elems = 0;    // 2 * grid * GP * D
+  size_t part_ml_elems = 0;   // 2 * grid * GP * 2
+  size_t bytes = 0;           // counters + partials
 };
 
-// Keys per split: aim for about 8 CTAs per SM at the cache's full length, in
-// whole pipeline stages.  The real lengths live on the device, so this is an
-// upper-bound estimate.
-int auto_chunk(int B, int Hq, int Hkv, int Lmax, int D, int num_sms) {
-  const int sk = attn::decode_stage_keys(D);
-  const int group = Hq / Hkv;
-  const long long rows = (long long)B * Hkv * (group / attn::decode_heads_per_cta(group));
-  const long long target = (long long)(num_sms > 0 ? num_sms : 148) * 8;
-  long long chunk = (rows * (long long)Lmax + target - 1) / target;
-  chunk = ((chunk + sk - 1) / sk) * sk;
-  if (chunk < sk) chunk = sk;
-  if (chunk > 64LL * sk) chunk = 64LL * sk;
-  return (int)chunk;
+// The stream-K split gives every CTA an equal slice of the key space and each
+// CTA at most two partial rows, so the partial area depends on the grid, the
+// heads per CTA and D -- not on the batch or the cache length.
+DecodeShape decode_shape(int Hq, int Hkv, int D, int num_sms) {
+  DecodeShape s;
+  const int gp = attn::decode_heads_per_cta(Hq / Hkv);
+  s.grid = attn::decode_grid(num_sms);
+  s.part_o_elems = (size_t)2 * s.grid * gp * D;
+  s.part_ml_elems = (size_t)2 * s.grid * gp * 2;
+  s.bytes = kCounterBytes + (s.part_o_elems + s.part_ml_elems) * sizeof(float);
+  return s;
 }
 
-DecodeShape decode_shape(int B, int Hq, int Hkv, int Lmax, int D, int chunk, int num_sms) {
-  DecodeShape s;
-  s.chunk = chunk > 0 ? chunk : auto_chunk(B, Hq, Hkv, Lmax, D, num_sms);
-  s.nsplit = Lmax > 0 ? (Lmax + s.chunk - 1) / s.chunk : 1;
-  const size_t rows = (size_t)B * Hq * s.nsplit;
-  s.part_o_elems = rows * D;
-  s.part_ml_elems = rows * 2;
-  s.bytes = (s.part_o_elems + s.part_ml_elems) * sizeof(float);
-  return s;
+// Rows of per-row counters the decode kernel uses for these sizes.
+long long decode_counter_rows(int B, int Hq, int Hkv) {
+  const int group = Hq / Hkv;
+  return (long long)B * Hkv * (group / attn::decode_heads_per_cta(group));
 }
 
 int validate_decode(const attn_decode_params* p) {
@@ -215,13 +215,14 @@ unsigned long long attn_decode_workspace_bytes(int B, int Hq, int Hkv, int Lmax,
   p.kv_lens = reinterpret_cast<const int*>(16);
   p.out = reinterpret_cast<void*>(16);
   if (validate_decode(&p) != ATTN_OK || B == 0) return 0;
+  if (2 + decode_counter_rows(B, Hq, Hkv) > attn::kDecodeCounterSlots) return 0;
   int sms = 0;
   {
     std::lock_guard<std::mutex> lock(g_mu);
     DeviceState* s = nullptr;
     if (device_state_locked(&s) == ATTN_OK) sms = s->num_sms;
   }
-  return decode_shape(B, Hq, Hkv, Lmax, D, chunk, sms).bytes;
+  return decode_shape(Hq, Hkv, D, sms).bytes;
 }
 
 int attn_decode_ex(const attn_decode_params* p) {
@@ -233,8 +234,8 @@ int attn_decode_ex(const attn_decode_params* p) {
   DeviceState* s = nullptr;
   st = device_state_locked(&s);
   if (st != ATTN_OK) return st;
-  const DecodeShape sh = decode_shape(p->B, p->Hq, p->Hkv, p->Lmax, p->D, p->chunk, s->num_sms);
-  if (sh.nsplit > kMaxSplits) return ATTN_ERR_UNSUPPORTED;  // combine keeps one weight per split in smem
+  if (2 + decode_counter_rows(p->B, p->Hq, p->Hkv) > attn::kDecodeCounterSlots) return ATTN_ERR_UNSUPPORTED;
+  const DecodeShape sh = decode_shape(p->Hq, p->Hkv, p->D, s->num_sms);
   st = ensure_workspace_locked(*s, sh.bytes, stream);
   if (st != ATTN_OK) return st;
   attn::DecodeLaunch L;
@@ -244,20 +245,20 @@ int attn_decode_ex(const attn_decode_params* p) {
   L.kv_lens = p->kv_lens;
   L.out = p->out;
   L.lse = p->lse;
-  L.part_o = static_cast<float*>(s->ws);
-  L.part_ml = static_cast<float*>(s->ws) + sh.part_o_elems;
+  L.counters = static_cast<unsigned*>(s->ws);
+  L.part_o = reinterpret_cast<float*>(static_cast<char*>(s->ws) + kCounterBytes);
+  L.part_ml = L.part_o + sh.part_o_elems;
   L.B = p->B;
   L.Hq = p->Hq;
   L.Hkv = p->Hkv;
   L.Lmax = p->Lmax;
   L.D = p->D;
-  L.chunk = sh.chunk;
-  L.nsplit = sh.nsplit;
+  L.min_keys = p->chunk > 0 ? p->chunk : 64;
   L.scale = p->scale;
   L.out_f32 = p->out_dtype == ATTN_DTYPE_F32;
   L.status = s->status;
   L.stream = stream;
-  return map_cuda(attn::launch_decode(L));
+  return map_cuda(attn::launch_decode(L, s->num_sms));
 }
 
 int attn_decode_noalloc(const attn_decode_params* p) {
@@ -280,16 +281,16 @@ int attn_decode_noalloc(const attn_decode_params* p) {
       cudaGetLastError();
       return ATTN_ERR_CUDA;
     }
+    // Its counter area must start at zero; the kernel keeps it zero afterwards.
+    if (cudaMemset(ptr, 0, kCounterBytes) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+      cudaGetLastError();
+      return ATTN_ERR_CUDA;
+    }
     g_noalloc_ptr[dev] = ptr;
   }
-  DecodeShape sh = decode_shape(p->B, p->Hq, p->Hkv, p->Lmax, p->D, p->chunk, s->num_sms);
-  if (p->chunk == 0) {
-    // Grow the automatic chunk (fewer splits, smaller partials) until they fit.
-    while (sh.bytes > kNoAllocScratchBytes && sh.chunk < p->Lmax)
-      sh = decode_shape(p->B, p->Hq, p->Hkv, p->Lmax, p->D, sh.chunk * 2, s->num_sms);
-  }
-  if (sh.bytes > kNoAllocScratchBytes) return ATTN_ERR_SCRATCH_TOO_SMALL;
-  if (sh.nsplit > kMaxSplits) return ATTN_ERR_UNSUPPORTED;
+  const DecodeShape sh = decode_shape(p->Hq, p->Hkv, p->D, s->num_sms);
+  if (2 + decode_counter_rows(p->B, p->Hq, p->Hkv) > attn::kDecodeCounterSlots || sh.bytes > kNoAllocScratchBytes)
+    return ATTN_ERR_SCRATCH_TOO_SMALL;
   attn::DecodeLaunch L;
   L.q = p->q;
   L.kcache = p->kcache;
@@ -297,20 +298,20 @@ int attn_decode_noalloc(const attn_decode_params* p) {
   L.kv_lens = p->kv_lens;
   L.out = p->out;
   L.lse = p->lse;
-  L.part_o = g_noalloc_ptr[dev];
-  L.part_ml = g_noalloc_ptr[dev] + sh.part_o_elems;
+  L.counters = reinterpret_cast<unsigned*>(g_noalloc_ptr[dev]);
+  L.part_o = g_noalloc_ptr[dev] + kCounterBytes / sizeof(float);
+  L.part_ml = L.part_o + sh.part_o_elems;
   L.B = p->B;
   L.Hq = p->Hq;
   L.Hkv = p->Hkv;
   L.Lmax = p->Lmax;
   L.D = p->D;
-  L.chunk = sh.chunk;
-  L.nsplit = sh.nsplit;
+  L.min_keys = p->chunk > 0 ? p->chunk : 64;
   L.scale = p->scale;
   L.out_f32 = p->out_dtype == ATTN_DTYPE_F32;
   L.status = s->status;
   L.stream = static_cast<cudaStream_t>(p->stream);
-  return map_cuda(attn::launch_decode(L));
+  return map_cuda(attn::launch_decode(L, s->num_sms));
 }
 
 int attn_decode(const void* q, const void* kcache, const void* vcache, const int* kv_lens, void* out, float* lse,
@@ -403,6 +404,15 @@ int attn_get_device_status(void* stream) {
   if (cudaMemcpy(&v, s->status, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return ATTN_ERR_CUDA;
   const unsigned zero = 0;
   if (cudaMemcpy(s->status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (v == ATTN_ERR_DEVICE_TIMEOUT) {
+    // A decode that gave up part-way may have left its work counters armed: clear them.
+    int dev = -1;
+    cudaGetDevice(&dev);
+    if (s->ws != nullptr) cudaMemset(s->ws, 0, kCounterBytes);
+    if (dev >= 0 && dev < kMaxDevices && g_noalloc_ptr[dev] != nullptr) cudaMemset(g_noalloc_ptr[dev], 0, kCounterBytes);
+    cudaDeviceSynchronize();
+    cudaGetLastError();
+  }
   return static_cast<int>(v);
 }
 

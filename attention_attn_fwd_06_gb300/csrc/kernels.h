@@ -14,22 +14,27 @@ struct DecodeLaunch {
   const int* kv_lens;   // int32 [B] (device)
   void* out;            // [B, Hq, D], bf16 or fp32
   float* lse;           // fp32 [B, Hq] or null
-  float* part_o;        // fp32 [B, Hq, nsplit, D]
-  float* part_ml;       // fp32 [B, Hq, nsplit, 2]  (m in log2 units, l)
+  float* part_o;        // fp32 [2 * grid][GP][D]   partial O per (CTA slot, head of the group)
+  float* part_ml;       // fp32 [2 * grid][GP][2]   (m in log2 units, l)
+  unsigned* counters;   // [2 + row]: partials landed per (b, kv head, head group) row; zero between calls
   int B, Hq, Hkv, Lmax, D;
-  int chunk;            // keys per split (multiple of the stage size)
-  int nsplit;           // ceil(Lmax / chunk)
+  int min_keys;         // smallest slice of the key space one CTA takes (>= 1)
   float scale;
   int out_f32;
   unsigned* status;     // device status word
   cudaStream_t stream;
 };
 
-// Keys per pipeline stage of the split pass (chunk must be a multiple of it).
+// Keys per pipeline stage of the split pass.
 int decode_stage_keys(int D);
-// Number of query heads one split CTA serves (the largest of 8, 4, 2, 1 dividing Hq / Hkv).
+// CTAs of the persistent decode launch (two per SM); the partial slots number 2 * grid.
+int decode_grid(int num_sms);
+// Number of query heads one decode CTA serves (the largest of 8, 4, 2, 1 dividing Hq / Hkv).
 int decode_heads_per_cta(int group);
-cudaError_t launch_decode(const DecodeLaunch& p);
+// Counter slots the decode kernel may use: 2 + B * Hkv * (Hq / Hkv / heads_per_cta) must fit.
+constexpr int kDecodeCounterSlots = 65536;
+// One persistent launch (two CTAs per SM) that also merges the split partials.
+cudaError_t launch_decode(const DecodeLaunch& p, int num_sms);
 
 // Prefill (tcgen05 tensor-core path).
 struct PrefillLaunch {

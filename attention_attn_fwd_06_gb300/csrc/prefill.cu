@@ -23,7 +23,8 @@
 //    kept, which is exact because O and l share it;
 //  * S is double-buffered so Q K_{j+1}^T runs on the tensor cores while the
 //    softmax works on S_j; P V_j runs while the softmax starts on S_{j+1}.
-//  * Heavy (late, causal) query tiles are launched first.
+//  * The query tiles of one head launch together (K/V reuse in L2), heaviest
+//    (latest, causal) first.
 //
 // Every wait is bounded (common.cuh); on a timeout the CTA records the status,
 // drains its in-flight copies and MMAs, frees TMEM and exits.
@@ -39,7 +40,8 @@ namespace {
 
 constexpr int BM = 128;  // query rows per tile (TMEM lanes)
 constexpr int BN = 128;  // keys per K/V tile
-constexpr int kThreads = 192;
+constexpr int NQ = 2;    // query tiles per CTA (ping-pong)
+constexpr int kThreads = 32 * (2 + 4 * NQ);  // TMA warp, MMA warp, one 4-warp softmax group per query tile
 constexpr int kWarpTMA = 0;
 constexpr int kWarpMMA = 1;
 constexpr int kFirstSoftmaxWarp = 2;
@@ -54,16 +56,20 @@ struct Cfg {
   static constexpr int TILE_BYTES = BM * D * 2;  // one Q, K or V tile (BM == BN)
   static constexpr int BLOCK_BYTES = BM * 128;   // one 64-column block of a tile
   static constexpr int NS = (D == 128) ? 2 : 4;  // K/V ring depth
-  static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + TILE_BYTES;
+  static constexpr int OFF_Q = 0;                // NQ query tiles
+  static constexpr int OFF_K = OFF_Q + NQ * TILE_BYTES;
   static constexpr int OFF_V = OFF_K + NS * TILE_BYTES;
   static constexpr int OFF_BAR = OFF_V + NS * TILE_BYTES;
-  // barriers: q_full, k_full[NS], v_full[NS], kv_empty[NS], s_full[2], p_full[2], o_done, drain
-  static constexpr int NBAR = 1 + 3 * NS + 2 + 2 + 1 + 1;
+  // barriers: q_full, k_full[NS], v_full[NS], kv_empty[NS], s_full[NQ], p_full[NQ], o_done[NQ], drain
+  static constexpr int NBAR = 1 + 3 * NS + 3 * NQ + 1;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // tmem address, abort flag
   static constexpr int SMEM_USED = OFF_MISC + 16;
   static constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // slack to align the base to 1024
-  static constexpr uint32_t TM_S0 = 0, TM_S1 = 128, TM_O = 256;
+  static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory");
+  // TMEM columns: S_t (fp32 128 x 128, P_t bf16 aliased in its first 64 columns), O_t (fp32 128 x D)
+  static constexpr uint32_t tm_s(int t) { return (uint32_t)(t * BN); }
+  static constexpr uint32_t tm_o(int t) { return (uint32_t)(NQ * BN + t * D); }
+  static_assert(NQ * BN + NQ * D <= (int)kTmemCols, "TMEM columns");
   static constexpr uint32_t IDESC_S = tc::idesc_bf16_f32(BM, BN, false);
   static constexpr uint32_t IDESC_O = tc::idesc_bf16_f32(BM, D, true);
 };
@@ -78,7 +84,7 @@ struct PrefillArgs {
   int causal;
   int out_f32;
   float scale_log2;  // scale * log2(e)
-  int ntiles;        // query tiles along the (longest) sequence
+  int npairs;        // CTAs along the (longest) sequence: NQ query tiles each
   int total_q, total_k;  // packed layout: rows of q/out and of k/v
   unsigned* status;
 };
@@ -99,16 +105,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* v_full = k_full + C::NS;
   uint64_t* kv_empty = v_full + C::NS;
   uint64_t* s_full = kv_empty + C::NS;
-  uint64_t* p_full = s_full + 2;
-  uint64_t* o_done = p_full + 2;
-  uint64_t* drain = o_done + 1;
+  uint64_t* p_full = s_full + NQ;
+  uint64_t* o_done = p_full + NQ;
+  uint64_t* drain = o_done + NQ;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
-  // ---------------- which tile: heavy (late) query tiles first ----------------
-  const int h = blockIdx.x;
-  const int bs = blockIdx.y;  // batch index (dense) or sequence index (packed)
-  const int tile = a.ntiles - 1 - (int)blockIdx.z;
+  // ---------------- which tiles ----------------
+  // Launch order: the query tiles of one head are adjacent (so the ~150 CTAs in
+  // flight touch ~10 heads and K/V are served from L2), heaviest (latest,
+  // causal) tiles first within the head.
+  const int pair = a.npairs - 1 - (int)blockIdx.x;
+  const int h = blockIdx.y;
+  const int bs = blockIdx.z;  // batch index (dense) or sequence index (packed)
   const int hk = h / (a.Hq / a.Hkv);
   int q_start = 0, k_start = 0, Lq_s = a.Lq, Lkv_s = a.Lkv;
   if (a.varlen) {
@@ -119,33 +128,45 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (q_start < 0 || Lq_s < 0 || Lq_s > a.Lq || q_start + Lq_s > a.total_q || k_start < 0 || Lkv_s < 0 ||
         k_start + Lkv_s > a.total_k) {
       // malformed cu_seqlens: touch nothing, report it
-      if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.z == 0) record_status(a.status, ATTN_ERR_DEVICE_BOUNDS);
+      if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) record_status(a.status, ATTN_ERR_DEVICE_BOUNDS);
       return;
     }
   }
-  const int q0 = tile * BM;
-  if (q0 >= Lq_s) return;  // whole CTA, before any barrier or TMEM use
-  const int off = Lkv_s - Lq_s;  // causal alignment: key j visible to row i iff j <= i + off
-  int n = 0;
-  if (Lkv_s > 0) {
-    if (a.causal) {
-      const int last_row = min(q0 + BM - 1, Lq_s - 1);
-      const int kmax = min(Lkv_s - 1, last_row + off);
-      n = (kmax < 0) ? 0 : kmax / BN + 1;
-    } else {
-      n = (Lkv_s + BN - 1) / BN;
+  const int q00 = pair * NQ * BM;  // first row of the CTA's first tile
+  if (q00 >= Lq_s) return;         // whole CTA, before any barrier or TMEM use
+  const int off = Lkv_s - Lq_s;    // causal alignment: key j visible to row i iff j <= i + off
+  // K/V tiles each query tile needs (0 when the tile is past the end or sees no key)
+  int nt[NQ];
+#pragma unroll
+  for (int t = 0; t < NQ; ++t) {
+    const int q0 = q00 + t * BM;
+    int n = 0;
+    if (q0 < Lq_s && Lkv_s > 0) {
+      if (a.causal) {
+        const int last_row = min(q0 + BM - 1, Lq_s - 1);
+        const int kmax = min(Lkv_s - 1, last_row + off);
+        n = (kmax < 0) ? 0 : kmax / BN + 1;
+      } else {
+        n = (Lkv_s + BN - 1) / BN;
+      }
     }
+    nt[t] = n;
   }
+  int n = 0;
+#pragma unroll
+  for (int t = 0; t < NQ; ++t) n = max(n, nt[t]);
   // TMA coordinates: dense maps are (d, row, b*H + h); packed maps are (d, h, token)
   const int qhead = a.varlen ? h : bs * a.Hq + h;
   const int khead = a.varlen ? hk : bs * a.Hkv + hk;
-  const int qrow = q_start + q0;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < C::NBAR; ++i) mbar_init(&bars[i], (&bars[i] == &p_full[0] || &bars[i] == &p_full[1]) ? 128 : 1);
+    for (int i = 0; i < C::NBAR; ++i) {
+      const bool is_p = (&bars[i] >= p_full) && (&bars[i] < p_full + NQ);
+      mbar_init(&bars[i], is_p ? 128 : 1);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -166,10 +187,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::tma_prefetch_desc(&tmv);
       int issued = 0;
       if (n > 0) {
-        mbar_arrive_expect_tx(q_full, C::TILE_BYTES);
-        for (int db = 0; db < C::NDB; ++db)
-          tc::tma_load_3d(Qs + db * C::BLOCK_BYTES, &tmq, db * 64, a.varlen ? qhead : qrow, a.varlen ? qrow : qhead,
-                          q_full);
+        uint32_t qbytes = 0;
+#pragma unroll
+        for (int t = 0; t < NQ; ++t) qbytes += nt[t] > 0 ? C::TILE_BYTES : 0;
+        mbar_arrive_expect_tx(q_full, qbytes);
+#pragma unroll
+        for (int t = 0; t < NQ; ++t) {
+          if (nt[t] == 0) continue;
+          const int qrow = q_start + q00 + t * BM;
+          for (int db = 0; db < C::NDB; ++db)
+            tc::tma_load_3d(Qs + t * C::TILE_BYTES + db * C::BLOCK_BYTES, &tmq, db * 64, a.varlen ? qhead : qrow,
+                            a.varlen ? qrow : qhead, q_full);
+        }
       }
       for (int j = 0; j < n; ++j) {
         const int slot = j % C::NS;
@@ -194,45 +223,59 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == kWarpMMA) {
-    // ---------------- MMA issuer ----------------
+    // ---------------- MMA issuer: S_A, S_B, then per step PV_A, S_A', PV_B, S_B' ----------------
     if (lane == 0 && n > 0) {
-      const uint32_t q_addr = smem_u32(Qs);
-      auto issue_s = [&](int j) {
-        const int slot = j % C::NS;
-        const uint32_t k_addr = smem_u32(Ks + slot * C::TILE_BYTES);
-        const uint32_t d_tmem = tbase + ((j & 1) ? C::TM_S1 : C::TM_S0);
+      auto issue_s = [&](int t, int j) {
+        const uint32_t q_addr = smem_u32(Qs + t * C::TILE_BYTES);
+        const uint32_t k_addr = smem_u32(Ks + (j % C::NS) * C::TILE_BYTES);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t koff = (kk >> 2) * C::BLOCK_BYTES + (kk & 3) * 32;
-          tc::mma_ss(d_tmem, tc::smem_desc_sw128(q_addr + koff, 16, 1024), tc::smem_desc_sw128(k_addr + koff, 16, 1024),
-                     C::IDESC_S, kk > 0);
+          tc::mma_ss(tbase + C::tm_s(t), tc::smem_desc_sw128(q_addr + koff, 16, 1024),
+                     tc::smem_desc_sw128(k_addr + koff, 16, 1024), C::IDESC_S, kk > 0);
         }
-        tc::mma_commit(&s_full[j & 1]);
+        tc::mma_commit(&s_full[t]);
+      };
+      auto issue_pv = [&](int t, int j) {
+        const uint32_t v_addr = smem_u32(Vs + (j % C::NS) * C::TILE_BYTES);
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)
+          tc::mma_ts(tbase + C::tm_o(t), tbase + C::tm_s(t) + kk * 8,
+                     tc::smem_desc_sw128(v_addr + kk * 2048, C::BLOCK_BYTES, 1024), C::IDESC_O,
+                     (j > 0 || kk > 0) ? 1u : 0u);
+        tc::mma_commit(&o_done[t]);
       };
       bool ok = mbar_wait(q_full, 0, a.status, abort_flag) && mbar_wait(&k_full[0], 0, a.status, abort_flag);
       if (ok) {
         tc::fence_after_sync();
-        issue_s(0);
+#pragma unroll
+        for (int t = 0; t < NQ; ++t)
+          if (nt[t] > 0) issue_s(t, 0);
       }
       for (int j = 0; ok && j < n; ++j) {
-        if (j + 1 < n) {
-          const int slot = (j + 1) % C::NS;
-          if (!mbar_wait(&k_full[slot], ((j + 1) / C::NS) & 1, a.status, abort_flag)) break;
-          tc::fence_after_sync();
-          issue_s(j + 1);
-        }
         const int slot = j % C::NS;
-        if (!mbar_wait(&p_full[j & 1], (j >> 1) & 1, a.status, abort_flag)) break;
         if (!mbar_wait(&v_full[slot], (j / C::NS) & 1, a.status, abort_flag)) break;
         tc::fence_after_sync();
-        const uint32_t v_addr = smem_u32(Vs + slot * C::TILE_BYTES);
-        const uint32_t p_tmem = tbase + ((j & 1) ? C::TM_S1 : C::TM_S0);
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk)
-          tc::mma_ts(tbase + C::TM_O, p_tmem + kk * 8, tc::smem_desc_sw128(v_addr + kk * 2048, C::BLOCK_BYTES, 1024),
-                     C::IDESC_O, (j > 0 || kk > 0) ? 1u : 0u);
+        for (int t = 0; t < NQ; ++t) {
+          if (j >= nt[t]) continue;
+          if (!mbar_wait(&p_full[t], j & 1, a.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc::fence_after_sync();
+          issue_pv(t, j);
+          if (j + 1 < nt[t]) {
+            if (!mbar_wait(&k_full[(j + 1) % C::NS], ((j + 1) / C::NS) & 1, a.status, abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc::fence_after_sync();
+            issue_s(t, j + 1);  // S_t aliases P_t: issued after P_t V_j, the tensor pipe keeps the order
+          }
+        }
+        if (!ok) break;
         tc::mma_commit(&kv_empty[slot]);
-        tc::mma_commit(o_done);
       }
       // Whatever happened, wait for every MMA issued above before TMEM is released.
       tc::mma_commit(drain);
@@ -240,24 +283,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ---------------- softmax + correction + epilogue: one thread per query row ----------------
-    const int quarter = warp & 3;                  // TMEM lane quarter this warp may access
-    const int row = quarter * 32 + lane;           // row of the tile == TMEM lane
+    const int t = (warp - kFirstSoftmaxWarp) >> 2;  // which query tile this group owns
+    const int quarter = warp & 3;                    // TMEM lane quarter this warp may access
+    const int row = quarter * 32 + lane;             // row of the tile == TMEM lane
     const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
-    const int qi = q0 + row;                       // query index within its sequence
-    const int horizon = qi + off;                  // last visible key under the causal mask
+    const int q0 = q00 + t * BM;
+    const int qi = q0 + row;                         // query index within its sequence
+    const int horizon = qi + off;                    // last visible key under the causal mask
+    const int my_n = nt[t];
     const float c = a.scale_log2;
-    float m_ref = -INFINITY;                       // running max, scaled log2 units
+    const uint32_t s_addr = tbase + lane_addr + C::tm_s(t);
+    const uint32_t o_addr = tbase + lane_addr + C::tm_o(t);
+    float m_ref = -INFINITY;                         // running max, scaled log2 units
     float l = 0.f;
     bool ok = true;
 
-    for (int j = 0; j < n; ++j) {
-      const int buf = j & 1;
-      if (!mbar_wait(&s_full[buf], (j >> 1) & 1, a.status, abort_flag)) {
+    for (int j = 0; j < my_n; ++j) {
+      if (!mbar_wait(&s_full[t], j & 1, a.status, abort_flag)) {
         ok = false;
         break;
       }
       tc::fence_after_sync();
-      const uint32_t s_addr = tbase + lane_addr + (buf ? C::TM_S1 : C::TM_S0);
       uint32_t sr[4][32];
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) tc::tmem_ld32(s_addr + cc * 32, sr[cc]);
@@ -305,39 +351,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       l += rs0 + rs1;
-      // P_j (bf16) overwrites the first 64 columns of this S buffer
+      // P_j (bf16) overwrites the first 64 columns of S_t
       tc::tmem_st32(s_addr, pk[0]);
       tc::tmem_st32(s_addr + 32, pk[1]);
-      tc::tmem_st_wait();
-
-      if (j > 0) {
-        // O may be touched only once P_{j-1} V_{j-1} has completed
-        if (!mbar_wait(o_done, (j - 1) & 1, a.status, abort_flag)) {
-          ok = false;
-          break;
-        }
-        tc::fence_after_sync();
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
-          const uint32_t o_addr = tbase + lane_addr + C::TM_O;
+      // O_t correction.  S_t(j) completing implies P_t V_{j-1} completed (issued before it), so O_t is idle.
+      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
-          for (int cc = 0; cc < D / 32; ++cc) {
-            uint32_t orr[32];
-            tc::tmem_ld32(o_addr + cc * 32, orr);
-            tc::tmem_ld_wait();
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t orr[32];
+          tc::tmem_ld32(o_addr + cc * 32, orr);
+          tc::tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
-            tc::tmem_st32(o_addr + cc * 32, orr);
-          }
-          tc::tmem_st_wait();
+          for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
+          tc::tmem_st32(o_addr + cc * 32, orr);
         }
       }
+      tc::tmem_st_wait();
       tc::fence_before_sync();
-      mbar_arrive(&p_full[buf]);
+      mbar_arrive(&p_full[t]);
     }
 
     // ---------------- epilogue: O / l, lse ----------------
-    if (ok && n > 0) {
-      ok = mbar_wait(o_done, (n - 1) & 1, a.status, abort_flag);
+    if (ok && my_n > 0) {
+      ok = mbar_wait(&o_done[t], (my_n - 1) & 1, a.status, abort_flag);
       tc::fence_after_sync();
     }
     const bool store = qi < Lq_s;
@@ -351,8 +387,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t orr[32];
-        if (n > 0) {
-          tc::tmem_ld32(tbase + lane_addr + C::TM_O + cc * 32, orr);
+        if (my_n > 0) {
+          tc::tmem_ld32(o_addr + cc * 32, orr);
           tc::tmem_ld_wait();
         } else {
 #pragma unroll
@@ -447,12 +483,12 @@ cudaError_t launch_d(const PrefillLaunch& p) {
   a.causal = p.causal;
   a.out_f32 = p.out_f32;
   a.scale_log2 = p.scale * kLog2e;
-  a.ntiles = (p.Lq + BM - 1) / BM;
+  a.npairs = (p.Lq + NQ * BM - 1) / (NQ * BM);
   a.total_q = p.total_q;
   a.total_k = p.total_k;
   a.status = p.status;
-  if (a.ntiles > 65535) return cudaErrorInvalidValue;
-  dim3 grid(p.Hq, p.B, a.ntiles);
+  if (p.Hq > 65535) return cudaErrorInvalidValue;
+  dim3 grid(a.npairs, p.Hq, p.B);
   prefill_fwd_kernel<D><<<grid, kThreads, C::SMEM_ALLOC, p.stream>>>(tmq, tmk, tmv, a);
   return cudaGetLastError();
 }

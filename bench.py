@@ -165,7 +165,7 @@ class DecodeCase:
         self.alg_bytes = kv_bytes + w.B * w.Hq * w.D * 2 * 2 + w.B * w.Hq * 4
         self.work = self.alg_bytes
         self.unit, self.kind = "GB/s", "hbm"
-        self.launches_per_step = 2
+        self.launches_per_step = 1
         self.h2d = sum(t.numel() * t.element_size() for t in self.host)
         self.d2h = self.out.numel() * 2 + self.lse.numel() * 4
 
@@ -461,7 +461,7 @@ def run_ours(args):
         peak, peak_src = pk["hbm_gbs"], pk["source"]
         roof = {"bound": "hbm", "achieved": per_gpu, "peak": peak, "unit": "GB/s", "frac": per_gpu / peak,
                 "traffic": read_traffic("decode_split"), "peak_source": peak_src,
-                "kernel": "decode_split_kernel + decode_combine_kernel (one attn_decode call, event-timed)"}
+                "kernel": "decode_split_kernel (one attn_decode call: split pass with the combine fused, event-timed)"}
     else:
         peak, peak_src = pk["bf16_tflops"], pk["source"]
         roof = {"bound": "tensor", "achieved": per_gpu, "peak": peak, "unit": "TFLOP/s", "frac": per_gpu / peak,

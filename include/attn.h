@@ -133,8 +133,14 @@ int attn_fwd_ex(const attn_fwd_params* p);
  *   lse      fp32 [B, Hq]  may be NULL
  *
  * Uses a library-owned split-KV workspace on the current device, grown on
- * demand (see attn_release_workspace).  Two kernels are enqueued: the split
- * pass and the combine.
+ * demand with cudaMalloc (see attn_release_workspace); during CUDA graph
+ * capture it is never grown (a call that would need a larger one returns
+ * ATTN_ERR_INVALID_ARG: make one uncaptured call with the largest sizes
+ * first).  Decode calls on one device share that workspace, so calls that can
+ * overlap on the GPU (different streams with no ordering) race on it.
+ * One kernel is enqueued: persistent CTAs (two per SM) each stream an equal
+ * slice of the flattened key space of all rows, and the CTA that lands a
+ * row's last partial merges that row's partials.
  */
 int attn_decode(const void* q, const void* kcache, const void* vcache, const int* kv_lens,
                 void* out, float* lse, int B, int Hq, int Hkv, int Lmax, int D, float scale,
@@ -143,8 +149,13 @@ int attn_decode(const void* q, const void* kcache, const void* vcache, const int
 /*
  * attn_decode_params / attn_decode_ex -- decode with every option.
  *   out_dtype     ATTN_DTYPE_BF16 or ATTN_DTYPE_F32
- *   chunk         keys per split-KV work item; 0 = choose automatically,
- *                 otherwise a multiple of 64 in [64, 65536]
+ *   chunk         0 = default; otherwise the smallest number of keys one CTA's
+ *                 slice of the key space may hold (default 64), in
+ *                 [1, 1048576]: smaller values spread short problems over more
+ *                 CTAs and split rows into more partials
+ * Rows: B * Hkv * (Hq / Hkv / g) must stay at or below 65534, g being the
+ * number of query heads one CTA serves (the largest of 8, 4, 2, 1 dividing
+ * Hq / Hkv); otherwise ATTN_ERR_UNSUPPORTED.
  */
 typedef struct attn_decode_params {
   const void* q;
@@ -164,7 +175,9 @@ int attn_decode_ex(const attn_decode_params* p);
 
 /*
  * attn_decode_workspace_bytes -- bytes of split-KV workspace a decode call
- * with these sizes needs (0 on invalid sizes).  chunk as in attn_decode_ex.
+ * with these sizes needs (0 on invalid sizes).  It depends on Hq / Hkv, D and
+ * the current device's SM count (148 assumed when no device is visible), not
+ * on B, Lmax or chunk: 256 KiB of counters plus two partials per CTA.
  */
 unsigned long long attn_decode_workspace_bytes(int B, int Hq, int Hkv, int Lmax, int D, int chunk);
 
@@ -198,24 +211,26 @@ void attn_release_workspace(void);
  * workspace with cudaMalloc on the first call with a larger problem; this
  * call never does.
  *
- * Same arguments, layouts and results as attn_decode_ex.  The split-KV
- * partials live in a fixed 4 MiB buffer compiled into the library
- * (a file-scope __device__ array): every GPU on which the library's kernels
- * are loaded holds that buffer until the process exits, whether or not this
- * call is used.  The partials need B * Hq * nsplit * (D + 2) * 4 bytes, with
- * nsplit = ceil(Lmax / chunk); with chunk == 0 the chunk is chosen as in
- * attn_decode_ex and then doubled until the partials fit.  A problem whose
- * partials cannot fit (even one split per row) returns
+ * Same arguments, layouts and results as attn_decode_ex.  Its scratch is a
+ * fixed 4 MiB buffer compiled into the library (a file-scope __device__
+ * array): every GPU on which the library's kernels are loaded holds that
+ * buffer until the process exits, whether or not this call is used.  The
+ * buffer holds 256 KiB of work counters followed by the split-KV partials,
+ * two per CTA of the persistent launch (2.5 MiB at most on a 152-SM GB300).
+ * A problem that does not fit -- more than 65534 (b, kv head, head group)
+ * rows, or partials beyond the buffer on a device with more SMs -- returns
  * ATTN_ERR_SCRATCH_TOO_SMALL before anything is enqueued.
  *
  * No call allocates: no cudaMalloc, no cudaFree, no allocating library
  * routine.  The first call on a device looks up the buffer's device address
- * (cudaGetSymbolAddress, once per device, with that device current); make
- * that first call outside any stream capture.  The buffer needs no zeroing:
- * every partial is written before it is read within the same call.  All calls
- * share the one buffer and it keeps the last call's contents: two calls that
- * can overlap on the GPU (different streams with no ordering between them)
- * race on it and may return wrong results.  Order such calls on one stream.
+ * (cudaGetSymbolAddress, once per device, with that device current) and
+ * zeroes the counter area (cudaMemset, then a device synchronise); make that
+ * first call outside any stream capture.  The kernel leaves the counters at
+ * zero after every call, and every partial is written before it is read in
+ * the same call.  All calls share the one buffer and it keeps the last call's
+ * contents: two calls that can overlap on the GPU (different streams with no
+ * ordering between them) race on it and may return wrong results.  Order such
+ * calls on one stream.
  */
 int attn_decode_noalloc(const attn_decode_params* p);
 

@@ -138,7 +138,15 @@ def test_no_cpu_fallback(lib):
 
 
 def test_workspace_bytes_formula(lib):
+    import torch
+
     assert lib.attn_decode_workspace_bytes(0, 8, 2, 64, 128, 0) == 0
     assert lib.attn_decode_workspace_bytes(1, 8, 2, 64, 100, 0) == 0
-    # B*Hq*nsplit*(D+2) floats with an explicit chunk
-    assert lib.attn_decode_workspace_bytes(2, 8, 2, 1000, 128, 256) == 2 * 8 * 4 * 130 * 4
+    sms = torch.cuda.get_device_properties(0).multi_processor_count if torch.cuda.is_available() else 148
+    grid = 2 * sms
+    # 256 KiB of counters + 2 partials per CTA x 4 heads per CTA x (D + 2) floats; independent of B, Lmax, chunk
+    want = 65536 * 4 + 2 * grid * 4 * 130 * 4
+    assert lib.attn_decode_workspace_bytes(2, 8, 2, 1000, 128, 256) == want
+    assert lib.attn_decode_workspace_bytes(64, 8, 2, 99999, 128, 0) == want
+    # too many rows for the counter area
+    assert lib.attn_decode_workspace_bytes(65535, 64, 64, 16, 128, 0) == 0

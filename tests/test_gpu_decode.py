@@ -4,7 +4,8 @@ Inputs are the same seeded bf16 tensors on both sides.  Small cases cover
 every grouped-head width the kernel specialises (1, 2, 4, 8 and a grouping
 that needs several head groups), both head dims, ragged and degenerate
 lengths (0, 1, not a multiple of the stage or the chunk, == Lmax) and several
-chunk sizes; the two decode workloads run at full size (all rows for the 8 x
+minimum slice sizes (down to one key per CTA, which splits rows into many
+partials); the two decode workloads run at full size (all rows for the 8 x
 4096 cache, a sample of rows for the 131072-key cache).
 """
 import numpy as np
@@ -51,9 +52,16 @@ def test_decode_small(B, Hq, Hkv, Lmax, D, lens):
     lens_t = torch.tensor(lens, dtype=torch.int32)
     scale = D ** -0.5
     O_ref, lse_ref = oracle.decode(q, kc, vc, lens, scale)
-    for chunk in (0, 64, 192):
+    # chunk = smallest key slice per CTA: 1 and 7 split rows into many partials (stresses the merge)
+    for chunk in (0, 1, 7, 64, 192):
         O, lse = run(q, kc, vc, lens_t, scale, chunk=chunk)
         assert_attn_close(O, lse, O_ref, lse_ref, f"chunk={chunk}")
+
+
+def test_decode_all_sequences_empty():
+    q, kc, vc, _ = make_decode(2, 8, 2, 64, 128, seed=4)
+    O, lse = run(q, kc, vc, torch.zeros(2, dtype=torch.int32), 0.088)
+    assert torch.all(O == 0) and torch.all(torch.isneginf(lse))
 
 
 def test_decode_zero_length_rows():

@@ -35,13 +35,13 @@ def test_noalloc_symbol_exported(lib):
 
 
 def test_noalloc_rejects_problem_beyond_scratch(lib):
-    # Validation runs before the device is touched, so a bad size is refused
-    # even without a GPU: 4096 rows x 1 split x (128 + 2) floats = 2 MiB fits,
-    # 16384 rows need 8.5 MiB even with one split each.
+    # The fixed buffer's counter area holds 65534 (b, kv head, head group) rows:
+    # 16384 sequences x 8 kv heads x 1 group (4 heads per CTA) is too many.
+    # Nothing is enqueued (the pointers are never dereferenced).
     p = AB.attn_decode_params()
     fake = 1 << 20
     p.q = p.kcache = p.vcache = p.kv_lens = p.out = fake
-    p.B, p.Hq, p.Hkv, p.Lmax, p.D, p.scale = 512, 32, 8, 64, 128, 0.088
+    p.B, p.Hq, p.Hkv, p.Lmax, p.D, p.scale = 16384, 32, 8, 64, 128, 0.088
     rc = lib.attn_decode_noalloc(ctypes.byref(p))
     if torch.cuda.is_available():
         assert rc == AB.ATTN_ERR_SCRATCH_TOO_SMALL
