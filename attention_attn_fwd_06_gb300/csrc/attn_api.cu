@@ -125,7 +125,7 @@ struct DecodeShape {
 DecodeShape decode_shape(int Hq, int Hkv, int D, int num_sms) {
   DecodeShape s;
   const int gp = attn::decode_heads_per_cta(Hq / Hkv);
-  s.grid = attn::decode_grid(num_sms);
+  s.grid = attn::decode_grid(num_sms, Hq / Hkv);
   s.part_o_elems = (size_t)2 * s.grid * gp * D;
   s.part_ml_elems = (size_t)2 * s.grid * gp * 2;
   s.bytes = kCounterBytes + (s.part_o_elems + s.part_ml_elems) * sizeof(float);
@@ -365,6 +365,7 @@ int attn_fwd_ex(const attn_fwd_params* p) {
   L.cu_k = p->cu_seqlens_k;
   L.total_q = p->total_q;
   L.total_k = p->total_k;
+  L.num_sms = s->num_sms;
   L.status = s->status;
   L.stream = stream;
   return map_cuda(attn::launch_prefill(L));

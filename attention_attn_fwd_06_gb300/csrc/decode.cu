@@ -13,7 +13,7 @@
 // lse = (M + log2 sum w_i l_i) ln 2.
 //
 // GB300 design:
-//  * Stream-K split: persistent CTAs (two per SM) each take an equal,
+//  * Stream-K split: persistent CTAs (three per SM; two with 8 heads per CTA) each take an equal,
 //    contiguous slice of the flattened key space of all (b, kv head, head
 //    group) rows, so every CTA streams the same number of bytes whatever the
 //    mix of sequence lengths, and there are no waves and no work-queue
@@ -23,7 +23,7 @@
 //    read from HBM once (the decoder page's "load each K/V block once, reuse it
 //    for all queries of the step").
 //  * A producer warp walks the slice and streams K and V rows (and, on a row
-//    piece's first stage, its q vectors) into a 3-stage shared-memory ring
+//    piece's first stage, its q vectors) into a shared-memory ring (2-3 stages)
 //    with 1-D bulk copies on the TMA engine (cp.async.bulk, mbarrier
 //    completion), running ahead of the consumers across row boundaries.
 //  * Consumer warps read 16-byte vectors of K/V from shared memory.  For a
@@ -64,8 +64,10 @@ struct DecodeCfg {
   static constexpr int KPW = SK / NW;                         // keys per consumer warp per stage
   static constexpr int ITER = KPW / KPI;
   static_assert(ITER * KPI * NW == SK, "stage must split evenly over the consumer warps");
-  static constexpr int NS = 3;                                // ring stages
+  static constexpr int MINB = (GP >= 8) ? 2 : 3;             // resident CTAs per SM (register budget)
+  static constexpr int NS = (MINB == 3) ? 2 : 3;              // ring stages
   static constexpr int THREADS = 32 * (NW + 1);
+  static constexpr int LENS_CACHE = 512;                      // kv_lens kept in shared memory for the walk
   static constexpr int TILE_ELEMS = SK * D;
   static constexpr int TILE_BYTES = TILE_ELEMS * 2;
   static constexpr int Q_BYTES = GP * D * 2;                  // q of the group's heads (bf16)
@@ -80,9 +82,10 @@ struct DecodeCfg {
   static constexpr int OFF_A = OFF_P + NW * 32 * 4;           // abuf[NW][GP]
   static constexpr int OFF_M = OFF_A + NW * GP * 4;           // mbuf[NW][GP]
   static constexpr int OFF_L = OFF_M + NW * GP * 4;           // lbuf[NW][GP]
-  static constexpr int OFF_MISC = OFF_L + NW * GP * 4;        // abort flag, last-partial flag
+  static constexpr int OFF_LENS = OFF_L + NW * GP * 4;        // lens[LENS_CACHE]
+  static constexpr int OFF_MISC = OFF_LENS + LENS_CACHE * 4;  // abort flag, last-partial flag
   static constexpr int SMEM = OFF_MISC + 16;
-  static_assert(SMEM <= 113 * 1024, "two CTAs per SM");
+  static_assert(MINB * (SMEM + 1024) <= 228 * 1024, "MINB CTAs per SM");
 };
 
 struct StageInfo {
@@ -107,7 +110,7 @@ __device__ __forceinline__ void store_out(void* out, size_t idx, float v, int ou
 }
 
 template <int D, int GP>
-__global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS, 2)
+__global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS, DecodeCfg<D, GP>::MINB)
     decode_split_kernel(const DecodeLaunch p, const int ngroups, const int group) {
   using C = DecodeCfg<D, GP>;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -124,6 +127,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS, 2)
   float* lbuf = reinterpret_cast<float*>(smem + C::OFF_L);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC);
   volatile int* last_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+  int* lens_s = reinterpret_cast<int*>(smem + C::OFF_LENS);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -149,11 +153,14 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS, 2)
       const int raw = p.kv_lens[b];
       const int len = clamp_len(raw, p.Lmax);
       if (raw != len && cta == 0) record_status(p.status, ATTN_ERR_DEVICE_BOUNDS);
+      if (b < C::LENS_CACHE) lens_s[b] = len;
       wsum += len;
     }
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, off);
+    __syncwarp();
     if (lane != 0) return;
+    auto seq_len = [&](int b) -> int { return b < C::LENS_CACHE ? lens_s[b] : clamp_len(p.kv_lens[b], p.Lmax); };
     const long long W = wsum * Hg;
     // At least min_keys keys per CTA; CTAs past the effective grid only handle empty sequences.
     long long geff = (W + p.min_keys - 1) / p.min_keys;
@@ -205,7 +212,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS, 2)
       long long acc = 0;  // first flattened key of sequence b
       int b = 0, len = 0;
       for (; b < p.B; ++b) {
-        len = clamp_len(p.kv_lens[b], p.Lmax);
+        len = seq_len(b);
         if (acc + (long long)Hg * len > lo) break;
         acc += (long long)Hg * len;
       }
@@ -228,7 +235,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS, 2)
           hg = 0;
           acc += (long long)Hg * len;
           for (++b; b < p.B; ++b) {
-            len = clamp_len(p.kv_lens[b], p.Lmax);
+            len = seq_len(b);
             if (len > 0) break;
           }
           row_start = acc;
@@ -237,7 +244,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS, 2)
     }
     // Sequences with no keys: O = 0, lse = -inf, spread over the CTAs.
     for (int b = cta; ok && b < p.B; b += gridDim.x) {
-      if (clamp_len(p.kv_lens[b], p.Lmax) != 0) continue;
+      if (seq_len(b) != 0) continue;
       for (int hg = 0; ok && hg < Hg; ++hg) ok = emit(b, hg, 0, 0, 0, 0, 0, 0);
     }
     if (ok) {
@@ -265,8 +272,8 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS, 2)
   float* pw = pbuf + warp * 32;
   float* aw = abuf + warp * GP;
 
-  float qf[GP][8];
-  float o[GP][8];
+  float2 qf[GP][4];     // scaled q, dims 8*sub .. 8*sub+7 as 4 pairs, per head
+  float2 o[GP][4];      // O accumulator, same dims
   float m = -INFINITY;  // running max (log2 units) of this lane's head, uniform over the lanes sharing it
   float l = 0.f;        // this lane's share of the running sum
 
@@ -287,11 +294,9 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS, 2)
         for (int j = 0; j < 4; ++j) {
           float lo, hi;
           bf16x2_to_f32(w4[j], lo, hi);
-          qf[g][2 * j] = lo * qscale;
-          qf[g][2 * j + 1] = hi * qscale;
+          qf[g][j] = make_float2(lo * qscale, hi * qscale);
+          o[g][j] = make_float2(0.f, 0.f);
         }
-#pragma unroll
-        for (int j = 0; j < 8; ++j) o[g][j] = 0.f;
       }
       m = -INFINITY;
       l = 0.f;
@@ -303,24 +308,32 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS, 2)
       const int kb = warp * C::KPW + it * C::KPI;
       if (kb >= nk) break;  // warp-uniform
 
-      // S = (scale*log2e) q . k for R rows x GP heads, partial over this lane's 8 dims
-      float acc[C::VPL];
+      // Load this iteration's K and V rows up front so the V latency hides behind the reductions.
+      uint4 kr[C::R], vr[C::R];
 #pragma unroll
       for (int r = 0; r < C::R; ++r) {
         const int key = kb + r * C::RPW + rw;
-        uint4 kr = make_uint4(0, 0, 0, 0);
-        if (key < nk) kr = lds128(Kt + key * D + 8 * sub);
-        float kf[8];
-        bf16x2_to_f32(kr.x, kf[0], kf[1]);
-        bf16x2_to_f32(kr.y, kf[2], kf[3]);
-        bf16x2_to_f32(kr.z, kf[4], kf[5]);
-        bf16x2_to_f32(kr.w, kf[6], kf[7]);
+        kr[r] = make_uint4(0, 0, 0, 0);
+        vr[r] = make_uint4(0, 0, 0, 0);
+        if (key < nk) {
+          kr[r] = lds128(Kt + key * D + 8 * sub);
+          vr[r] = lds128(Vt + key * D + 8 * sub);
+        }
+      }
+      // S = (scale*log2e) q . k for R rows x GP heads, partial over this lane's 8 dims (packed fp32x2 FMAs)
+      float acc[C::VPL];
+#pragma unroll
+      for (int r = 0; r < C::R; ++r) {
+        const uint32_t w4[4] = {kr[r].x, kr[r].y, kr[r].z, kr[r].w};
+        float2 kf[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) bf16x2_to_f32(w4[j], kf[j].x, kf[j].y);
 #pragma unroll
         for (int g = 0; g < GP; ++g) {
-          float s = 0.f;
+          float2 s2 = __ffma2_rn(qf[g][0], kf[0], make_float2(0.f, 0.f));
 #pragma unroll
-          for (int j = 0; j < 8; ++j) s = fmaf(qf[g][j], kf[j], s);
-          acc[r * GP + g] = s;
+          for (int j = 1; j < 4; ++j) s2 = __ffma2_rn(qf[g][j], kf[j], s2);
+          acc[r * GP + g] = s2.x + s2.y;
         }
       }
       // Reduce-scatter over the LPR lanes of a row: afterwards lane `sub` holds
@@ -354,28 +367,38 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS, 2)
       if (__any_sync(0xffffffffu, alpha < 1.f)) {
 #pragma unroll
         for (int g = 0; g < GP; ++g) {
-          const float a = aw[g];
+          const float2 a2 = make_float2(aw[g], aw[g]);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) o[g][j] *= a;
+          for (int j = 0; j < 4; ++j) o[g][j] = __fmul2_rn(o[g][j], a2);
         }
       }
       // O += P V over the same R rows
 #pragma unroll
       for (int r = 0; r < C::R; ++r) {
-        const int key = kb + r * C::RPW + rw;
-        uint4 vr = make_uint4(0, 0, 0, 0);
-        if (key < nk) vr = lds128(Vt + key * D + 8 * sub);
-        float vf[8];
-        bf16x2_to_f32(vr.x, vf[0], vf[1]);
-        bf16x2_to_f32(vr.y, vf[2], vf[3]);
-        bf16x2_to_f32(vr.z, vf[4], vf[5]);
-        bf16x2_to_f32(vr.w, vf[6], vf[7]);
+        const uint32_t w4[4] = {vr[r].x, vr[r].y, vr[r].z, vr[r].w};
+        float2 vf[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) bf16x2_to_f32(w4[j], vf[j].x, vf[j].y);
         const float* pr = pw + rw * C::LPR + r * GP;
+        float pg[GP];
+        if constexpr (GP % 4 == 0) {
+#pragma unroll
+          for (int g4 = 0; g4 < GP / 4; ++g4) {
+            const float4 p4 = reinterpret_cast<const float4*>(pr)[g4];
+            pg[4 * g4] = p4.x;
+            pg[4 * g4 + 1] = p4.y;
+            pg[4 * g4 + 2] = p4.z;
+            pg[4 * g4 + 3] = p4.w;
+          }
+        } else {
+#pragma unroll
+          for (int g = 0; g < GP; ++g) pg[g] = pr[g];
+        }
 #pragma unroll
         for (int g = 0; g < GP; ++g) {
-          const float pg = pr[g];
+          const float2 p2 = make_float2(pg[g], pg[g]);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) o[g][j] = fmaf(pg, vf[j], o[g][j]);
+          for (int j = 0; j < 4; ++j) o[g][j] = __ffma2_rn(p2, vf[j], o[g][j]);
         }
       }
       __syncwarp();
@@ -394,7 +417,10 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS, 2)
 #pragma unroll
       for (int g = 0; g < GP; ++g)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) o[g][j] += __shfl_xor_sync(0xffffffffu, o[g][j], mask);
+        for (int j = 0; j < 4; ++j) {
+          o[g][j].x += __shfl_xor_sync(0xffffffffu, o[g][j].x, mask);
+          o[g][j].y += __shfl_xor_sync(0xffffffffu, o[g][j].y, mask);
+        }
     if (rw == 0 && sub < GP) {
       mbuf[warp * GP + sub] = m;
       lbuf[warp * GP + sub] = lsum;
@@ -414,7 +440,10 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS, 2)
           const float e = (mw == -INFINITY) ? 0.f : ex2_approx(mw - M);
           float* dst = obuf + g * D + 8 * sub;
 #pragma unroll
-          for (int j = 0; j < 8; ++j) dst[j] = fmaf(e, o[g][j], dst[j]);
+          for (int j = 0; j < 4; ++j) {
+            dst[2 * j] = fmaf(e, o[g][j].x, dst[2 * j]);
+            dst[2 * j + 1] = fmaf(e, o[g][j].y, dst[2 * j + 1]);
+          }
         }
       }
       named_bar_sync(1, nct);
@@ -450,42 +479,77 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS, 2)
       }
     }
     if (si.np > 1) {
-      // Publish the partial; the CTA that lands a row's last partial merges them all.
-      __threadfence();
+      // Publish the partial (the barrier orders every thread's stores before thread 0's release
+      // fence and atomic); the CTA that lands a row's last partial merges them all.
       named_bar_sync(1, nct);
       if (ctid == 0) {
         const unsigned ctr = 2u + (unsigned)(si.b * Hg + si.hg);
+        __threadfence();
         const unsigned old = atomicAdd(&p.counters[ctr], 1u);
         const int is_last = (old == (unsigned)si.np - 1u);
-        if (is_last) atomicExch(&p.counters[ctr], 0u);  // re-arm for the next call
+        if (is_last) {
+          atomicExch(&p.counters[ctr], 0u);  // re-arm for the next call
+          __threadfence();                   // acquire: the other CTAs' partials are visible from here on
+        }
         *last_flag = is_last;
       }
       named_bar_sync(1, nct);
       if (*last_flag) {
-        __threadfence();
-        for (int idx = ctid; idx < GP * D; idx += nct) {
+        // Single pass over the row's partials with a running max; loads go out NB partials at a time.
+        // Partial slots of the row: CTA c holds slot 2c (+1 for the first CTA when the row starts
+        // inside its slice).
+        constexpr int KP = (GP * D + C::NW * 32 - 1) / (C::NW * 32);
+        constexpr int NB = (KP >= 8) ? 1 : (8 / KP);
+        float Mx[KP], Lx[KP], Ox[KP];
+#pragma unroll
+        for (int k = 0; k < KP; ++k) {
+          Mx[k] = -INFINITY;
+          Lx[k] = 0.f;
+          Ox[k] = 0.f;
+        }
+        for (int i0 = 0; i0 < si.np; i0 += NB) {
+          float mv[KP][NB], lv[KP][NB], ov[KP][NB];
+#pragma unroll
+          for (int bb = 0; bb < NB; ++bb) {
+            const int i = i0 + bb;
+            const int sl = 2 * (si.cta_lo + i) + (i == 0 ? si.lo_odd : 0);
+#pragma unroll
+            for (int k = 0; k < KP; ++k) {
+              const int idx = ctid + k * nct;
+              mv[k][bb] = -INFINITY;
+              lv[k][bb] = 0.f;
+              ov[k][bb] = 0.f;
+              if (i < si.np && idx < GP * D) {
+                const int g = idx / D;
+                const size_t prow = (size_t)sl * GP + g;
+                mv[k][bb] = __ldcg(p.part_ml + prow * 2);
+                lv[k][bb] = __ldcg(p.part_ml + prow * 2 + 1);
+                ov[k][bb] = __ldcg(p.part_o + prow * D + (idx - g * D));
+              }
+            }
+          }
+#pragma unroll
+          for (int bb = 0; bb < NB; ++bb)
+#pragma unroll
+            for (int k = 0; k < KP; ++k) {
+              if (mv[k][bb] == -INFINITY) continue;
+              const float Mn = fmaxf(Mx[k], mv[k][bb]);
+              const float a = ex2_approx(Mx[k] - Mn);  // 0 while Mx is -inf
+              const float w = ex2_approx(mv[k][bb] - Mn);
+              Lx[k] = fmaf(Lx[k], a, w * lv[k][bb]);
+              Ox[k] = fmaf(Ox[k], a, w * ov[k][bb]);
+              Mx[k] = Mn;
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < KP; ++k) {
+          const int idx = ctid + k * nct;
+          if (idx >= GP * D) continue;
           const int g = idx / D;
           const int d = idx - g * D;
           const size_t bh = (size_t)si.b * p.Hq + hq0 + g;
-          // partial slots of the row: CTA c holds slot 2c (+1 for the first CTA when the row
-          // starts inside its slice)
-          float M = -INFINITY;
-#pragma unroll 4
-          for (int i = 0; i < si.np; ++i) {
-            const int sl = 2 * (si.cta_lo + i) + (i == 0 ? si.lo_odd : 0);
-            M = fmaxf(M, __ldcg(p.part_ml + ((size_t)sl * GP + g) * 2));
-          }
-          float L = 0.f, O = 0.f;
-#pragma unroll 4
-          for (int i = 0; i < si.np; ++i) {
-            const int sl = 2 * (si.cta_lo + i) + (i == 0 ? si.lo_odd : 0);
-            const size_t prow = (size_t)sl * GP + g;
-            const float w = ex2_approx(__ldcg(p.part_ml + prow * 2) - M);
-            L = fmaf(w, __ldcg(p.part_ml + prow * 2 + 1), L);
-            O = fmaf(w, __ldcg(p.part_o + prow * D + d), O);
-          }
-          store_out<float>(p.out, bh * D + d, O / L, p.out_f32);
-          if (d == 0 && p.lse != nullptr) p.lse[bh] = (M + log2f(L)) * kLn2;
+          store_out<float>(p.out, bh * D + d, Ox[k] / Lx[k], p.out_f32);
+          if (d == 0 && p.lse != nullptr) p.lse[bh] = (Mx[k] + log2f(Lx[k])) * kLn2;
         }
       }
     }
@@ -506,7 +570,7 @@ cudaError_t launch_split(const DecodeLaunch& p, int ngroups, int group, int num_
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  decode_split_kernel<D, GP><<<decode_grid(num_sms), C::THREADS, C::SMEM, p.stream>>>(p, ngroups, group);
+  decode_split_kernel<D, GP><<<decode_grid(num_sms, group), C::THREADS, C::SMEM, p.stream>>>(p, ngroups, group);
   return cudaGetLastError();
 }
 
@@ -527,13 +591,17 @@ cudaError_t dispatch_gp(const DecodeLaunch& p, int num_sms) {
 
 int decode_stage_keys(int D) { return D == 64 ? DecodeCfg<64, 1>::SK : DecodeCfg<128, 1>::SK; }
 
-int decode_grid(int num_sms) { return 2 * (num_sms > 0 ? num_sms : 148); }
-
 int decode_heads_per_cta(int group) {
   for (int gp = 8; gp > 1; gp >>= 1)
     if (group % gp == 0) return gp;
   return 1;
 }
+
+int decode_grid(int num_sms, int group) {
+  const int minb = decode_heads_per_cta(group) >= 8 ? DecodeCfg<128, 8>::MINB : DecodeCfg<128, 4>::MINB;
+  return minb * (num_sms > 0 ? num_sms : 148);
+}
+
 
 cudaError_t launch_decode(const DecodeLaunch& p, int num_sms) {
   return (p.D == 64) ? dispatch_gp<64>(p, num_sms) : dispatch_gp<128>(p, num_sms);

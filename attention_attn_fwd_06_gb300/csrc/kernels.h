@@ -27,13 +27,14 @@ struct DecodeLaunch {
 
 // Keys per pipeline stage of the split pass.
 int decode_stage_keys(int D);
-// CTAs of the persistent decode launch (two per SM); the partial slots number 2 * grid.
-int decode_grid(int num_sms);
+// CTAs of the persistent decode launch (three per SM, two with 8 heads per CTA); the partial slots
+// number 2 * grid.
+int decode_grid(int num_sms, int group);
 // Number of query heads one decode CTA serves (the largest of 8, 4, 2, 1 dividing Hq / Hkv).
 int decode_heads_per_cta(int group);
 // Counter slots the decode kernel may use: 2 + B * Hkv * (Hq / Hkv / heads_per_cta) must fit.
 constexpr int kDecodeCounterSlots = 65536;
-// One persistent launch (two CTAs per SM) that also merges the split partials.
+// One persistent launch that also merges the split partials.
 cudaError_t launch_decode(const DecodeLaunch& p, int num_sms);
 
 // Prefill (tcgen05 tensor-core path).
@@ -50,6 +51,7 @@ struct PrefillLaunch {
   const int* cu_q;  // null for the dense layout
   const int* cu_k;
   int total_q, total_k;
+  int num_sms;      // persistent grid size
   unsigned* status;
   cudaStream_t stream;
 };

@@ -9,21 +9,23 @@
 // scaled by `scale` and causally masked (bottom-right aligned) as in the
 // standard chain of the same section; the per-row log-sum-exp is written too.
 //
-// GB300 design (one CTA per 128-row query tile, 6 warps):
-//  * warp 0 (one lane) issues TMA tile loads: Q once, then K_j and V_j into a
-//    shared-memory ring (128-byte swizzled boxes of 64 columns x 128 rows);
-//  * warp 1 owns the TMEM allocation (512 columns) and one lane issues every
-//    tcgen05.mma: S_j = Q K_j^T into one of two TMEM S buffers (fp32,
-//    128 x 128), and O += P_j V_j with P read from TMEM and V_j from shared
-//    memory (MN-major operand, no transpose pass);
-//  * warps 2-5 (128 threads) run the softmax, one thread per query row = one
-//    TMEM lane: load the S row, mask, row max, exp2 on MUFU, row sum, write P
-//    as bf16 back over the S buffer, and rescale the O row in TMEM when the
-//    running max rose by more than 8 (log2 units) -- otherwise the stale max is
-//    kept, which is exact because O and l share it;
-//  * S is double-buffered so Q K_{j+1}^T runs on the tensor cores while the
-//    softmax works on S_j; P V_j runs while the softmax starts on S_{j+1}.
-//  * The query tiles of one head launch together (K/V reuse in L2), heaviest
+// GB300 design (two 128-row query tiles per CTA, 10 warps):
+//  * warp 0 (one lane) issues TMA tile loads: both Q tiles once, then K_j and
+//    V_j into two shared-memory rings (128-byte swizzled boxes of 64 columns x
+//    128 rows); a K slot is refilled once the S MMAs reading it are done, a V
+//    slot once the P V MMAs are, so loads run about two steps ahead;
+//  * warp 1 owns the TMEM allocation (512 columns: S_A, S_B, O_A, O_B) and one
+//    lane issues every tcgen05.mma: S_t = Q_t K_j^T (both operands from shared
+//    memory, fp32 accumulator in TMEM) and O_t += P_t V_j with P read from TMEM
+//    (where it overwrote S_t) and V_j as an MN-major operand (no transpose);
+//  * warps 2-5 and 6-9 are one softmax group per query tile, one thread per
+//    query row = one TMEM lane: load the S row, mask, row max, exp2 on MUFU,
+//    row sum, write P as bf16 over S, and rescale the O row in TMEM when the
+//    running max rose by more than 8 (log2 units) -- otherwise the stale max
+//    is kept, which is exact because O and l share it;
+//  * per K/V step the MMA warp issues P_A V_j, S_A(j+1), P_B V_j, S_B(j+1):
+//    one tile's softmax runs while the tensor pipe works for the other tile;
+//  * the query tiles of one head launch together (K/V reuse in L2), heaviest
 //    (latest, causal) first.
 //
 // Every wait is bounded (common.cuh); on a timeout the CTA records the status,
@@ -60,8 +62,9 @@ struct Cfg {
   static constexpr int OFF_K = OFF_Q + NQ * TILE_BYTES;
   static constexpr int OFF_V = OFF_K + NS * TILE_BYTES;
   static constexpr int OFF_BAR = OFF_V + NS * TILE_BYTES;
-  // barriers: q_full, k_full[NS], v_full[NS], kv_empty[NS], s_full[NQ], p_full[NQ], o_done[NQ], drain
-  static constexpr int NBAR = 1 + 3 * NS + 3 * NQ + 1;
+  // barriers: q_full, q_empty, k_full[NS], v_full[NS], k_empty[NS], v_empty[NS], s_full[NQ], p_full[NQ],
+  // o_done[NQ], drain
+  static constexpr int NBAR = 2 + 4 * NS + 3 * NQ + 1;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // tmem address, abort flag
   static constexpr int SMEM_USED = OFF_MISC + 16;
   static constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // slack to align the base to 1024
@@ -84,10 +87,78 @@ struct PrefillArgs {
   int causal;
   int out_f32;
   float scale_log2;  // scale * log2(e)
-  int npairs;        // CTAs along the (longest) sequence: NQ query tiles each
+  int ns;            // work items per (sequence, head): pairs of tile pairs
+  int total_items;   // B * Hq * ns
   int total_q, total_k;  // packed layout: rows of q/out and of k/v
   unsigned* status;
 };
+
+// One job = one pair of 128-row query tiles of one (sequence, head).
+struct Job {
+  int bs, h, hk;
+  int q_start, k_start, Lq_s, Lkv_s;
+  int q00;  // first row of the first tile
+  int off;  // causal alignment: key j visible to row i iff j <= i + off
+  int nt[NQ];
+  int n;    // max nt: K/V steps of the job
+};
+
+// Work item `item` holds the tile pairs (np-1-s) and s of one (sequence, head), np being that
+// sequence's number of tile pairs: on a causal square the two cost the same in total, so equal
+// numbers of items per CTA balance.  `half` picks the heavy (0) or light (1) pair.  Returns false
+// when the job is empty (past the sequence end, the middle pair of an odd count, malformed offsets).
+__device__ __forceinline__ bool make_job(const PrefillArgs& a, int item, int half, Job& jb) {
+  const int s = item % a.ns;
+  const int rest = item / a.ns;
+  jb.h = rest % a.Hq;
+  jb.bs = rest / a.Hq;
+  jb.hk = jb.h / (a.Hq / a.Hkv);
+  jb.q_start = 0;
+  jb.k_start = 0;
+  jb.Lq_s = a.Lq;
+  jb.Lkv_s = a.Lkv;
+  if (a.varlen) {
+    jb.q_start = a.cu_q[jb.bs];
+    jb.Lq_s = a.cu_q[jb.bs + 1] - jb.q_start;
+    jb.k_start = a.cu_k[jb.bs];
+    jb.Lkv_s = a.cu_k[jb.bs + 1] - jb.k_start;
+    if (jb.q_start < 0 || jb.Lq_s < 0 || jb.Lq_s > a.Lq || jb.q_start + jb.Lq_s > a.total_q || jb.k_start < 0 ||
+        jb.Lkv_s < 0 || jb.k_start + jb.Lkv_s > a.total_k) {
+      record_status(a.status, ATTN_ERR_DEVICE_BOUNDS);  // malformed cu_seqlens: touch nothing
+      return false;
+    }
+  }
+  const int np = (jb.Lq_s + NQ * BM - 1) / (NQ * BM);
+  const int heavy = np - 1 - s;
+  int pair;
+  if (half == 0) {
+    pair = heavy;
+  } else {
+    if (s >= heavy) return false;  // the middle pair of an odd count is done by half 0
+    pair = s;
+  }
+  if (pair < 0) return false;
+  jb.q00 = pair * NQ * BM;
+  jb.off = jb.Lkv_s - jb.Lq_s;
+  jb.n = 0;
+#pragma unroll
+  for (int t = 0; t < NQ; ++t) {
+    const int q0 = jb.q00 + t * BM;
+    int n = 0;
+    if (q0 < jb.Lq_s && jb.Lkv_s > 0) {
+      if (a.causal) {
+        const int last_row = min(q0 + BM - 1, jb.Lq_s - 1);
+        const int kmax = min(jb.Lkv_s - 1, last_row + jb.off);
+        n = (kmax < 0) ? 0 : kmax / BN + 1;
+      } else {
+        n = (jb.Lkv_s + BN - 1) / BN;
+      }
+    }
+    jb.nt[t] = n;
+    jb.n = max(jb.n, n);
+  }
+  return true;
+}
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -101,63 +172,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* Vs = smem + C::OFF_V;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* q_full = bars;
-  uint64_t* k_full = bars + 1;
+  uint64_t* q_empty = bars + 1;         // Q tiles free: every S MMA of the job has completed
+  uint64_t* k_full = bars + 2;
   uint64_t* v_full = k_full + C::NS;
-  uint64_t* kv_empty = v_full + C::NS;
-  uint64_t* s_full = kv_empty + C::NS;
+  uint64_t* k_empty = v_full + C::NS;   // K slot free: every S = Q K^T reading it has completed
+  uint64_t* v_empty = k_empty + C::NS;  // V slot free: every P V reading it has completed
+  uint64_t* s_full = v_empty + C::NS;
   uint64_t* p_full = s_full + NQ;
   uint64_t* o_done = p_full + NQ;
   uint64_t* drain = o_done + NQ;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
-
-  // ---------------- which tiles ----------------
-  // Launch order: the query tiles of one head are adjacent (so the ~150 CTAs in
-  // flight touch ~10 heads and K/V are served from L2), heaviest (latest,
-  // causal) tiles first within the head.
-  const int pair = a.npairs - 1 - (int)blockIdx.x;
-  const int h = blockIdx.y;
-  const int bs = blockIdx.z;  // batch index (dense) or sequence index (packed)
-  const int hk = h / (a.Hq / a.Hkv);
-  int q_start = 0, k_start = 0, Lq_s = a.Lq, Lkv_s = a.Lkv;
-  if (a.varlen) {
-    q_start = a.cu_q[bs];
-    Lq_s = a.cu_q[bs + 1] - q_start;
-    k_start = a.cu_k[bs];
-    Lkv_s = a.cu_k[bs + 1] - k_start;
-    if (q_start < 0 || Lq_s < 0 || Lq_s > a.Lq || q_start + Lq_s > a.total_q || k_start < 0 || Lkv_s < 0 ||
-        k_start + Lkv_s > a.total_k) {
-      // malformed cu_seqlens: touch nothing, report it
-      if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) record_status(a.status, ATTN_ERR_DEVICE_BOUNDS);
-      return;
-    }
-  }
-  const int q00 = pair * NQ * BM;  // first row of the CTA's first tile
-  if (q00 >= Lq_s) return;         // whole CTA, before any barrier or TMEM use
-  const int off = Lkv_s - Lq_s;    // causal alignment: key j visible to row i iff j <= i + off
-  // K/V tiles each query tile needs (0 when the tile is past the end or sees no key)
-  int nt[NQ];
-#pragma unroll
-  for (int t = 0; t < NQ; ++t) {
-    const int q0 = q00 + t * BM;
-    int n = 0;
-    if (q0 < Lq_s && Lkv_s > 0) {
-      if (a.causal) {
-        const int last_row = min(q0 + BM - 1, Lq_s - 1);
-        const int kmax = min(Lkv_s - 1, last_row + off);
-        n = (kmax < 0) ? 0 : kmax / BN + 1;
-      } else {
-        n = (Lkv_s + BN - 1) / BN;
-      }
-    }
-    nt[t] = n;
-  }
-  int n = 0;
-#pragma unroll
-  for (int t = 0; t < NQ; ++t) n = max(n, nt[t]);
-  // TMA coordinates: dense maps are (d, row, b*H + h); packed maps are (d, h, token)
-  const int qhead = a.varlen ? h : bs * a.Hq + h;
-  const int khead = a.varlen ? hk : bs * a.Hkv + hk;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -179,55 +204,80 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::fence_after_sync();
   const uint32_t tbase = *tmem_slot;
 
+  // Every role walks the same job sequence: items blockIdx.x, +gridDim.x, ...; two jobs per item.
   if (warp == kWarpTMA) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
       tc::tma_prefetch_desc(&tmq);
       tc::tma_prefetch_desc(&tmk);
       tc::tma_prefetch_desc(&tmv);
-      int issued = 0;
-      if (n > 0) {
-        uint32_t qbytes = 0;
+      int kv = 0;     // K/V steps issued (ring position)
+      int qjobs = 0;  // jobs whose Q was loaded
+      bool q_pending = false;
+      bool ok = true;
+      for (int item = blockIdx.x; ok && item < a.total_items; item += gridDim.x) {
+        for (int half = 0; ok && half < 2; ++half) {
+          Job jb;
+          if (!make_job(a, item, half, jb) || jb.n == 0) continue;
+          const int qhead = a.varlen ? jb.h : jb.bs * a.Hq + jb.h;
+          const int khead = a.varlen ? jb.hk : jb.bs * a.Hkv + jb.hk;
+          if (qjobs > 0 && !mbar_wait(q_empty, (qjobs - 1) & 1, a.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          uint32_t qbytes = 0;
 #pragma unroll
-        for (int t = 0; t < NQ; ++t) qbytes += nt[t] > 0 ? C::TILE_BYTES : 0;
-        mbar_arrive_expect_tx(q_full, qbytes);
+          for (int t = 0; t < NQ; ++t) qbytes += jb.nt[t] > 0 ? C::TILE_BYTES : 0;
+          mbar_arrive_expect_tx(q_full, qbytes);
 #pragma unroll
-        for (int t = 0; t < NQ; ++t) {
-          if (nt[t] == 0) continue;
-          const int qrow = q_start + q00 + t * BM;
-          for (int db = 0; db < C::NDB; ++db)
-            tc::tma_load_3d(Qs + t * C::TILE_BYTES + db * C::BLOCK_BYTES, &tmq, db * 64, a.varlen ? qhead : qrow,
-                            a.varlen ? qrow : qhead, q_full);
+          for (int t = 0; t < NQ; ++t) {
+            if (jb.nt[t] == 0) continue;
+            const int qrow = jb.q_start + jb.q00 + t * BM;
+            for (int db = 0; db < C::NDB; ++db)
+              tc::tma_load_3d(Qs + t * C::TILE_BYTES + db * C::BLOCK_BYTES, &tmq, db * 64, a.varlen ? qhead : qrow,
+                              a.varlen ? qrow : qhead, q_full);
+          }
+          q_pending = true;
+          ++qjobs;
+          for (int j = 0; j < jb.n; ++j) {
+            // K slots free up after the S MMAs, V slots after the P V MMAs: the two rings refill independently
+            const int slot = kv % C::NS;
+            const int krow = jb.k_start + j * BN;
+            if (kv >= C::NS && !mbar_wait(&k_empty[slot], ((kv / C::NS) - 1) & 1, a.status, abort_flag)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&k_full[slot], C::TILE_BYTES);
+            for (int db = 0; db < C::NDB; ++db)
+              tc::tma_load_3d(Ks + slot * C::TILE_BYTES + db * C::BLOCK_BYTES, &tmk, db * 64,
+                              a.varlen ? khead : krow, a.varlen ? krow : khead, &k_full[slot]);
+            if (kv >= C::NS && !mbar_wait(&v_empty[slot], ((kv / C::NS) - 1) & 1, a.status, abort_flag)) {
+              mbar_wait(&k_full[slot], (kv / C::NS) & 1, a.status, nullptr);  // K is in flight: let it land
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&v_full[slot], C::TILE_BYTES);
+            for (int db = 0; db < C::NDB; ++db)
+              tc::tma_load_3d(Vs + slot * C::TILE_BYTES + db * C::BLOCK_BYTES, &tmv, db * 64,
+                              a.varlen ? khead : krow, a.varlen ? krow : khead, &v_full[slot]);
+            ++kv;
+          }
         }
       }
-      for (int j = 0; j < n; ++j) {
-        const int slot = j % C::NS;
-        if (j >= C::NS && !mbar_wait(&kv_empty[slot], ((j / C::NS) - 1) & 1, a.status, abort_flag)) break;
-        const int krow = k_start + j * BN;
-        mbar_arrive_expect_tx(&k_full[slot], C::TILE_BYTES);
-        for (int db = 0; db < C::NDB; ++db)
-          tc::tma_load_3d(Ks + slot * C::TILE_BYTES + db * C::BLOCK_BYTES, &tmk, db * 64, a.varlen ? khead : krow,
-                          a.varlen ? krow : khead, &k_full[slot]);
-        mbar_arrive_expect_tx(&v_full[slot], C::TILE_BYTES);
-        for (int db = 0; db < C::NDB; ++db)
-          tc::tma_load_3d(Vs + slot * C::TILE_BYTES + db * C::BLOCK_BYTES, &tmv, db * 64, a.varlen ? khead : krow,
-                          a.varlen ? krow : khead, &v_full[slot]);
-        issued = j + 1;
-      }
       if (*abort_flag) {  // let in-flight copies land before shared memory is released
-        if (n > 0) mbar_wait(q_full, 0, a.status, nullptr);
-        for (int j = (issued > C::NS ? issued - C::NS : 0); j < issued; ++j) {
-          mbar_wait(&k_full[j % C::NS], (j / C::NS) & 1, a.status, nullptr);
-          mbar_wait(&v_full[j % C::NS], (j / C::NS) & 1, a.status, nullptr);
+        if (q_pending) mbar_wait(q_full, (qjobs - 1) & 1, a.status, nullptr);
+        for (int g = (kv > C::NS ? kv - C::NS : 0); g < kv; ++g) {
+          mbar_wait(&k_full[g % C::NS], (g / C::NS) & 1, a.status, nullptr);
+          mbar_wait(&v_full[g % C::NS], (g / C::NS) & 1, a.status, nullptr);
         }
       }
     }
   } else if (warp == kWarpMMA) {
     // ---------------- MMA issuer: S_A, S_B, then per step PV_A, S_A', PV_B, S_B' ----------------
-    if (lane == 0 && n > 0) {
-      auto issue_s = [&](int t, int j) {
+    if (lane == 0) {
+      auto issue_s = [&](int t, int g) {
         const uint32_t q_addr = smem_u32(Qs + t * C::TILE_BYTES);
-        const uint32_t k_addr = smem_u32(Ks + (j % C::NS) * C::TILE_BYTES);
+        const uint32_t k_addr = smem_u32(Ks + (g % C::NS) * C::TILE_BYTES);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t koff = (kk >> 2) * C::BLOCK_BYTES + (kk & 3) * 32;
@@ -236,46 +286,74 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc::mma_commit(&s_full[t]);
       };
-      auto issue_pv = [&](int t, int j) {
-        const uint32_t v_addr = smem_u32(Vs + (j % C::NS) * C::TILE_BYTES);
+      auto issue_pv = [&](int t, int g, bool first) {
+        const uint32_t v_addr = smem_u32(Vs + (g % C::NS) * C::TILE_BYTES);
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
           tc::mma_ts(tbase + C::tm_o(t), tbase + C::tm_s(t) + kk * 8,
                      tc::smem_desc_sw128(v_addr + kk * 2048, C::BLOCK_BYTES, 1024), C::IDESC_O,
-                     (j > 0 || kk > 0) ? 1u : 0u);
+                     (!first || kk > 0) ? 1u : 0u);
         tc::mma_commit(&o_done[t]);
       };
-      bool ok = mbar_wait(q_full, 0, a.status, abort_flag) && mbar_wait(&k_full[0], 0, a.status, abort_flag);
-      if (ok) {
-        tc::fence_after_sync();
-#pragma unroll
-        for (int t = 0; t < NQ; ++t)
-          if (nt[t] > 0) issue_s(t, 0);
-      }
-      for (int j = 0; ok && j < n; ++j) {
-        const int slot = j % C::NS;
-        if (!mbar_wait(&v_full[slot], (j / C::NS) & 1, a.status, abort_flag)) break;
-        tc::fence_after_sync();
-#pragma unroll
-        for (int t = 0; t < NQ; ++t) {
-          if (j >= nt[t]) continue;
-          if (!mbar_wait(&p_full[t], j & 1, a.status, abort_flag)) {
+      int kv = 0, qjobs = 0;
+      int ps[NQ] = {};  // P V steps issued per tile (p_full phases consumed)
+      bool ok = true;
+      for (int item = blockIdx.x; ok && item < a.total_items; item += gridDim.x) {
+        for (int half = 0; ok && half < 2; ++half) {
+          Job jb;
+          if (!make_job(a, item, half, jb) || jb.n == 0) continue;
+          const int g0 = kv;
+          if (!mbar_wait(q_full, qjobs & 1, a.status, abort_flag) ||
+              !mbar_wait(&k_full[g0 % C::NS], (g0 / C::NS) & 1, a.status, abort_flag)) {
             ok = false;
             break;
           }
           tc::fence_after_sync();
-          issue_pv(t, j);
-          if (j + 1 < nt[t]) {
-            if (!mbar_wait(&k_full[(j + 1) % C::NS], ((j + 1) / C::NS) & 1, a.status, abort_flag)) {
+          // S_t of the new job may overwrite S_t / P_t: the previous job's P_t V was issued before (in order).
+#pragma unroll
+          for (int t = 0; t < NQ; ++t)
+            if (jb.nt[t] > 0) issue_s(t, g0);
+          tc::mma_commit(&k_empty[g0 % C::NS]);
+          if (jb.n == 1) tc::mma_commit(q_empty);
+          for (int j = 0; ok && j < jb.n; ++j) {
+            const int g = g0 + j;
+            const int slot = g % C::NS;
+            if (!mbar_wait(&v_full[slot], (g / C::NS) & 1, a.status, abort_flag)) {
               ok = false;
               break;
             }
             tc::fence_after_sync();
-            issue_s(t, j + 1);  // S_t aliases P_t: issued after P_t V_j, the tensor pipe keeps the order
+            bool next_s = false;
+#pragma unroll
+            for (int t = 0; t < NQ; ++t) {
+              if (j >= jb.nt[t]) continue;
+              // P_t of step j; the job's first P V overwrites O_t, which the softmax group finished reading
+              // (its previous epilogue) before it produced this P
+              if (!mbar_wait(&p_full[t], ps[t] & 1, a.status, abort_flag)) {
+                ok = false;
+                break;
+              }
+              ++ps[t];
+              tc::fence_after_sync();
+              issue_pv(t, g, j == 0);
+              if (j + 1 < jb.nt[t]) {
+                if (!mbar_wait(&k_full[(g + 1) % C::NS], ((g + 1) / C::NS) & 1, a.status, abort_flag)) {
+                  ok = false;
+                  break;
+                }
+                tc::fence_after_sync();
+                issue_s(t, g + 1);  // S_t aliases P_t: issued after P_t V_j, the tensor pipe keeps the order
+                next_s = true;
+              }
+            }
+            if (!ok) break;
+            tc::mma_commit(&v_empty[slot]);                         // both P V_j issued
+            if (next_s) tc::mma_commit(&k_empty[(g + 1) % C::NS]);  // every S reading K_{j+1} issued
+            if (j == jb.n - 2) tc::mma_commit(q_empty);             // the job's last S MMAs are issued
           }
+          kv += jb.n;
+          ++qjobs;
         }
-        if (!ok) break;
-        tc::mma_commit(&kv_empty[slot]);
       }
       // Whatever happened, wait for every MMA issued above before TMEM is released.
       tc::mma_commit(drain);
@@ -283,144 +361,164 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ---------------- softmax + correction + epilogue: one thread per query row ----------------
-    const int t = (warp - kFirstSoftmaxWarp) >> 2;  // which query tile this group owns
+    const int t = (warp - kFirstSoftmaxWarp) >> 2;  // which query tile of each job this group owns
     const int quarter = warp & 3;                    // TMEM lane quarter this warp may access
     const int row = quarter * 32 + lane;             // row of the tile == TMEM lane
     const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
-    const int q0 = q00 + t * BM;
-    const int qi = q0 + row;                         // query index within its sequence
-    const int horizon = qi + off;                    // last visible key under the causal mask
-    const int my_n = nt[t];
     const float c = a.scale_log2;
     const uint32_t s_addr = tbase + lane_addr + C::tm_s(t);
     const uint32_t o_addr = tbase + lane_addr + C::tm_o(t);
-    float m_ref = -INFINITY;                         // running max, scaled log2 units
-    float l = 0.f;
+    int ss = 0;  // S steps of this tile consumed so far (s_full / o_done phases)
     bool ok = true;
 
-    for (int j = 0; j < my_n; ++j) {
-      if (!mbar_wait(&s_full[t], j & 1, a.status, abort_flag)) {
-        ok = false;
-        break;
-      }
-      tc::fence_after_sync();
-      uint32_t sr[4][32];
-#pragma unroll
-      for (int cc = 0; cc < 4; ++cc) tc::tmem_ld32(s_addr + cc * 32, sr[cc]);
-      tc::tmem_ld_wait();
+    for (int item = blockIdx.x; ok && item < a.total_items; item += gridDim.x) {
+      for (int half = 0; ok && half < 2; ++half) {
+        Job jb;
+        if (!make_job(a, item, half, jb)) continue;
+        const int q0 = jb.q00 + t * BM;
+        if (q0 >= jb.Lq_s) continue;                    // this tile lies past the sequence end
+        const int qi = q0 + row;                         // query index within its sequence
+        const int horizon = qi + jb.off;                 // last visible key under the causal mask
+        const int my_n = jb.nt[t];
+        float m_ref = -INFINITY;                         // running max, scaled log2 units
+        float l = 0.f;
 
-      const int kbase = j * BN;
-      const bool need_mask = (kbase + BN > Lkv_s) || (a.causal && kbase + BN - 1 > q0 + off);
-      if (need_mask) {
-        const int lim = a.causal ? min(Lkv_s - 1, horizon) : (Lkv_s - 1);
+        for (int j = 0; j < my_n; ++j) {
+          if (!mbar_wait(&s_full[t], ss & 1, a.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          ++ss;
+          tc::fence_after_sync();
+          uint32_t sr[4][32];
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc)
+          for (int cc = 0; cc < 4; ++cc) tc::tmem_ld32(s_addr + cc * 32, sr[cc]);
+          tc::tmem_ld_wait();
+
+          const int kbase = j * BN;
+          const bool need_mask = (kbase + BN > jb.Lkv_s) || (a.causal && kbase + BN - 1 > q0 + jb.off);
+          if (need_mask) {
+            const int lim = a.causal ? min(jb.Lkv_s - 1, horizon) : (jb.Lkv_s - 1);
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (kbase + cc * 32 + i > lim) sr[cc][i] = __float_as_uint(-INFINITY);
-      }
-      float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+            for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        mx0 = fmaxf(mx0, __uint_as_float(sr[0][i]));
-        mx1 = fmaxf(mx1, __uint_as_float(sr[1][i]));
-        mx2 = fmaxf(mx2, __uint_as_float(sr[2][i]));
-        mx3 = fmaxf(mx3, __uint_as_float(sr[3][i]));
-      }
-      const float mt = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c;
-      float alpha = 1.f;
-      if (mt > m_ref + kRescaleThreshold) {
-        alpha = ex2_approx(m_ref - mt);  // 0 when m_ref is still -inf
-        m_ref = mt;
-        l *= alpha;
-      }
-      const float neg = (m_ref == -INFINITY) ? 0.f : -m_ref;
-      const bool live = m_ref != -INFINITY;
-      float rs0 = 0.f, rs1 = 0.f;
-      uint32_t pk[2][32];
+              for (int i = 0; i < 32; ++i)
+                if (kbase + cc * 32 + i > lim) sr[cc][i] = __float_as_uint(-INFINITY);
+          }
+          float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
+          for (int i = 0; i < 32; ++i) {
+            mx0 = fmaxf(mx0, __uint_as_float(sr[0][i]));
+            mx1 = fmaxf(mx1, __uint_as_float(sr[1][i]));
+            mx2 = fmaxf(mx2, __uint_as_float(sr[2][i]));
+            mx3 = fmaxf(mx3, __uint_as_float(sr[3][i]));
+          }
+          const float mt = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c;
+          float alpha = 1.f;
+          if (mt > m_ref + kRescaleThreshold) {
+            alpha = ex2_approx(m_ref - mt);  // 0 when m_ref is still -inf
+            m_ref = mt;
+            l *= alpha;
+          }
+          const float neg = (m_ref == -INFINITY) ? 0.f : -m_ref;
+          const bool live = m_ref != -INFINITY;
+          float rs0 = 0.f, rs1 = 0.f;
+          uint32_t pk[2][32];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          float p0 = ex2_approx(fmaf(__uint_as_float(sr[cc][2 * i]), c, neg));
-          float p1 = ex2_approx(fmaf(__uint_as_float(sr[cc][2 * i + 1]), c, neg));
-          if (!live) p0 = p1 = 0.f;
-          rs0 += p0;
-          rs1 += p1;
-          pk[cc >> 1][(cc & 1) * 16 + i] = tc::pack_bf16x2(p0, p1);
+          for (int cc = 0; cc < 4; ++cc) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              float p0 = ex2_approx(fmaf(__uint_as_float(sr[cc][2 * i]), c, neg));
+              float p1 = ex2_approx(fmaf(__uint_as_float(sr[cc][2 * i + 1]), c, neg));
+              if (!live) p0 = p1 = 0.f;
+              rs0 += p0;
+              rs1 += p1;
+              pk[cc >> 1][(cc & 1) * 16 + i] = tc::pack_bf16x2(p0, p1);
+            }
+          }
+          l += rs0 + rs1;
+          // P_j (bf16) overwrites the first 64 columns of S_t
+          tc::tmem_st32(s_addr, pk[0]);
+          tc::tmem_st32(s_addr + 32, pk[1]);
+          // O_t correction.  S_t(j) completing implies P_t V_{j-1} completed (issued before it), so O_t is idle.
+          if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+            for (int cc = 0; cc < D / 32; ++cc) {
+              uint32_t orr[32];
+              tc::tmem_ld32(o_addr + cc * 32, orr);
+              tc::tmem_ld_wait();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
+              tc::tmem_st32(o_addr + cc * 32, orr);
+            }
+          }
+          tc::tmem_st_wait();
+          tc::fence_before_sync();
+          mbar_arrive(&p_full[t]);
         }
-      }
-      l += rs0 + rs1;
-      // P_j (bf16) overwrites the first 64 columns of S_t
-      tc::tmem_st32(s_addr, pk[0]);
-      tc::tmem_st32(s_addr + 32, pk[1]);
-      // O_t correction.  S_t(j) completing implies P_t V_{j-1} completed (issued before it), so O_t is idle.
-      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        if (!ok) break;
+
+        // ---------------- epilogue: O / l, lse ----------------
+        if (my_n > 0) {
+          // the job's last P V: o_done phase ss - 1 (earlier phases completed before S_t(last) did)
+          if (!mbar_wait(&o_done[t], (ss - 1) & 1, a.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc::fence_after_sync();
+        }
+        const bool store = qi < jb.Lq_s;
+        const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+        size_t orow;  // element offset of this row in out
+        if (a.varlen)
+          orow = ((size_t)(jb.q_start + qi) * a.Hq + jb.h) * D;
+        else
+          orow = (((size_t)jb.bs * a.Hq + jb.h) * a.Lq + qi) * D;
 #pragma unroll
         for (int cc = 0; cc < D / 32; ++cc) {
           uint32_t orr[32];
-          tc::tmem_ld32(o_addr + cc * 32, orr);
-          tc::tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
-          tc::tmem_st32(o_addr + cc * 32, orr);
-        }
-      }
-      tc::tmem_st_wait();
-      tc::fence_before_sync();
-      mbar_arrive(&p_full[t]);
-    }
-
-    // ---------------- epilogue: O / l, lse ----------------
-    if (ok && my_n > 0) {
-      ok = mbar_wait(&o_done[t], (my_n - 1) & 1, a.status, abort_flag);
-      tc::fence_after_sync();
-    }
-    const bool store = qi < Lq_s;
-    const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
-    size_t orow;  // element offset of this row in out
-    if (a.varlen)
-      orow = ((size_t)(q_start + qi) * a.Hq + h) * D;
-    else
-      orow = (((size_t)bs * a.Hq + h) * a.Lq + qi) * D;
-    if (ok) {
-#pragma unroll
-      for (int cc = 0; cc < D / 32; ++cc) {
-        uint32_t orr[32];
-        if (my_n > 0) {
-          tc::tmem_ld32(o_addr + cc * 32, orr);
-          tc::tmem_ld_wait();
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) orr[i] = 0u;
-        }
-        if (store) {
-          if (a.out_f32) {
-            float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(a.out) + orow + cc * 32);
-#pragma unroll
-            for (int v4 = 0; v4 < 8; ++v4)
-              dst[v4] = make_float4(__uint_as_float(orr[4 * v4]) * inv_l, __uint_as_float(orr[4 * v4 + 1]) * inv_l,
-                                    __uint_as_float(orr[4 * v4 + 2]) * inv_l, __uint_as_float(orr[4 * v4 + 3]) * inv_l);
+          if (my_n > 0) {
+            tc::tmem_ld32(o_addr + cc * 32, orr);
+            tc::tmem_ld_wait();
           } else {
-            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.out) + orow + cc * 32);
 #pragma unroll
-            for (int v4 = 0; v4 < 4; ++v4) {
-              uint4 w;
-              w.x = tc::pack_bf16x2(__uint_as_float(orr[8 * v4 + 0]) * inv_l, __uint_as_float(orr[8 * v4 + 1]) * inv_l);
-              w.y = tc::pack_bf16x2(__uint_as_float(orr[8 * v4 + 2]) * inv_l, __uint_as_float(orr[8 * v4 + 3]) * inv_l);
-              w.z = tc::pack_bf16x2(__uint_as_float(orr[8 * v4 + 4]) * inv_l, __uint_as_float(orr[8 * v4 + 5]) * inv_l);
-              w.w = tc::pack_bf16x2(__uint_as_float(orr[8 * v4 + 6]) * inv_l, __uint_as_float(orr[8 * v4 + 7]) * inv_l);
-              dst[v4] = w;
+            for (int i = 0; i < 32; ++i) orr[i] = 0u;
+          }
+          if (store) {
+            if (a.out_f32) {
+              float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(a.out) + orow + cc * 32);
+#pragma unroll
+              for (int v4 = 0; v4 < 8; ++v4)
+                dst[v4] = make_float4(__uint_as_float(orr[4 * v4]) * inv_l, __uint_as_float(orr[4 * v4 + 1]) * inv_l,
+                                      __uint_as_float(orr[4 * v4 + 2]) * inv_l,
+                                      __uint_as_float(orr[4 * v4 + 3]) * inv_l);
+            } else {
+              uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.out) + orow + cc * 32);
+#pragma unroll
+              for (int v4 = 0; v4 < 4; ++v4) {
+                uint4 w;
+                w.x = tc::pack_bf16x2(__uint_as_float(orr[8 * v4 + 0]) * inv_l,
+                                      __uint_as_float(orr[8 * v4 + 1]) * inv_l);
+                w.y = tc::pack_bf16x2(__uint_as_float(orr[8 * v4 + 2]) * inv_l,
+                                      __uint_as_float(orr[8 * v4 + 3]) * inv_l);
+                w.z = tc::pack_bf16x2(__uint_as_float(orr[8 * v4 + 4]) * inv_l,
+                                      __uint_as_float(orr[8 * v4 + 5]) * inv_l);
+                w.w = tc::pack_bf16x2(__uint_as_float(orr[8 * v4 + 6]) * inv_l,
+                                      __uint_as_float(orr[8 * v4 + 7]) * inv_l);
+                dst[v4] = w;
+              }
             }
           }
         }
-      }
-      if (store && a.lse != nullptr) {
-        const float lse = (l > 0.f) ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
-        if (a.varlen)
-          a.lse[(size_t)(q_start + qi) * a.Hq + h] = lse;
-        else
-          a.lse[((size_t)bs * a.Hq + h) * a.Lq + qi] = lse;
+        if (store && a.lse != nullptr) {
+          const float lse = (l > 0.f) ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
+          if (a.varlen)
+            a.lse[(size_t)(jb.q_start + qi) * a.Hq + jb.h] = lse;
+          else
+            a.lse[((size_t)jb.bs * a.Hq + jb.h) * a.Lq + qi] = lse;
+        }
+        // (the O_t reads above completed -- tcgen05.wait::ld -- before this group's next P is published,
+        //  which is what the next job's first P V waits for)
       }
     }
   }
@@ -483,12 +581,18 @@ cudaError_t launch_d(const PrefillLaunch& p) {
   a.causal = p.causal;
   a.out_f32 = p.out_f32;
   a.scale_log2 = p.scale * kLog2e;
-  a.npairs = (p.Lq + NQ * BM - 1) / (NQ * BM);
+  const int npairs = (p.Lq + NQ * BM - 1) / (NQ * BM);
+  a.ns = (npairs + 1) / 2;
   a.total_q = p.total_q;
   a.total_k = p.total_k;
   a.status = p.status;
-  if (p.Hq > 65535) return cudaErrorInvalidValue;
-  dim3 grid(a.npairs, p.Hq, p.B);
+  const long long items = (long long)p.B * p.Hq * a.ns;
+  if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
+  a.total_items = (int)items;
+  // persistent: one CTA per SM (shared memory allows no more), never more CTAs than items
+  int grid = p.num_sms > 0 ? p.num_sms : 148;
+  if (grid > a.total_items) grid = a.total_items;
+  if (grid < 1) grid = 1;
   prefill_fwd_kernel<D><<<grid, kThreads, C::SMEM_ALLOC, p.stream>>>(tmq, tmk, tmv, a);
   return cudaGetLastError();
 }

@@ -143,7 +143,7 @@ def test_workspace_bytes_formula(lib):
     assert lib.attn_decode_workspace_bytes(0, 8, 2, 64, 128, 0) == 0
     assert lib.attn_decode_workspace_bytes(1, 8, 2, 64, 100, 0) == 0
     sms = torch.cuda.get_device_properties(0).multi_processor_count if torch.cuda.is_available() else 148
-    grid = 2 * sms
+    grid = 3 * sms  # persistent decode: three CTAs per SM when a CTA serves 4 query heads
     # 256 KiB of counters + 2 partials per CTA x 4 heads per CTA x (D + 2) floats; independent of B, Lmax, chunk
     want = 65536 * 4 + 2 * grid * 4 * 130 * 4
     assert lib.attn_decode_workspace_bytes(2, 8, 2, 1000, 128, 256) == want
