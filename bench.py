@@ -60,11 +60,12 @@ def peaks():
                 "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
-def read_traffic(kernel: str):
-    """Per-launch DRAM bytes from the committed ncu summary, if it matches the current kernel source."""
+def read_traffic(kernel: str, workload: str):
+    """Per-launch DRAM bytes of `kernel` on `workload` from the committed ncu summary, or None when there is
+    none or the kernel source changed since the counters were taken."""
     import hashlib
 
-    path = os.path.join(ROOT, "profiles", f"{kernel}_traffic.txt")
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}_traffic.txt")
     if not os.path.exists(path):
         return None
     kv = {}
@@ -460,12 +461,12 @@ def run_ours(args):
     if case.kind == "hbm":
         peak, peak_src = pk["hbm_gbs"], pk["source"]
         roof = {"bound": "hbm", "achieved": per_gpu, "peak": peak, "unit": "GB/s", "frac": per_gpu / peak,
-                "traffic": read_traffic("decode_split"), "peak_source": peak_src,
+                "traffic": read_traffic("decode_split", case.w.name), "peak_source": peak_src,
                 "kernel": "decode_split_kernel (one attn_decode call: split pass with the combine fused, event-timed)"}
     else:
         peak, peak_src = pk["bf16_tflops"], pk["source"]
         roof = {"bound": "tensor", "achieved": per_gpu, "peak": peak, "unit": "TFLOP/s", "frac": per_gpu / peak,
-                "traffic": read_traffic("prefill_fwd"), "peak_source": peak_src,
+                "traffic": read_traffic("prefill_fwd", case.w.name), "peak_source": peak_src,
                 "kernel": "prefill_fwd_kernel (one attn_fwd call, event-timed)"}
 
     line = {
