@@ -87,7 +87,8 @@ struct PrefillArgs {
   int causal;
   int out_f32;
   float scale_log2;  // scale * log2(e)
-  int ns;            // work items per (sequence, head): pairs of tile pairs
+  int ns;            // work items per (sequence, head)
+  int single;        // 1: an item is one tile pair; 0: an item is the tile pairs np-1-s and s
   int total_items;   // B * Hq * ns
   int total_q, total_k;  // packed layout: rows of q/out and of k/v
   unsigned* status;
@@ -103,10 +104,11 @@ struct Job {
   int n;    // max nt: K/V steps of the job
 };
 
-// Work item `item` holds the tile pairs (np-1-s) and s of one (sequence, head), np being that
-// sequence's number of tile pairs: on a causal square the two cost the same in total, so equal
-// numbers of items per CTA balance.  `half` picks the heavy (0) or light (1) pair.  Returns false
-// when the job is empty (past the sequence end, the middle pair of an odd count, malformed offsets).
+// Work item `item` of one (sequence, head) holds either the tile pairs (np-1-s) and s, np being that
+// sequence's number of tile pairs -- on a causal square the two cost the same in total, so equal
+// numbers of items per persistent CTA balance -- or (single mode) just tile pair np-1-s.  `half` picks
+// the heavy (0) or light (1) pair.  Returns false when the job is empty (past the sequence end, the
+// middle pair of an odd count, malformed offsets).
 __device__ __forceinline__ bool make_job(const PrefillArgs& a, int item, int half, Job& jb) {
   const int s = item % a.ns;
   const int rest = item / a.ns;
@@ -134,7 +136,7 @@ __device__ __forceinline__ bool make_job(const PrefillArgs& a, int item, int hal
   if (half == 0) {
     pair = heavy;
   } else {
-    if (s >= heavy) return false;  // the middle pair of an odd count is done by half 0
+    if (a.single || s >= heavy) return false;  // the middle pair of an odd count is done by half 0
     pair = s;
   }
   if (pair < 0) return false;
@@ -405,38 +407,42 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int i = 0; i < 32; ++i)
                 if (kbase + cc * 32 + i > lim) sr[cc][i] = __float_as_uint(-INFINITY);
           }
-          float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+          // row max with three-input max (two new values per instruction), four independent chains
+          float mx[4];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            mx0 = fmaxf(mx0, __uint_as_float(sr[0][i]));
-            mx1 = fmaxf(mx1, __uint_as_float(sr[1][i]));
-            mx2 = fmaxf(mx2, __uint_as_float(sr[2][i]));
-            mx3 = fmaxf(mx3, __uint_as_float(sr[3][i]));
+          for (int cc = 0; cc < 4; ++cc) {
+            mx[cc] = __uint_as_float(sr[cc][0]);
+#pragma unroll
+            for (int i = 1; i < 31; i += 2)
+              mx[cc] = max3f(mx[cc], __uint_as_float(sr[cc][i]), __uint_as_float(sr[cc][i + 1]));
+            mx[cc] = fmaxf(mx[cc], __uint_as_float(sr[cc][31]));
           }
-          const float mt = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c;
+          const float mt = max3f(mx[0], mx[1], fmaxf(mx[2], mx[3])) * c;
           float alpha = 1.f;
           if (mt > m_ref + kRescaleThreshold) {
             alpha = ex2_approx(m_ref - mt);  // 0 when m_ref is still -inf
             m_ref = mt;
             l *= alpha;
           }
+          // p = 2^(s*c - m_ref): exponent arguments and row sums on packed fp32x2 FMAs/adds
           const float neg = (m_ref == -INFINITY) ? 0.f : -m_ref;
           const bool live = m_ref != -INFINITY;
-          float rs0 = 0.f, rs1 = 0.f;
+          const float2 c2 = make_float2(c, c), n2 = make_float2(neg, neg);
+          float2 rs[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
           uint32_t pk[2][32];
 #pragma unroll
           for (int cc = 0; cc < 4; ++cc) {
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-              float p0 = ex2_approx(fmaf(__uint_as_float(sr[cc][2 * i]), c, neg));
-              float p1 = ex2_approx(fmaf(__uint_as_float(sr[cc][2 * i + 1]), c, neg));
-              if (!live) p0 = p1 = 0.f;
-              rs0 += p0;
-              rs1 += p1;
-              pk[cc >> 1][(cc & 1) * 16 + i] = tc::pack_bf16x2(p0, p1);
+              const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[cc][2 * i]), __uint_as_float(sr[cc][2 * i + 1])),
+                                          c2, n2);
+              float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+              if (!live) pp = make_float2(0.f, 0.f);
+              rs[i & 1] = __fadd2_rn(rs[i & 1], pp);
+              pk[cc >> 1][(cc & 1) * 16 + i] = tc::pack_bf16x2(pp.x, pp.y);
             }
           }
-          l += rs0 + rs1;
+          l += (rs[0].x + rs[0].y) + (rs[1].x + rs[1].y);
           // P_j (bf16) overwrites the first 64 columns of S_t
           tc::tmem_st32(s_addr, pk[0]);
           tc::tmem_st32(s_addr + 32, pk[1]);
@@ -582,15 +588,20 @@ cudaError_t launch_d(const PrefillLaunch& p) {
   a.out_f32 = p.out_f32;
   a.scale_log2 = p.scale * kLog2e;
   const int npairs = (p.Lq + NQ * BM - 1) / (NQ * BM);
-  a.ns = (npairs + 1) / 2;
+  // Dense causal: persistent CTAs over items of two mirrored tile pairs (equal cost).  Otherwise item costs
+  // differ (packed sequences) or are all equal (non-causal), and one CTA per tile pair, heaviest first,
+  // balances better.
+  const bool persistent = !varlen && p.causal;
+  a.single = persistent ? 0 : 1;
+  a.ns = persistent ? (npairs + 1) / 2 : npairs;
   a.total_q = p.total_q;
   a.total_k = p.total_k;
   a.status = p.status;
   const long long items = (long long)p.B * p.Hq * a.ns;
   if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
   a.total_items = (int)items;
-  // persistent: one CTA per SM (shared memory allows no more), never more CTAs than items
-  int grid = p.num_sms > 0 ? p.num_sms : 148;
+  // persistent: one CTA per SM (shared memory allows no more); otherwise one CTA per item
+  int grid = persistent ? (p.num_sms > 0 ? p.num_sms : 148) : a.total_items;
   if (grid > a.total_items) grid = a.total_items;
   if (grid < 1) grid = 1;
   prefill_fwd_kernel<D><<<grid, kThreads, C::SMEM_ALLOC, p.stream>>>(tmq, tmk, tmv, a);
