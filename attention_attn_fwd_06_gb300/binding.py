@@ -37,6 +37,7 @@ EXPORTED = (
     "attn_decode",
     "attn_decode_ex",
     "attn_decode_noalloc",
+    "attn_decode_paged",
     "attn_decode_workspace_bytes",
     "attn_get_device_status",
     "attn_status_string",
@@ -60,6 +61,18 @@ class attn_fwd_params(ctypes.Structure):
         ("scale", ctypes.c_float), ("causal", ctypes.c_int), ("out_dtype", ctypes.c_int),
         ("cu_seqlens_q", ctypes.c_void_p), ("cu_seqlens_k", ctypes.c_void_p),
         ("total_q", ctypes.c_int), ("total_k", ctypes.c_int),
+        ("stream", ctypes.c_void_p),
+    ]
+
+
+class attn_decode_paged_params(ctypes.Structure):
+    _fields_ = [
+        ("q", ctypes.c_void_p), ("kpages", ctypes.c_void_p), ("vpages", ctypes.c_void_p),
+        ("block_table", ctypes.c_void_p), ("kv_lens", ctypes.c_void_p), ("out", ctypes.c_void_p),
+        ("lse", ctypes.c_void_p),
+        ("B", ctypes.c_int), ("Hq", ctypes.c_int), ("Hkv", ctypes.c_int), ("D", ctypes.c_int),
+        ("page_size", ctypes.c_int), ("max_pages", ctypes.c_int), ("num_pages", ctypes.c_int),
+        ("scale", ctypes.c_float), ("out_dtype", ctypes.c_int), ("chunk", ctypes.c_int),
         ("stream", ctypes.c_void_p),
     ]
 
@@ -99,6 +112,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.attn_decode_ex.restype = I
         lib.attn_decode_noalloc.argtypes = [ctypes.POINTER(attn_decode_params)]
         lib.attn_decode_noalloc.restype = I
+        lib.attn_decode_paged.argtypes = [ctypes.POINTER(attn_decode_paged_params)]
+        lib.attn_decode_paged.restype = I
         lib.attn_decode_workspace_bytes.argtypes = [I, I, I, I, I, I]
         lib.attn_decode_workspace_bytes.restype = ctypes.c_ulonglong
         lib.attn_get_device_status.argtypes = [P]
@@ -234,6 +249,40 @@ def attn_decode(q, kcache, vcache, kv_lens, out=None, lse=None, scale=None, chun
     p.chunk = int(chunk)
     p.stream = _stream_handle(stream, q.device)
     _check(load().attn_decode_ex(ctypes.byref(p)), "attn_decode")
+    return out, lse
+
+
+def attn_decode_paged(q, kpages, vpages, block_table, kv_lens, out=None, lse=None, scale=None, chunk=0,
+                      out_dtype=torch.bfloat16, want_lse=True, stream=None):
+    """Decode over a paged cache: pages [num_pages,Hkv,page_size,D] bf16, block_table int32 [B,max_pages]."""
+    _need(q, "q", torch.bfloat16, 3)
+    _need(kpages, "kpages", torch.bfloat16, 4)
+    _need(vpages, "vpages", torch.bfloat16, 4)
+    _need(block_table, "block_table", torch.int32, 2)
+    _need(kv_lens, "kv_lens", torch.int32, 1)
+    B, Hq, D = q.shape
+    num_pages, Hkv, page_size = kpages.shape[0], kpages.shape[1], kpages.shape[2]
+    if tuple(kpages.shape) != (num_pages, Hkv, page_size, D) or tuple(vpages.shape) != tuple(kpages.shape):
+        raise ValueError("page pool shapes do not match q")
+    if block_table.shape[0] != B or kv_lens.shape[0] != B:
+        raise ValueError("block_table and kv_lens must have B rows")
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=out_dtype, device=q.device)
+    _need(out, "out", out_dtype, 3)
+    if lse is None and want_lse:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, 2)
+    p = attn_decode_paged_params()
+    p.q, p.kpages, p.vpages = _ptr(q), _ptr(kpages), _ptr(vpages)
+    p.block_table, p.kv_lens, p.out, p.lse = _ptr(block_table), _ptr(kv_lens), _ptr(out), _ptr(lse)
+    p.B, p.Hq, p.Hkv, p.D = B, Hq, Hkv, D
+    p.page_size, p.max_pages, p.num_pages = page_size, block_table.shape[1], num_pages
+    p.scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    p.out_dtype = ATTN_DTYPE_F32 if out_dtype == torch.float32 else ATTN_DTYPE_BF16
+    p.chunk = int(chunk)
+    p.stream = _stream_handle(stream, q.device)
+    _check(load().attn_decode_paged(ctypes.byref(p)), "attn_decode_paged")
     return out, lse
 
 

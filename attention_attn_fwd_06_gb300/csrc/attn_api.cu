@@ -238,7 +238,7 @@ int attn_decode_ex(const attn_decode_params* p) {
   const DecodeShape sh = decode_shape(p->Hq, p->Hkv, p->D, s->num_sms);
   st = ensure_workspace_locked(*s, sh.bytes, stream);
   if (st != ATTN_OK) return st;
-  attn::DecodeLaunch L;
+  attn::DecodeLaunch L{};
   L.q = p->q;
   L.kcache = p->kcache;
   L.vcache = p->vcache;
@@ -291,7 +291,7 @@ int attn_decode_noalloc(const attn_decode_params* p) {
   const DecodeShape sh = decode_shape(p->Hq, p->Hkv, p->D, s->num_sms);
   if (2 + decode_counter_rows(p->B, p->Hq, p->Hkv) > attn::kDecodeCounterSlots || sh.bytes > kNoAllocScratchBytes)
     return ATTN_ERR_SCRATCH_TOO_SMALL;
-  attn::DecodeLaunch L;
+  attn::DecodeLaunch L{};
   L.q = p->q;
   L.kcache = p->kcache;
   L.vcache = p->vcache;
@@ -311,6 +311,70 @@ int attn_decode_noalloc(const attn_decode_params* p) {
   L.out_f32 = p->out_dtype == ATTN_DTYPE_F32;
   L.status = s->status;
   L.stream = static_cast<cudaStream_t>(p->stream);
+  return map_cuda(attn::launch_decode(L, s->num_sms));
+}
+
+int attn_decode_paged(const attn_decode_paged_params* pp) {
+  if (pp == nullptr) return ATTN_ERR_INVALID_ARG;
+  if (pp->page_size < 8 || pp->page_size > 65536 || pp->max_pages < 1 || pp->num_pages < 1)
+    return ATTN_ERR_INVALID_ARG;
+  const long long lmax = (long long)pp->max_pages * pp->page_size;
+  if (lmax > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+  // Validate everything else as the contiguous call does (same meaning of every other field).
+  attn_decode_params p = {};
+  p.q = pp->q;
+  p.kcache = pp->kpages;
+  p.vcache = pp->vpages;
+  p.kv_lens = pp->kv_lens;
+  p.out = pp->out;
+  p.lse = pp->lse;
+  p.B = pp->B;
+  p.Hq = pp->Hq;
+  p.Hkv = pp->Hkv;
+  p.Lmax = (int)lmax;
+  p.D = pp->D;
+  p.scale = pp->scale;
+  p.out_dtype = pp->out_dtype;
+  p.chunk = pp->chunk;
+  p.stream = pp->stream;
+  int st = validate_decode(&p);
+  if (st != ATTN_OK) return st;
+  if (p.B == 0) return ATTN_OK;
+  if (pp->block_table == nullptr) return ATTN_ERR_INVALID_ARG;
+  if (!aligned4(pp->block_table)) return ATTN_ERR_ALIGNMENT;
+  cudaStream_t stream = static_cast<cudaStream_t>(p.stream);
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState* s = nullptr;
+  st = device_state_locked(&s);
+  if (st != ATTN_OK) return st;
+  if (2 + decode_counter_rows(p.B, p.Hq, p.Hkv) > attn::kDecodeCounterSlots) return ATTN_ERR_UNSUPPORTED;
+  const DecodeShape sh = decode_shape(p.Hq, p.Hkv, p.D, s->num_sms);
+  st = ensure_workspace_locked(*s, sh.bytes, stream);
+  if (st != ATTN_OK) return st;
+  attn::DecodeLaunch L{};
+  L.q = p.q;
+  L.kcache = p.kcache;
+  L.vcache = p.vcache;
+  L.block_table = pp->block_table;
+  L.page_size = pp->page_size;
+  L.max_pages = pp->max_pages;
+  L.num_pages = pp->num_pages;
+  L.kv_lens = p.kv_lens;
+  L.out = p.out;
+  L.lse = p.lse;
+  L.counters = static_cast<unsigned*>(s->ws);
+  L.part_o = reinterpret_cast<float*>(static_cast<char*>(s->ws) + kCounterBytes);
+  L.part_ml = L.part_o + sh.part_o_elems;
+  L.B = p.B;
+  L.Hq = p.Hq;
+  L.Hkv = p.Hkv;
+  L.Lmax = p.Lmax;
+  L.D = p.D;
+  L.min_keys = p.chunk > 0 ? p.chunk : 64;
+  L.scale = p.scale;
+  L.out_f32 = p.out_dtype == ATTN_DTYPE_F32;
+  L.status = s->status;
+  L.stream = stream;
   return map_cuda(attn::launch_decode(L, s->num_sms));
 }
 
@@ -346,7 +410,7 @@ int attn_fwd_ex(const attn_fwd_params* p) {
     st = device_state_locked(&s);
   }
   if (st != ATTN_OK) return st;
-  attn::PrefillLaunch L;
+  attn::PrefillLaunch L{};
   L.q = p->q;
   L.k = p->k;
   L.v = p->v;

@@ -22,7 +22,8 @@
 //    One CTA serves ALL the query heads of its group, so every K/V byte is
 //    read from HBM once (the decoder page's "load each K/V block once, reuse it
 //    for all queries of the step").
-//  * A producer warp walks the slice and streams K and V rows (and, on a row
+//  * A producer warp walks the slice and streams K and V rows (contiguous
+//    cache, or pages of a paged cache through its block table) (and, on a row
 //    piece's first stage, its q vectors) into a shared-memory ring (2-3 stages)
 //    with 1-D bulk copies on the TMA engine (cp.async.bulk, mbarrier
 //    completion), running ahead of the consumers across row boundaries.
@@ -159,7 +160,8 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS, DecodeCfg<D, GP>::M
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, off);
     __syncwarp();
-    if (lane != 0) return;
+    // The whole producer warp walks the slice in lock-step (lane 0 issues copies and barrier operations;
+    // the other lanes fetch page-table windows for the paged layout).
     auto seq_len = [&](int b) -> int { return b < C::LENS_CACHE ? lens_s[b] : clamp_len(p.kv_lens[b], p.Lmax); };
     const long long W = wsum * Hg;
     // At least min_keys keys per CTA; CTAs past the effective grid only handle empty sequences.
@@ -172,37 +174,86 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS, DecodeCfg<D, GP>::M
 
     int t = 0;  // stages issued
     bool ok = true;
+    const bool paged = p.block_table != nullptr;
+    // Paged layout: lane i holds the page id of page (win_base + i) of sequence win_b.
+    int win_b = -1, win_base = 0, my_page = 0;
+    auto load_window = [&](int b, int first_page) {
+      win_b = b;
+      win_base = first_page;
+      const int pg = first_page + lane;
+      my_page = 0;
+      if (pg < p.max_pages) {
+        const int id = p.block_table[(size_t)b * p.max_pages + pg];
+        if (id < 0 || id >= p.num_pages) {
+          record_status(p.status, ATTN_ERR_DEVICE_BOUNDS);  // out-of-pool page id: read page 0 instead
+        } else {
+          my_page = id;
+        }
+      }
+      __syncwarp();
+    };
+    // Copy keys [k0, k0 + nk) of row (b, hkv) to shared memory at dst (K) and dstv (V).
+    auto copy_keys = [&](int b, int hkv, int k0, int nk, __nv_bfloat16* dstk, __nv_bfloat16* dstv, uint64_t* bar) {
+      if (!paged) {
+        if (lane == 0) {
+          const size_t row0 = ((size_t)b * p.Hkv + hkv) * (size_t)p.Lmax + (size_t)k0;
+          const uint32_t bytes = (uint32_t)nk * D * 2;
+          bulk_g2s(dstk, reinterpret_cast<const __nv_bfloat16*>(p.kcache) + row0 * D, bytes, bar);
+          bulk_g2s(dstv, reinterpret_cast<const __nv_bfloat16*>(p.vcache) + row0 * D, bytes, bar);
+        }
+        return;
+      }
+      const int ps = p.page_size;
+      const int first = k0 / ps, last = (k0 + nk - 1) / ps;
+      if (b != win_b || first < win_base || last >= win_base + 32) load_window(b, first);
+      int k = k0, done = 0;
+      for (int pg = first; pg <= last; ++pg) {
+        const int page = __shfl_sync(0xffffffffu, my_page, pg - win_base);
+        const int off = k - pg * ps;
+        const int n = min(ps - off, nk - done);
+        if (lane == 0) {
+          const size_t row0 = ((size_t)page * p.Hkv + hkv) * (size_t)ps + (size_t)off;
+          const uint32_t bytes = (uint32_t)n * D * 2;
+          bulk_g2s(dstk + done * D, reinterpret_cast<const __nv_bfloat16*>(p.kcache) + row0 * D, bytes, bar);
+          bulk_g2s(dstv + done * D, reinterpret_cast<const __nv_bfloat16*>(p.vcache) + row0 * D, bytes, bar);
+        }
+        k += n;
+        done += n;
+      }
+    };
+    auto wait_empty = [&](int slot_r) -> bool {
+      int okw = 1;
+      if (lane == 0) okw = mbar_wait(&empty[slot_r], ((t / C::NS) - 1) & 1, p.status, abort_flag) ? 1 : 0;
+      return __shfl_sync(0xffffffffu, okw, 0) != 0;
+    };
+
     auto emit = [&](int b, int hg, int kb, int ke, int np, int slot, int cta_lo, int lo_odd) -> bool {
       // stream keys [kb, ke) of row (b, hg); ke == kb emits a single key-less stage
       const int hkv = hg / ngroups;
       const int hq0 = hkv * group + (hg - hkv * ngroups) * GP;
-      const size_t kv_row0 = ((size_t)b * p.Hkv + hkv) * (size_t)p.Lmax + (size_t)kb;
-      const __nv_bfloat16* kg = reinterpret_cast<const __nv_bfloat16*>(p.kcache) + kv_row0 * D;
-      const __nv_bfloat16* vg = reinterpret_cast<const __nv_bfloat16*>(p.vcache) + kv_row0 * D;
       const __nv_bfloat16* qg = reinterpret_cast<const __nv_bfloat16*>(p.q) + ((size_t)b * p.Hq + hq0) * D;
       const int nkeys = ke - kb;
       const int nst = nkeys > 0 ? (nkeys + C::SK - 1) / C::SK : 1;
       for (int u = 0; u < nst; ++u, ++t) {
         const int slot_r = t % C::NS;
-        if (t >= C::NS && !mbar_wait(&empty[slot_r], ((t / C::NS) - 1) & 1, p.status, abort_flag)) return false;
+        if (t >= C::NS && !wait_empty(slot_r)) return false;
         const int nk = nkeys > 0 ? min(C::SK, nkeys - u * C::SK) : 0;
-        StageInfo si;
-        si.b = b;
-        si.hg = hg;
-        si.nk = nk;
-        si.flags = (u == 0 ? 1 : 0) | (u == nst - 1 ? 2 : 0);
-        si.np = np;
-        si.slot = slot;
-        si.cta_lo = cta_lo;
-        si.lo_odd = lo_odd;
-        info[slot_r] = si;
-        const uint32_t bytes = (uint32_t)nk * D * 2;
-        mbar_arrive_expect_tx(&full[slot_r], 2 * bytes + (u == 0 ? (uint32_t)C::Q_BYTES : 0u));
-        if (nk > 0) {
-          bulk_g2s(Ks + slot_r * C::TILE_ELEMS, kg + (size_t)u * C::SK * D, bytes, &full[slot_r]);
-          bulk_g2s(Vs + slot_r * C::TILE_ELEMS, vg + (size_t)u * C::SK * D, bytes, &full[slot_r]);
+        if (lane == 0) {
+          StageInfo si;
+          si.b = b;
+          si.hg = hg;
+          si.nk = nk;
+          si.flags = (u == 0 ? 1 : 0) | (u == nst - 1 ? 2 : 0);
+          si.np = np;
+          si.slot = slot;
+          si.cta_lo = cta_lo;
+          si.lo_odd = lo_odd;
+          info[slot_r] = si;
+          mbar_arrive_expect_tx(&full[slot_r], 2u * (uint32_t)nk * D * 2 + (u == 0 ? (uint32_t)C::Q_BYTES : 0u));
+          if (u == 0) bulk_g2s(Qs + slot_r * C::Q_BYTES, qg, C::Q_BYTES, &full[slot_r]);
         }
-        if (u == 0) bulk_g2s(Qs + slot_r * C::Q_BYTES, qg, C::Q_BYTES, &full[slot_r]);
+        if (nk > 0)
+          copy_keys(b, hkv, kb + u * C::SK, nk, Ks + slot_r * C::TILE_ELEMS, Vs + slot_r * C::TILE_ELEMS, &full[slot_r]);
       }
       return true;
     };
@@ -250,12 +301,14 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS, DecodeCfg<D, GP>::M
     if (ok) {
       // end-of-work marker
       const int slot_r = t % C::NS;
-      if (t < C::NS || mbar_wait(&empty[slot_r], ((t / C::NS) - 1) & 1, p.status, abort_flag)) {
-        info[slot_r].b = -1;
-        mbar_arrive(&full[slot_r]);
+      if (t < C::NS || wait_empty(slot_r)) {
+        if (lane == 0) {
+          info[slot_r].b = -1;
+          mbar_arrive(&full[slot_r]);
+        }
       }
     }
-    if (*abort_flag) {
+    if (lane == 0 && *abort_flag) {
       // Let copies already in flight land before the CTA's shared memory is released.
       for (int u = (t > C::NS ? t - C::NS : 0); u < t; ++u)
         mbar_wait(&full[u % C::NS], (u / C::NS) & 1, p.status, nullptr);
@@ -484,12 +537,12 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS, DecodeCfg<D, GP>::M
       named_bar_sync(1, nct);
       if (ctid == 0) {
         const unsigned ctr = 2u + (unsigned)(si.b * Hg + si.hg);
-        __threadfence();
+        fence_acq_rel_gpu();  // release: the CTA's partial (ordered before by the barrier) is visible first
         const unsigned old = atomicAdd(&p.counters[ctr], 1u);
         const int is_last = (old == (unsigned)si.np - 1u);
         if (is_last) {
           atomicExch(&p.counters[ctr], 0u);  // re-arm for the next call
-          __threadfence();                   // acquire: the other CTAs' partials are visible from here on
+          fence_acq_rel_gpu();               // acquire: the other CTAs' partials are visible from here on
         }
         *last_flag = is_last;
       }

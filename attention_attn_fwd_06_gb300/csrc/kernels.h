@@ -9,8 +9,10 @@ namespace attn {
 // Split-KV decode (the split pass writes fp32 partials, the combine merges them).
 struct DecodeLaunch {
   const void* q;        // bf16 [B, Hq, D]
-  const void* kcache;   // bf16 [B, Hkv, Lmax, D]
-  const void* vcache;   // bf16 [B, Hkv, Lmax, D]
+  const void* kcache;   // bf16 [B, Hkv, Lmax, D], or the page pool [num_pages, Hkv, page_size, D]
+  const void* vcache;   // same layout as kcache
+  const int* block_table;  // null: contiguous cache; else int32 [B, max_pages] page ids (Lmax = max_pages*page_size)
+  int page_size, max_pages, num_pages;
   const int* kv_lens;   // int32 [B] (device)
   void* out;            // [B, Hq, D], bf16 or fp32
   float* lse;           // fp32 [B, Hq] or null

@@ -18,7 +18,7 @@ from dataclasses import dataclass, field
 
 import torch
 
-__all__ = ["Workload", "WORKLOADS", "make_prefill", "make_decode", "make_varlen", "randn_bf16"]
+__all__ = ["Workload", "WORKLOADS", "make_prefill", "make_decode", "make_varlen", "make_pages", "randn_bf16"]
 
 
 @dataclass(frozen=True)
@@ -48,6 +48,8 @@ WORKLOADS = {
     for w in [
         Workload("tiny_causal", "prefill", 1000, B=1, Hq=2, Hkv=2, D=64, L=128, causal=True, out_f32=True),
         Workload("decode_gqa", "decode", 1001, B=8, Hq=32, Hkv=8, D=128, L=4096, kv_range=(512, 4096)),
+        Workload("decode_gqa_paged16", "decode", 1001, B=8, Hq=32, Hkv=8, D=128, L=4096, kv_range=(512, 4096),
+                 extra={"page_size": 16}),
         Workload("decode_long", "decode", 1002, B=4, Hq=32, Hkv=8, D=128, L=131072,
                  kv_lens=(32768, 65536, 98304, 131072)),
         Workload("prefill_causal", "prefill", 1003, B=4, Hq=32, Hkv=32, D=128, L=4096, causal=True),
@@ -125,3 +127,29 @@ def make_varlen(nseq, Hq, Hkv, D, seed, seqlens=None, seq_range=None):
     k = randn_bf16((total, Hkv, D), g)
     v = randn_bf16((total, Hkv, D), g)
     return q, k, v, torch.tensor(cu, dtype=torch.int32)
+
+
+def make_pages(kcache, vcache, page_size, seed, spare_pages=3, fill_unused=float("nan")):
+    """Scatter a contiguous cache [B,Hkv,Lmax,D] into a page pool [num_pages,Hkv,page_size,D].
+
+    Pages are placed at a seeded random permutation of pool slots; block_table
+    [B, max_pages] (int32) lists them per sequence.  Pool pages no sequence uses,
+    and rows past Lmax in the last page, hold ``fill_unused`` (NaN by default) so
+    a read of them shows up in the output.
+    """
+    B, Hkv, Lmax, D = kcache.shape
+    max_pages = (Lmax + page_size - 1) // page_size
+    num_pages = B * max_pages + spare_pages
+    g = _gen(seed)
+    perm = torch.randperm(num_pages, generator=g)
+    kp = torch.full((num_pages, Hkv, page_size, D), fill_unused, dtype=kcache.dtype)
+    vp = torch.full((num_pages, Hkv, page_size, D), fill_unused, dtype=vcache.dtype)
+    table = torch.empty((B, max_pages), dtype=torch.int32)
+    for b in range(B):
+        for i in range(max_pages):
+            pid = int(perm[b * max_pages + i])
+            table[b, i] = pid
+            lo, hi = i * page_size, min(Lmax, (i + 1) * page_size)
+            kp[pid, :, : hi - lo] = kcache[b, :, lo:hi]
+            vp[pid, :, : hi - lo] = vcache[b, :, lo:hi]
+    return kp, vp, table

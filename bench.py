@@ -155,7 +155,15 @@ class DecodeCase:
         self.w = w
         q, kc, vc, lens = make_decode(w.B, w.Hq, w.Hkv, w.L, w.D, w.seed,
                                       kv_lens=w.kv_lens or None, kv_range=w.kv_range or None)
-        self.host = [t.pin_memory() for t in (q, kc, vc, lens)]
+        self.page_size = w.extra.get("page_size")
+        self.oracle_host = (q, kc, vc)
+        if self.page_size:
+            from attention_attn_fwd_06_gb300.inputs import make_pages
+
+            kp, vp, table = make_pages(kc, vc, self.page_size, w.seed + 7, fill_unused=0.0)
+            self.host = [t.pin_memory() for t in (q, kp, vp, lens, table)]
+        else:
+            self.host = [t.pin_memory() for t in (q, kc, vc, lens)]
         self.dev = [t.to(device) for t in self.host]
         self.out = torch.empty((w.B, w.Hq, w.D), dtype=torch.bfloat16, device=device)
         self.lse = torch.empty((w.B, w.Hq), dtype=torch.float32, device=device)
@@ -170,19 +178,23 @@ class DecodeCase:
         self.h2d = sum(t.numel() * t.element_size() for t in self.host)
         self.d2h = self.out.numel() * 2 + self.lse.numel() * 4
 
-    def step(self):
+    def _call(self):
         from attention_attn_fwd_06_gb300 import binding as AB
 
-        q, kc, vc, lens = self.dev
-        AB.attn_decode(q, kc, vc, lens, out=self.out, lse=self.lse, scale=self.w.scale)
+        if self.page_size:
+            q, kp, vp, lens, table = self.dev
+            AB.attn_decode_paged(q, kp, vp, table, lens, out=self.out, lse=self.lse, scale=self.w.scale)
+        else:
+            q, kc, vc, lens = self.dev
+            AB.attn_decode(q, kc, vc, lens, out=self.out, lse=self.lse, scale=self.w.scale)
+
+    def step(self):
+        self._call()
 
     def step_e2e(self):
-        from attention_attn_fwd_06_gb300 import binding as AB
-
         for d, h in zip(self.dev, self.host):
             d.copy_(h, non_blocking=True)
-        q, kc, vc, lens = self.dev
-        AB.attn_decode(q, kc, vc, lens, out=self.out, lse=self.lse, scale=self.w.scale)
+        self._call()
         self.out_h.copy_(self.out, non_blocking=True)
         self.lse_h.copy_(self.lse, non_blocking=True)
 
@@ -291,7 +303,7 @@ def run_oracle_pool(case, budget_s):
     cores = os.cpu_count() or 1
     units = []
     if isinstance(case, DecodeCase):
-        q, kc, vc = (t.float().numpy() for t in case.host[:3])
+        q, kc, vc = (t.float().numpy() for t in case.oracle_host)
         g = w.Hq // w.Hkv
         for b in range(w.B):
             for h in range(w.Hq):
@@ -365,6 +377,8 @@ def workload_config(case):
     if w.kind == "decode":
         cfg.update({"Lmax": w.L, "kv_lens": "uniform [%d, %d]" % w.kv_range if w.kv_range else list(w.kv_lens),
                     "kv_tokens_total": sum(case.lens)})
+        if w.extra.get("page_size"):
+            cfg["page_size"] = w.extra["page_size"]
     elif w.kind == "varlen":
         cfg.update({"nseq": w.B, "seq_range": list(w.seq_range), "total_tokens": sum(case.seqlens),
                     "causal": w.causal})

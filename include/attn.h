@@ -174,6 +174,44 @@ typedef struct attn_decode_params {
 int attn_decode_ex(const attn_decode_params* p);
 
 /*
+ * attn_decode_paged_params / attn_decode_paged -- decode over a paged KV cache
+ * (the serving form of the cache: fixed-size pages from a shared pool, listed
+ * per sequence in a block table, as in PagedAttention, which "Что такое kernel
+ * fusion и как он применяется в LLM serving?" §6 names).  Same computation
+ * and results as attn_decode_ex on the cache the pages describe.
+ *
+ *   kpages, vpages  bf16 [num_pages, Hkv, page_size, D]: page g of kv head h
+ *                   holds page_size consecutive key (value) rows
+ *   block_table     DEVICE int32 [B, max_pages]: entry (b, i) is the pool page
+ *                   holding keys i*page_size .. (i+1)*page_size-1 of sequence b
+ *   kv_lens         DEVICE int32 [B], at most max_pages * page_size (clamped
+ *                   and flagged otherwise, as in attn_decode)
+ *   page_size       keys per page, 8 .. 65536 (any value, not only powers of 2)
+ *   max_pages       columns of block_table; num_pages rows of the pool.  A page
+ *                   id outside [0, num_pages) is flagged ATTN_ERR_DEVICE_BOUNDS
+ *                   in the device status word and page 0 is read instead.
+ *   other fields    as attn_decode_params (q, out, lse, B, Hq, Hkv, D, scale,
+ *                   out_dtype, chunk, stream); same workspace as attn_decode_ex.
+ */
+typedef struct attn_decode_paged_params {
+  const void* q;
+  const void* kpages;
+  const void* vpages;
+  const int* block_table;
+  const int* kv_lens;
+  void* out;
+  float* lse;
+  int B, Hq, Hkv, D;
+  int page_size, max_pages, num_pages;
+  float scale;
+  int out_dtype;
+  int chunk;
+  void* stream;
+} attn_decode_paged_params;
+
+int attn_decode_paged(const attn_decode_paged_params* p);
+
+/*
  * attn_decode_workspace_bytes -- bytes of split-KV workspace a decode call
  * with these sizes needs (0 on invalid sizes).  It depends on Hq / Hkv, D and
  * the current device's SM count (148 assumed when no device is visible), not

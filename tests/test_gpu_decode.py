@@ -15,7 +15,7 @@ import torch
 import oracle
 from attention_attn_fwd_06_gb300 import binding as AB
 from attention_attn_fwd_06_gb300.build import build
-from attention_attn_fwd_06_gb300.inputs import WORKLOADS, make_decode
+from attention_attn_fwd_06_gb300.inputs import WORKLOADS, make_decode, make_pages
 from tests._parity import assert_attn_close
 
 pytestmark = pytest.mark.gpu
@@ -153,4 +153,38 @@ def test_decode_workload_long_sampled():
     assert_attn_close(O[torch.as_tensor(bi), torch.as_tensor(hi)], lse[torch.as_tensor(bi), torch.as_tensor(hi)],
                       O_ref[bi, hi], lse_ref[bi, hi], "decode_long")
     assert torch.isfinite(O).all() and torch.isfinite(lse).all()
+    assert AB.attn_get_device_status() == AB.ATTN_OK
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Lmax,D,page_size", [
+    (3, 16, 4, 700, 128, 16),    # vLLM-sized pages, 4 heads per kv head
+    (3, 16, 4, 700, 128, 48),    # a page size that is not a power of two
+    (2, 32, 8, 1000, 128, 256),  # pages longer than a pipeline stage
+    (2, 8, 8, 333, 64, 32),      # D = 64, MHA
+    (1, 16, 2, 129, 128, 8),     # smallest page size, 8 heads per kv head
+])
+def test_decode_paged_matches_contiguous_and_oracle(B, Hq, Hkv, Lmax, D, page_size):
+    q, kc, vc, lens = make_decode(B, Hq, Hkv, Lmax, D, seed=900 + page_size, kv_range=(1, Lmax))
+    kp, vp, table = make_pages(kc, vc, page_size, seed=901)
+    dev = torch.device("cuda:0")
+    scale = D ** -0.5
+    for chunk in (0, 7):
+        Oc, lc = AB.attn_decode(q.to(dev), kc.to(dev), vc.to(dev), lens.to(dev), scale=scale, chunk=chunk)
+        Op, lp = AB.attn_decode_paged(q.to(dev), kp.to(dev), vp.to(dev), table.to(dev), lens.to(dev), scale=scale,
+                                      chunk=chunk)
+        torch.cuda.synchronize()
+        # same keys in the same stages: the paged result is bitwise the contiguous one
+        assert torch.equal(Op.cpu(), Oc.cpu()) and torch.equal(lp.cpu(), lc.cpu())
+    O_ref, lse_ref = oracle.decode(q, kc, vc, lens.tolist(), scale)
+    assert_attn_close(Op.cpu(), lp.cpu(), O_ref, lse_ref)
+    assert AB.attn_get_device_status() == AB.ATTN_OK
+
+
+def test_decode_paged_bad_page_id_is_flagged():
+    q, kc, vc, lens = make_decode(2, 8, 2, 64, 128, seed=77)
+    kp, vp, table = make_pages(kc, vc, 16, seed=78, fill_unused=0.0)
+    table[1, 2] = kp.shape[0] + 5  # outside the pool
+    dev = torch.device("cuda:0")
+    AB.attn_decode_paged(q.to(dev), kp.to(dev), vp.to(dev), table.to(dev), lens.to(dev))
+    assert AB.attn_get_device_status() == AB.ATTN_ERR_DEVICE_BOUNDS
     assert AB.attn_get_device_status() == AB.ATTN_OK
