@@ -68,7 +68,7 @@ struct DecodeCfg {
   static constexpr int MINB = (GP >= 8) ? 2 : 3;             // resident CTAs per SM (register budget)
   static constexpr int NS = (MINB == 3) ? 2 : 3;              // ring stages
   static constexpr int THREADS = 32 * (NW + 1);
-  static constexpr int LENS_CACHE = 512;                      // kv_lens kept in shared memory for the walk
+  static constexpr int LENS_CACHE = (GP >= 8) ? 128 : 512;   // kv_lens kept in shared memory for the walk
   static constexpr int TILE_ELEMS = SK * D;
   static constexpr int TILE_BYTES = TILE_ELEMS * 2;
   static constexpr int Q_BYTES = GP * D * 2;                  // q of the group's heads (bf16)
@@ -76,8 +76,8 @@ struct DecodeCfg {
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + NS * TILE_BYTES;
   static constexpr int OFF_Q = OFF_V + NS * TILE_BYTES;
-  static constexpr int OFF_O = OFF_Q + NS * Q_BYTES;          // obuf[GP][D] fp32 (merge)
-  static constexpr int OFF_BAR = OFF_O + GP * D * 4;          // full[NS], empty[NS]
+  static constexpr int OFF_O = OFF_Q + NS * Q_BYTES;          // obuf[2][GP][D] fp32 (merge; also combine weights)
+  static constexpr int OFF_BAR = OFF_O + 2 * GP * D * 4;      // full[NS], empty[NS]
   static constexpr int OFF_INFO = OFF_BAR + 2 * NS * 8;       // StageInfo[NS]
   static constexpr int OFF_P = OFF_INFO + NS * 32;            // pbuf[NW][32]
   static constexpr int OFF_A = OFF_P + NW * 32 * 4;           // abuf[NW][GP]
@@ -143,7 +143,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS, DecodeCfg<D, GP>::M
     *abort_flag = 0;
     fence_mbar_init();
   }
-  for (int i = threadIdx.x; i < GP * D; i += blockDim.x) obuf[i] = 0.f;
+  for (int i = threadIdx.x; i < 2 * GP * D; i += blockDim.x) obuf[i] = 0.f;
   __syncthreads();
 
   if (warp == C::NW) {
@@ -479,11 +479,12 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS, DecodeCfg<D, GP>::M
       lbuf[warp * GP + sub] = lsum;
     }
     named_bar_sync(1, nct);
-    // Warps add their rescaled O into obuf one after another (a fixed order keeps results bitwise
-    // reproducible); obuf is zero on entry.
+    // Warp w adds its rescaled O into buffer w % 2 on turn w / 2: two warps at a time, in a fixed order (bitwise
+    // reproducible); both buffers are zero on entry.
 #pragma unroll 1
-    for (int w = 0; w < C::NW; ++w) {
-      if (warp == w && rw == 0) {
+    for (int turn = 0; turn < (C::NW + 1) / 2; ++turn) {
+      if ((warp >> 1) == turn && rw == 0) {
+        float* buf = obuf + (warp & 1) * GP * D;
 #pragma unroll
         for (int g = 0; g < GP; ++g) {
           float M = -INFINITY;
@@ -491,7 +492,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS, DecodeCfg<D, GP>::M
           for (int w2 = 0; w2 < C::NW; ++w2) M = fmaxf(M, mbuf[w2 * GP + g]);
           const float mw = mbuf[warp * GP + g];
           const float e = (mw == -INFINITY) ? 0.f : ex2_approx(mw - M);
-          float* dst = obuf + g * D + 8 * sub;
+          float* dst = buf + g * D + 8 * sub;
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             dst[2 * j] = fmaf(e, o[g][j].x, dst[2 * j]);
@@ -515,8 +516,9 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS, DecodeCfg<D, GP>::M
         const float mw = mbuf[w * GP + g];
         L = fmaf((mw == -INFINITY) ? 0.f : ex2_approx(mw - M), lbuf[w * GP + g], L);
       }
-      const float O = obuf[idx];
+      const float O = obuf[idx] + obuf[GP * D + idx];
       obuf[idx] = 0.f;
+      obuf[GP * D + idx] = 0.f;
       const size_t bh = (size_t)si.b * p.Hq + hq0 + g;
       if (si.np <= 1) {
         const bool empty_seq = (si.np == 0);
@@ -537,62 +539,71 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS, DecodeCfg<D, GP>::M
       named_bar_sync(1, nct);
       if (ctid == 0) {
         const unsigned ctr = 2u + (unsigned)(si.b * Hg + si.hg);
-        fence_acq_rel_gpu();  // release: the CTA's partial (ordered before by the barrier) is visible first
-        const unsigned old = atomicAdd(&p.counters[ctr], 1u);
+        // release: the CTA's partial (ordered before this by the barrier) is visible before the count;
+        // acquire: when this CTA is the last, the other CTAs' partials are visible to it
+        const unsigned old = atomic_add_acq_rel_gpu(&p.counters[ctr], 1u);
         const int is_last = (old == (unsigned)si.np - 1u);
-        if (is_last) {
-          atomicExch(&p.counters[ctr], 0u);  // re-arm for the next call
-          fence_acq_rel_gpu();               // acquire: the other CTAs' partials are visible from here on
-        }
+        if (is_last) atomicExch(&p.counters[ctr], 0u);  // re-arm for the next call
         *last_flag = is_last;
       }
       named_bar_sync(1, nct);
       if (*last_flag) {
-        // Single pass over the row's partials with a running max; loads go out NB partials at a time.
-        // Partial slots of the row: CTA c holds slot 2c (+1 for the first CTA when the row starts
-        // inside its slice).
+        // Merge the row's partials.  Partial slots of the row: CTA c holds slot 2c (+1 for the first CTA when the
+        // row starts inside its slice).  Per round of up to D partials: stage their maxima in shared memory
+        // (obuf is free here), one thread per head turns them into weights 2^(m - M) and the running sum, then
+        // every thread sums its O entries with all of a round's loads in flight.
         constexpr int KP = (GP * D + C::NW * 32 - 1) / (C::NW * 32);
-        constexpr int NB = (KP >= 8) ? 1 : (8 / KP);
-        float Mx[KP], Lx[KP], Ox[KP];
+        float* wgt = obuf;               // [D][GP] weights of the round
+        float* msum_s = obuf + GP * D;   // [GP] running max
+        float* lsum_s = msum_s + GP;     // [GP] running sum
+        float* rsc_s = lsum_s + GP;      // [GP] rescale of earlier rounds
+        float acc[KP];
 #pragma unroll
-        for (int k = 0; k < KP; ++k) {
-          Mx[k] = -INFINITY;
-          Lx[k] = 0.f;
-          Ox[k] = 0.f;
-        }
-        for (int i0 = 0; i0 < si.np; i0 += NB) {
-          float mv[KP][NB], lv[KP][NB], ov[KP][NB];
-#pragma unroll
-          for (int bb = 0; bb < NB; ++bb) {
-            const int i = i0 + bb;
+        for (int k = 0; k < KP; ++k) acc[k] = 0.f;
+        const int npart = si.np;
+        for (int i0 = 0; i0 < npart; i0 += D) {
+          const int chunk = min(npart - i0, D);
+          for (int e = ctid; e < chunk * GP; e += nct) {
+            const int i = i0 + e / GP, g = e % GP;
             const int sl = 2 * (si.cta_lo + i) + (i == 0 ? si.lo_odd : 0);
-#pragma unroll
-            for (int k = 0; k < KP; ++k) {
-              const int idx = ctid + k * nct;
-              mv[k][bb] = -INFINITY;
-              lv[k][bb] = 0.f;
-              ov[k][bb] = 0.f;
-              if (i < si.np && idx < GP * D) {
-                const int g = idx / D;
-                const size_t prow = (size_t)sl * GP + g;
-                mv[k][bb] = __ldcg(p.part_ml + prow * 2);
-                lv[k][bb] = __ldcg(p.part_ml + prow * 2 + 1);
-                ov[k][bb] = __ldcg(p.part_o + prow * D + (idx - g * D));
-              }
-            }
+            wgt[e] = __ldcg(p.part_ml + ((size_t)sl * GP + g) * 2);
           }
-#pragma unroll
-          for (int bb = 0; bb < NB; ++bb)
-#pragma unroll
-            for (int k = 0; k < KP; ++k) {
-              if (mv[k][bb] == -INFINITY) continue;
-              const float Mn = fmaxf(Mx[k], mv[k][bb]);
-              const float a = ex2_approx(Mx[k] - Mn);  // 0 while Mx is -inf
-              const float w = ex2_approx(mv[k][bb] - Mn);
-              Lx[k] = fmaf(Lx[k], a, w * lv[k][bb]);
-              Ox[k] = fmaf(Ox[k], a, w * ov[k][bb]);
-              Mx[k] = Mn;
+          named_bar_sync(1, nct);
+          if (ctid < GP) {
+            const int g = ctid;
+            const float Mold = (i0 == 0) ? -INFINITY : msum_s[g];
+            float M = Mold;
+            for (int i = 0; i < chunk; ++i) M = fmaxf(M, wgt[i * GP + g]);
+            const float rsc = (i0 == 0) ? 0.f : ex2_approx(Mold - M);
+            float L = (i0 == 0) ? 0.f : lsum_s[g] * rsc;
+            for (int i = 0; i < chunk; ++i) {
+              const int ii = i0 + i;
+              const int sl = 2 * (si.cta_lo + ii) + (ii == 0 ? si.lo_odd : 0);
+              const float w = ex2_approx(wgt[i * GP + g] - M);
+              wgt[i * GP + g] = w;
+              L = fmaf(w, __ldcg(p.part_ml + ((size_t)sl * GP + g) * 2 + 1), L);
             }
+            msum_s[g] = M;
+            lsum_s[g] = L;
+            rsc_s[g] = rsc;
+          }
+          named_bar_sync(1, nct);
+#pragma unroll
+          for (int k = 0; k < KP; ++k) {
+            const int idx = ctid + k * nct;
+            if (idx >= GP * D) continue;
+            const int g = idx / D;
+            const int d = idx - g * D;
+            float a = acc[k] * rsc_s[g];
+#pragma unroll 8
+            for (int i = 0; i < chunk; ++i) {
+              const int ii = i0 + i;
+              const int sl = 2 * (si.cta_lo + ii) + (ii == 0 ? si.lo_odd : 0);
+              a = fmaf(wgt[i * GP + g], __ldcg(p.part_o + ((size_t)sl * GP + g) * D + d), a);
+            }
+            acc[k] = a;
+          }
+          named_bar_sync(1, nct);  // the next round overwrites wgt
         }
 #pragma unroll
         for (int k = 0; k < KP; ++k) {
@@ -601,9 +612,11 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS, DecodeCfg<D, GP>::M
           const int g = idx / D;
           const int d = idx - g * D;
           const size_t bh = (size_t)si.b * p.Hq + hq0 + g;
-          store_out<float>(p.out, bh * D + d, Ox[k] / Lx[k], p.out_f32);
-          if (d == 0 && p.lse != nullptr) p.lse[bh] = (Mx[k] + log2f(Lx[k])) * kLn2;
+          store_out<float>(p.out, bh * D + d, acc[k] / lsum_s[g], p.out_f32);
+          if (d == 0 && p.lse != nullptr) p.lse[bh] = (msum_s[g] + log2f(lsum_s[g])) * kLn2;
         }
+        named_bar_sync(1, nct);
+        for (int e = ctid; e < 2 * GP * D; e += nct) obuf[e] = 0.f;
       }
     }
     named_bar_sync(1, nct);  // mbuf/lbuf/obuf/last_flag are reused by the next piece
