@@ -18,19 +18,21 @@ from dataclasses import dataclass, field
 
 import torch
 
-__all__ = ["Workload", "WORKLOADS", "make_prefill", "make_decode", "make_varlen", "make_pages", "randn_bf16"]
+__all__ = ["Workload", "WORKLOADS", "make_prefill", "make_decode", "make_decode_multi", "make_varlen", "make_pages",
+           "randn_bf16"]
 
 
 @dataclass(frozen=True)
 class Workload:
     name: str
-    kind: str  # "prefill" | "decode" | "varlen"
+    kind: str  # "prefill" | "decode" | "decode_multi" | "varlen"
     seed: int
     B: int
     Hq: int
     Hkv: int
     D: int
     L: int = 0  # prefill Lq == Lkv; decode Lmax
+    Lq: int = 1  # decode_multi: new tokens per sequence
     causal: bool = True
     out_f32: bool = False
     kv_lens: tuple = ()  # decode: fixed lengths, or () to draw from kv_range
@@ -52,6 +54,8 @@ WORKLOADS = {
                  extra={"page_size": 16}),
         Workload("decode_long", "decode", 1002, B=4, Hq=32, Hkv=8, D=128, L=131072,
                  kv_lens=(32768, 65536, 98304, 131072)),
+        Workload("decode_multi_gqa", "decode_multi", 1006, B=8, Hq=32, Hkv=8, D=128, L=4096, Lq=8,
+                 kv_range=(512, 4096)),
         Workload("prefill_causal", "prefill", 1003, B=4, Hq=32, Hkv=32, D=128, L=4096, causal=True),
         Workload("prefill_ragged_gqa", "varlen", 1004, B=16, Hq=32, Hkv=8, D=128, causal=True,
                  seq_range=(256, 8192)),
@@ -96,6 +100,26 @@ def make_decode(B, Hq, Hkv, Lmax, D, seed, kv_lens=None, kv_range=None):
     """
     g = _gen(seed)
     q = randn_bf16((B, Hq, D), g)
+    kc = randn_bf16((B, Hkv, Lmax, D), g)
+    vc = randn_bf16((B, Hkv, Lmax, D), g)
+    if kv_lens is not None and len(kv_lens) > 0:
+        lens = torch.tensor(list(kv_lens), dtype=torch.int32)
+    elif kv_range is None:
+        lens = torch.full((B,), int(Lmax), dtype=torch.int32)
+    else:
+        lo, hi = kv_range
+        lens = torch.randint(int(lo), int(hi) + 1, (B,), generator=g, dtype=torch.int64).to(torch.int32)
+    return q, kc, vc, lens
+
+
+def make_decode_multi(B, Hq, Hkv, Lq, Lmax, D, seed, kv_lens=None, kv_range=None):
+    """Multi-token decode inputs: q [B,Hq,Lq,D], caches [B,Hkv,Lmax,D] bf16, kv_lens int32 [B].
+
+    Lengths as in :func:`make_decode`; they count every cached key, the Lq new
+    tokens' own keys included.
+    """
+    g = _gen(seed)
+    q = randn_bf16((B, Hq, Lq, D), g)
     kc = randn_bf16((B, Hkv, Lmax, D), g)
     vc = randn_bf16((B, Hkv, Lmax, D), g)
     if kv_lens is not None and len(kv_lens) > 0:

@@ -16,6 +16,7 @@ from .sdpa import (  # noqa: F401
     attention_varlen,
     attention_varlen_rows,
     decode,
+    decode_multi,
     kv_head_of,
     log_sum_exp,
     scores,

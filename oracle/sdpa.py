@@ -56,6 +56,7 @@ __all__ = [
     "attention_varlen",
     "attention_varlen_rows",
     "decode",
+    "decode_multi",
 ]
 
 
@@ -232,4 +233,37 @@ def decode(q, kcache, vcache, kv_lens, scale: float, heads=None):
         o, ls = attention_head(q[b, h][None, :], to_f64(kcache[b, hk, :n]), to_f64(vcache[b, hk, :n]), scale,
                                causal=False)
         O[b, h], lse[b, h] = o[0], ls[0]
+    return O, lse
+
+
+def decode_multi(q, kcache, vcache, kv_lens, scale: float, heads=None):
+    """Decode of several new tokens per sequence over a KV cache.
+
+    q [B,Hq,Lq,D], kcache/vcache [B,Hkv,Lmax,D], kv_lens [B].  Rows
+    ``0 .. kv_lens[b]-1`` of sequence b's cache hold all of its keys, the Lq new
+    tokens' own keys being the last Lq of them, so new token t (0-based) sits
+    at position ``kv_lens[b] - Lq + t`` and attends to keys
+    ``0 .. kv_lens[b] - Lq + t``: the causal mask of the Lq x kv_len score
+    block aligned to its bottom-right corner, as for prefill.  The
+    decoder-attention page ("Техника выжимания производительности", item 1,
+    token-level parallelism) processes several query tokens of a step at once
+    against K/V blocks loaded once; what each token computes is the single
+    decode above over its own visible prefix.  Returns O [B,Hq,Lq,D] and
+    lse [B,Hq,Lq]; ``heads`` optionally restricts the work to (b, hq) pairs,
+    the other entries being NaN.
+    """
+    q = to_f64(q)
+    lens = np.asarray(kv_lens, dtype=np.int64)
+    B, Hq, Lq, D = q.shape
+    Hkv = kcache.shape[1]
+    _check_heads(Hq, Hkv)
+    if heads is None:
+        heads = [(b, h) for b in range(B) for h in range(Hq)]
+    O = np.full((B, Hq, Lq, vcache.shape[3]), np.nan)
+    lse = np.full((B, Hq, Lq), np.nan)
+    for b, h in heads:
+        n = int(lens[b])
+        hk = kv_head_of(h, Hq, Hkv)
+        O[b, h], lse[b, h] = attention_head(q[b, h], to_f64(kcache[b, hk, :n]), to_f64(vcache[b, hk, :n]), scale,
+                                            causal=True)
     return O, lse

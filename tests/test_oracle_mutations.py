@@ -12,7 +12,8 @@ from oracle import sdpa as OA
 from tests.test_oracle_pins import PINS
 
 _orig = {name: getattr(OA, name) for name in
-         ("scores", "visible_mask", "kv_head_of", "softmax_two_pass", "log_sum_exp", "attention_head")}
+         ("scores", "visible_mask", "kv_head_of", "softmax_two_pass", "log_sum_exp", "attention_head",
+          "decode_multi")}
 
 
 def _softmax_wrong_axis(S, visible):
@@ -38,6 +39,25 @@ def _attention_head_k_for_v(Qh, Kh, Vh, scale, causal, visible=None):
                                    scale, causal, visible)
 
 
+def _multi_with_mask(mask_of):
+    """decode_multi with the visible set of token t over n keys given by mask_of(Lq, n) instead."""
+    def bad(q, kcache, vcache, kv_lens, scale, heads=None):
+        q = OA.to_f64(q)
+        B, Hq, Lq, D = q.shape
+        Hkv = kcache.shape[1]
+        O = np.full((B, Hq, Lq, vcache.shape[3]), np.nan)
+        lse = np.full((B, Hq, Lq), np.nan)
+        for b in range(B):
+            n = int(kv_lens[b])
+            for h in range(Hq):
+                hk = OA.kv_head_of(h, Hq, Hkv)
+                O[b, h], lse[b, h] = OA.attention_head(q[b, h], OA.to_f64(kcache[b, hk, :n]),
+                                                       OA.to_f64(vcache[b, hk, :n]), scale, True,
+                                                       visible=mask_of(Lq, n))
+        return O, lse
+    return bad
+
+
 MUTATIONS = {
     "scale_dropped": ("scores", lambda Qh, Kh, scale: Qh @ Kh.T),
     "logit_sign": ("scores", lambda Qh, Kh, scale: -scale * (Qh @ Kh.T)),
@@ -52,6 +72,11 @@ MUTATIONS = {
     "lse_log2": ("log_sum_exp", lambda m, l: np.where(l > 0, m + np.log2(np.where(l > 0, l, 1.0)), -np.inf)),
     "lse_drops_max": ("log_sum_exp", lambda m, l: np.where(l > 0, np.log(np.where(l > 0, l, 1.0)), -np.inf)),
     "k_used_for_v": ("attention_head", _attention_head_k_for_v),
+    "multi_sees_whole_cache": ("decode_multi", _multi_with_mask(lambda Lq, n: np.ones((Lq, n), bool))),
+    "multi_top_left": ("decode_multi", _multi_with_mask(
+        lambda Lq, n: np.arange(n)[None, :] <= np.arange(Lq)[:, None])),
+    "multi_excludes_own_key": ("decode_multi", _multi_with_mask(
+        lambda Lq, n: np.arange(n)[None, :] < np.arange(Lq)[:, None] + (n - Lq))),
 }
 
 

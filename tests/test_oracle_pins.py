@@ -12,7 +12,8 @@ pages' definition of attention (Operator Fusion, GPU learning diary day 24,
   logsumexp for one query;
 * structural reductions: GQA == MHA with repeated K/V heads, decode ==
   last row of causal prefill, packed sequences == per-sequence dense,
-  scale folded into q, key permutation invariance.
+  scale folded into q, key permutation invariance, each token of a
+  multi-token decode step == single-token decode over its own prefix.
 
 ``PINS`` lists every pin; ``tests/test_oracle_mutations.py`` plants mistakes
 in the oracle and checks that some pin fails for each.
@@ -269,6 +270,51 @@ def pin_bf16_inputs_promote_exactly():
     np.testing.assert_array_equal(OA.to_f64(t), np.array([1.0 + 2 ** -7, -3.0, 2.0 ** -100]))
 
 
+def pin_decode_multi_rows_are_single_decodes():
+    """Token t of a multi-token decode step == single-token decode over the keys up to its own position
+    (kv_len - Lq + t + 1 of them; none when that is <= 0)."""
+    r = _rng(160)
+    B, Hq, Hkv, Lq, Lmax, D = 3, 4, 2, 5, 12, 6
+    lens = [12, 7, 3]  # the last sequence has kv_len < Lq: its first tokens see no key
+    q = r.standard_normal((B, Hq, Lq, D))
+    kc = r.standard_normal((B, Hkv, Lmax, D))
+    vc = r.standard_normal((B, Hkv, Lmax, D))
+    O, lse = OA.decode_multi(q, kc, vc, lens, 0.45)
+    for t in range(Lq):
+        lens_t = [max(0, n - Lq + t + 1) for n in lens]
+        Od, lsed = OA.decode(q[:, :, t], kc, vc, lens_t, 0.45)
+        np.testing.assert_allclose(O[:, :, t], Od, atol=1e-14, err_msg=f"token {t}")
+        np.testing.assert_allclose(lse[:, :, t], lsed, atol=1e-14, err_msg=f"token {t}")
+    assert np.all(O[2, :, :2] == 0) and np.all(np.isneginf(lse[2, :, :2]))
+
+
+def pin_decode_multi_brute_force():
+    """Multi-token decode == the literal loops (bottom-right causal) over each sequence's cache prefix."""
+    r = _rng(161)
+    B, Hq, Hkv, Lq, Lmax, D = 2, 4, 2, 3, 9, 4
+    lens = [9, 4]
+    q = r.standard_normal((B, Hq, Lq, D))
+    kc = r.standard_normal((B, Hkv, Lmax, D))
+    vc = r.standard_normal((B, Hkv, Lmax, D))
+    O, lse = OA.decode_multi(q, kc, vc, lens, 0.7)
+    for b, n in enumerate(lens):
+        Ob, lb = attention_loops(q[b:b + 1], kc[b:b + 1, :, :n], vc[b:b + 1, :, :n], 0.7, True)
+        np.testing.assert_allclose(O[b:b + 1], np.array(Ob), atol=1e-13)
+        np.testing.assert_allclose(lse[b:b + 1], np.array(lb), atol=1e-13)
+
+
+def pin_decode_multi_golden():
+    """The hand-worked causal 2x2 case as a two-token step over a cache whose rows past kv_len are NaN."""
+    with open(GOLDEN) as f:
+        c = next(x for x in json.load(f)["cases"] if x["name"].startswith("causal 2x2"))
+    q, k, v = np.array(c["q"]), np.array(c["k"]), np.array(c["v"])
+    pad = np.full((1, 1, 3, 2), np.nan)
+    kc, vc = np.concatenate([k, pad], axis=2), np.concatenate([v, pad], axis=2)
+    O, lse = OA.decode_multi(q, kc, vc, [2], c["scale"])
+    np.testing.assert_allclose(O, np.array(c["O"]), rtol=0, atol=1e-14)
+    np.testing.assert_allclose(lse, np.array(c["lse"]), rtol=0, atol=1e-14)
+
+
 PINS = [
     pin_brute_force,
     pin_rows_sum_to_one,
@@ -287,6 +333,9 @@ PINS = [
     pin_rows_equal_full,
     pin_empty_rows,
     pin_bf16_inputs_promote_exactly,
+    pin_decode_multi_rows_are_single_decodes,
+    pin_decode_multi_brute_force,
+    pin_decode_multi_golden,
 ]
 
 
