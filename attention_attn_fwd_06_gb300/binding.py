@@ -38,6 +38,7 @@ EXPORTED = (
     "attn_decode_ex",
     "attn_decode_noalloc",
     "attn_decode_paged",
+    "attn_decode_multi",
     "attn_decode_workspace_bytes",
     "attn_get_device_status",
     "attn_status_string",
@@ -73,6 +74,17 @@ class attn_decode_paged_params(ctypes.Structure):
         ("B", ctypes.c_int), ("Hq", ctypes.c_int), ("Hkv", ctypes.c_int), ("D", ctypes.c_int),
         ("page_size", ctypes.c_int), ("max_pages", ctypes.c_int), ("num_pages", ctypes.c_int),
         ("scale", ctypes.c_float), ("out_dtype", ctypes.c_int), ("chunk", ctypes.c_int),
+        ("stream", ctypes.c_void_p),
+    ]
+
+
+class attn_decode_multi_params(ctypes.Structure):
+    _fields_ = [
+        ("q", ctypes.c_void_p), ("kcache", ctypes.c_void_p), ("vcache", ctypes.c_void_p),
+        ("kv_lens", ctypes.c_void_p), ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p),
+        ("B", ctypes.c_int), ("Hq", ctypes.c_int), ("Hkv", ctypes.c_int), ("Lq", ctypes.c_int),
+        ("Lmax", ctypes.c_int), ("D", ctypes.c_int),
+        ("scale", ctypes.c_float), ("out_dtype", ctypes.c_int),
         ("stream", ctypes.c_void_p),
     ]
 
@@ -114,6 +126,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.attn_decode_noalloc.restype = I
         lib.attn_decode_paged.argtypes = [ctypes.POINTER(attn_decode_paged_params)]
         lib.attn_decode_paged.restype = I
+        lib.attn_decode_multi.argtypes = [ctypes.POINTER(attn_decode_multi_params)]
+        lib.attn_decode_multi.restype = I
         lib.attn_decode_workspace_bytes.argtypes = [I, I, I, I, I, I]
         lib.attn_decode_workspace_bytes.restype = ctypes.c_ulonglong
         lib.attn_get_device_status.argtypes = [P]
@@ -283,6 +297,37 @@ def attn_decode_paged(q, kpages, vpages, block_table, kv_lens, out=None, lse=Non
     p.chunk = int(chunk)
     p.stream = _stream_handle(stream, q.device)
     _check(load().attn_decode_paged(ctypes.byref(p)), "attn_decode_paged")
+    return out, lse
+
+
+def attn_decode_multi(q, kcache, vcache, kv_lens, out=None, lse=None, scale=None, out_dtype=torch.bfloat16,
+                      want_lse=True, stream=None):
+    """Multi-token decode: q [B,Hq,Lq,D], caches [B,Hkv,Lmax,D] bf16, kv_lens int32 [B] counting the new tokens'
+    own keys -> (out [B,Hq,Lq,D], lse [B,Hq,Lq])."""
+    _need(q, "q", torch.bfloat16, 4)
+    _need(kcache, "kcache", torch.bfloat16, 4)
+    _need(vcache, "vcache", torch.bfloat16, 4)
+    _need(kv_lens, "kv_lens", torch.int32, 1)
+    B, Hq, Lq, D = q.shape
+    Hkv, Lmax = kcache.shape[1], kcache.shape[2]
+    if tuple(kcache.shape) != (B, Hkv, Lmax, D) or tuple(vcache.shape) != tuple(kcache.shape):
+        raise ValueError("cache shapes do not match q")
+    if kv_lens.shape[0] != B:
+        raise ValueError("kv_lens must have B entries")
+    if out is None:
+        out = torch.empty((B, Hq, Lq, D), dtype=out_dtype, device=q.device)
+    _need(out, "out", out_dtype, 4)
+    if lse is None and want_lse:
+        lse = torch.empty((B, Hq, Lq), dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, 3)
+    p = attn_decode_multi_params()
+    p.q, p.kcache, p.vcache, p.kv_lens, p.out, p.lse = (_ptr(t) for t in (q, kcache, vcache, kv_lens, out, lse))
+    p.B, p.Hq, p.Hkv, p.Lq, p.Lmax, p.D = B, Hq, Hkv, Lq, Lmax, D
+    p.scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    p.out_dtype = ATTN_DTYPE_F32 if out_dtype == torch.float32 else ATTN_DTYPE_BF16
+    p.stream = _stream_handle(stream, q.device)
+    _check(load().attn_decode_multi(ctypes.byref(p)), "attn_decode_multi")
     return out, lse
 
 

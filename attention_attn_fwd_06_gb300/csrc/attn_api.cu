@@ -378,6 +378,66 @@ int attn_decode_paged(const attn_decode_paged_params* pp) {
   return map_cuda(attn::launch_decode(L, s->num_sms));
 }
 
+int attn_decode_multi(const attn_decode_multi_params* p) {
+  if (p == nullptr) return ATTN_ERR_INVALID_ARG;
+  if (p->Lq < 1) return ATTN_ERR_INVALID_ARG;
+  // Everything but q/out's token axis means what it means for attn_decode_ex.
+  attn_decode_params d = {};
+  d.q = p->q;
+  d.kcache = p->kcache;
+  d.vcache = p->vcache;
+  d.kv_lens = p->kv_lens;
+  d.out = p->out;
+  d.lse = p->lse;
+  d.B = p->B;
+  d.Hq = p->Hq;
+  d.Hkv = p->Hkv;
+  d.Lmax = p->Lmax;
+  d.D = p->D;
+  d.scale = p->scale;
+  d.out_dtype = p->out_dtype;
+  d.stream = p->stream;
+  int st = validate_decode(&d);
+  if (st != ATTN_OK) return st;
+  if (p->B == 0) return ATTN_OK;
+  const long long rows = (long long)(p->Hq / p->Hkv) * p->Lq;
+  if (rows > 128) return ATTN_ERR_UNSUPPORTED;
+  if ((long long)p->B * p->Hq * p->Lq > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+  if (2 + (long long)p->B * p->Hkv > attn::kDecodeCounterSlots) return ATTN_ERR_UNSUPPORTED;
+  cudaStream_t stream = static_cast<cudaStream_t>(p->stream);
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState* s = nullptr;
+  st = device_state_locked(&s);
+  if (st != ATTN_OK) return st;
+  const size_t slots = (size_t)2 * attn::decode_multi_grid(s->num_sms);
+  const size_t part_o_elems = slots * (size_t)rows * p->D;
+  const size_t part_ml_elems = slots * (size_t)rows * 2;
+  st = ensure_workspace_locked(*s, kCounterBytes + (part_o_elems + part_ml_elems) * sizeof(float), stream);
+  if (st != ATTN_OK) return st;
+  attn::DecodeMultiLaunch L{};
+  L.q = p->q;
+  L.kcache = p->kcache;
+  L.vcache = p->vcache;
+  L.kv_lens = p->kv_lens;
+  L.out = p->out;
+  L.lse = p->lse;
+  L.counters = static_cast<unsigned*>(s->ws);
+  L.part_o = reinterpret_cast<float*>(static_cast<char*>(s->ws) + kCounterBytes);
+  L.part_ml = L.part_o + part_o_elems;
+  L.B = p->B;
+  L.Hq = p->Hq;
+  L.Hkv = p->Hkv;
+  L.Lq = p->Lq;
+  L.Lmax = p->Lmax;
+  L.D = p->D;
+  L.scale = p->scale;
+  L.out_f32 = p->out_dtype == ATTN_DTYPE_F32;
+  L.num_sms = s->num_sms;
+  L.status = s->status;
+  L.stream = stream;
+  return map_cuda(attn::launch_decode_multi(L));
+}
+
 int attn_decode(const void* q, const void* kcache, const void* vcache, const int* kv_lens, void* out, float* lse,
                 int B, int Hq, int Hkv, int Lmax, int D, float scale, void* stream) {
   attn_decode_params p = {};

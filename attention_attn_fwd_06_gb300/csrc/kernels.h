@@ -39,6 +39,29 @@ constexpr int kDecodeCounterSlots = 65536;
 // One persistent launch that also merges the split partials.
 cudaError_t launch_decode(const DecodeLaunch& p, int num_sms);
 
+// Multi-token decode (tcgen05 tensor-core path): Lq new tokens per sequence over a contiguous KV cache.
+struct DecodeMultiLaunch {
+  const void* q;        // bf16 [B, Hq, Lq, D]
+  const void* kcache;   // bf16 [B, Hkv, Lmax, D]
+  const void* vcache;   // same layout as kcache
+  const int* kv_lens;   // int32 [B] (device); keys of every token, the new ones included
+  void* out;            // [B, Hq, Lq, D], bf16 or fp32
+  float* lse;           // fp32 [B, Hq, Lq] or null
+  float* part_o;        // fp32 [2 * grid][R][D], R = (Hq / Hkv) * Lq
+  float* part_ml;       // fp32 [2 * grid][R][2]
+  unsigned* counters;   // [2 + b * Hkv + hk]; zero between calls (shared with the single-token decode)
+  int B, Hq, Hkv, Lq, Lmax, D;
+  float scale;
+  int out_f32;
+  int num_sms;
+  unsigned* status;
+  cudaStream_t stream;
+};
+
+// CTAs of the persistent multi-token decode launch (one per SM); the partial slots number 2 * grid.
+int decode_multi_grid(int num_sms);
+cudaError_t launch_decode_multi(const DecodeMultiLaunch& p);
+
 // Prefill (tcgen05 tensor-core path).
 struct PrefillLaunch {
   const void* q;

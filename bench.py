@@ -5,8 +5,9 @@ Default workload: single-token GQA decode over a KV cache (B=8, Hq=32, Hkv=8,
 D=128, kv_len uniform in [512, 4096], cache Lmax=4096), the configuration the
 decode HBM-bandwidth metric is quoted on.  One step = one ``attn_decode`` call
 (split pass + log-sum-exp combine) over that batch.  Other workloads:
-``--workload decode_long | prefill_causal | prefill_ragged_gqa |
-prefill_noncausal_d64 | tiny_causal``.
+``--workload decode_long | decode_gqa_paged16 | decode_multi_gqa |
+prefill_causal | prefill_ragged_gqa | prefill_noncausal_d64 | tiny_causal``
+(``decode_multi_gqa``: 8 new tokens per sequence through ``attn_decode_multi``).
 
 Timing: inputs resident in HBM; W untimed warm-up steps; then exactly K
 steps, each bracketed by CUDA events on the launching stream, with a write of
@@ -146,34 +147,54 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------- workloads
 
+def _pin(t):
+    """Page-locked copy for the end-to-end leg; plain memory when no GPU is visible (the oracle-only arm)."""
+    import torch
+
+    return t.pin_memory() if torch.cuda.is_available() else t
+
+
 class DecodeCase:
     def __init__(self, w, device):
         import torch
 
-        from attention_attn_fwd_06_gb300.inputs import make_decode
+        from attention_attn_fwd_06_gb300.inputs import make_decode, make_decode_multi
 
         self.w = w
-        q, kc, vc, lens = make_decode(w.B, w.Hq, w.Hkv, w.L, w.D, w.seed,
-                                      kv_lens=w.kv_lens or None, kv_range=w.kv_range or None)
+        self.multi = w.kind == "decode_multi"
+        self.Lq = w.Lq if self.multi else 1
+        if self.multi:
+            q, kc, vc, lens = make_decode_multi(w.B, w.Hq, w.Hkv, w.Lq, w.L, w.D, w.seed,
+                                                kv_lens=w.kv_lens or None, kv_range=w.kv_range or None)
+        else:
+            q, kc, vc, lens = make_decode(w.B, w.Hq, w.Hkv, w.L, w.D, w.seed,
+                                          kv_lens=w.kv_lens or None, kv_range=w.kv_range or None)
         self.page_size = w.extra.get("page_size")
         self.oracle_host = (q, kc, vc)
         if self.page_size:
             from attention_attn_fwd_06_gb300.inputs import make_pages
 
             kp, vp, table = make_pages(kc, vc, self.page_size, w.seed + 7, fill_unused=0.0)
-            self.host = [t.pin_memory() for t in (q, kp, vp, lens, table)]
+            self.host = [_pin(t) for t in (q, kp, vp, lens, table)]
         else:
-            self.host = [t.pin_memory() for t in (q, kc, vc, lens)]
+            self.host = [_pin(t) for t in (q, kc, vc, lens)]
         self.dev = [t.to(device) for t in self.host]
-        self.out = torch.empty((w.B, w.Hq, w.D), dtype=torch.bfloat16, device=device)
-        self.lse = torch.empty((w.B, w.Hq), dtype=torch.float32, device=device)
-        self.out_h = torch.empty_like(self.out, device="cpu").pin_memory()
-        self.lse_h = torch.empty_like(self.lse, device="cpu").pin_memory()
+        tok = (self.Lq,) if self.multi else ()
+        self.out = torch.empty((w.B, w.Hq) + tok + (w.D,), dtype=torch.bfloat16, device=device)
+        self.lse = torch.empty((w.B, w.Hq) + tok, dtype=torch.float32, device=device)
+        self.out_h = _pin(torch.empty_like(self.out, device="cpu"))
+        self.lse_h = _pin(torch.empty_like(self.lse, device="cpu"))
         self.lens = [int(x) for x in lens.tolist()]
+        # algorithmic bytes: every attended K/V row once, q and O once, lse once
         kv_bytes = sum(self.lens) * w.Hkv * w.D * 2 * 2
-        self.alg_bytes = kv_bytes + w.B * w.Hq * w.D * 2 * 2 + w.B * w.Hq * 4
+        rows = w.B * w.Hq * self.Lq
+        self.alg_bytes = kv_bytes + rows * w.D * 2 * 2 + rows * 4
         self.work = self.alg_bytes
         self.unit, self.kind = "GB/s", "hbm"
+        self.kernel = "decode_multi" if self.multi else "decode_split"
+        self.kernel_desc = ("decode_multi_kernel (one attn_decode_multi call: tcgen05 split pass with the merge fused, "
+                            "event-timed)" if self.multi else
+                            "decode_split_kernel (one attn_decode call: split pass with the combine fused, event-timed)")
         self.launches_per_step = 1
         self.h2d = sum(t.numel() * t.element_size() for t in self.host)
         self.d2h = self.out.numel() * 2 + self.lse.numel() * 4
@@ -184,6 +205,9 @@ class DecodeCase:
         if self.page_size:
             q, kp, vp, lens, table = self.dev
             AB.attn_decode_paged(q, kp, vp, table, lens, out=self.out, lse=self.lse, scale=self.w.scale)
+        elif self.multi:
+            q, kc, vc, lens = self.dev
+            AB.attn_decode_multi(q, kc, vc, lens, out=self.out, lse=self.lse, scale=self.w.scale)
         else:
             q, kc, vc, lens = self.dev
             AB.attn_decode(q, kc, vc, lens, out=self.out, lse=self.lse, scale=self.w.scale)
@@ -214,23 +238,25 @@ class PrefillCase:
             q, k, v, cu = make_varlen(w.B, w.Hq, w.Hkv, w.D, w.seed, seq_range=w.seq_range)
             self.cu = cu
             self.seqlens = [int(cu[i + 1] - cu[i]) for i in range(w.B)]
-            self.host = [t.pin_memory() for t in (q, k, v, cu)]
+            self.host = [_pin(t) for t in (q, k, v, cu)]
             total = int(cu[-1])
             self.out = torch.empty((total, w.Hq, w.D), dtype=torch.bfloat16, device=device)
             self.lse = torch.empty((total, w.Hq), dtype=torch.float32, device=device)
         else:
             q, k, v = make_prefill(w.B, w.Hq, w.Hkv, w.L, w.L, w.D, w.seed)
             self.seqlens = [w.L] * w.B
-            self.host = [t.pin_memory() for t in (q, k, v)]
+            self.host = [_pin(t) for t in (q, k, v)]
             odt = torch.float32 if w.out_f32 else torch.bfloat16
             self.out = torch.empty((w.B, w.Hq, w.L, w.D), dtype=odt, device=device)
             self.lse = torch.empty((w.B, w.Hq, w.L), dtype=torch.float32, device=device)
         self.dev = [t.to(device) for t in self.host]
-        self.out_h = torch.empty_like(self.out, device="cpu").pin_memory()
-        self.lse_h = torch.empty_like(self.lse, device="cpu").pin_memory()
+        self.out_h = _pin(torch.empty_like(self.out, device="cpu"))
+        self.lse_h = _pin(torch.empty_like(self.lse, device="cpu"))
         pairs = sum((L * (L + 1)) // 2 if w.causal else L * L for L in self.seqlens)
         self.work = 4.0 * w.D * w.Hq * pairs
         self.unit, self.kind = "TFLOP/s", "tensor"
+        self.kernel = "prefill_fwd"
+        self.kernel_desc = "prefill_fwd_kernel (one attn_fwd call, event-timed)"
         self.launches_per_step = 1
         self.h2d = sum(t.numel() * t.element_size() for t in self.host)
         self.d2h = self.out.numel() * self.out.element_size() + self.lse.numel() * 4
@@ -278,6 +304,10 @@ def _oracle_task(args):
         q, kc, vc, n, scale = payload
         oracle.attention_head(q[None, :].astype(np.float64), kc[:n].astype(np.float64), vc[:n].astype(np.float64),
                               scale, causal=False)
+    elif kind == "decode_multi":
+        q, kc, vc, n, scale = payload  # q [Lq, D]: bottom-right causal over the sequence's n keys
+        oracle.attention_head(q.astype(np.float64), kc[:n].astype(np.float64), vc[:n].astype(np.float64), scale,
+                              causal=True)
     else:
         q, k, v, scale, causal = payload
         oracle.attention_head(q.astype(np.float64), k.astype(np.float64), v.astype(np.float64), scale, causal)
@@ -305,13 +335,14 @@ def run_oracle_pool(case, budget_s):
     if isinstance(case, DecodeCase):
         q, kc, vc = (t.float().numpy() for t in case.oracle_host)
         g = w.Hq // w.Hkv
+        Lq = case.Lq
         for b in range(w.B):
             for h in range(w.Hq):
                 n = case.lens[b]
                 hk = h // g
-                bytes_ = n * w.D * 2 * 2 / g + w.D * 2 * 2 + 4
-                units.append((("decode", (q[b, h], kc[b, hk], vc[b, hk], n, w.scale)), bytes_))
-        what = "(b, hq) decode rows"
+                bytes_ = n * w.D * 2 * 2 / g + Lq * (w.D * 2 * 2 + 4)
+                units.append(((case.w.kind, (q[b, h], kc[b, hk], vc[b, hk], n, w.scale)), bytes_))
+        what = "(b, hq) decode rows" if Lq == 1 else f"(b, hq) decode rows of {Lq} tokens"
     else:
         hosts = [t.float().numpy() for t in case.host[:3]]
         cu = case.host[3].numpy() if w.kind == "varlen" else None
@@ -367,14 +398,16 @@ def make_case(name, device):
     from attention_attn_fwd_06_gb300.inputs import WORKLOADS
 
     w = WORKLOADS[name]
-    return DecodeCase(w, device) if w.kind == "decode" else PrefillCase(w, device)
+    return DecodeCase(w, device) if w.kind in ("decode", "decode_multi") else PrefillCase(w, device)
 
 
 def workload_config(case):
     w = case.w
     cfg = {"workload": w.name, "kind": w.kind, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
            "l2": "512 MB buffer written between timed steps (inputs may fit in the 129 MB L2)"}
-    if w.kind == "decode":
+    if w.kind in ("decode", "decode_multi"):
+        if w.kind == "decode_multi":
+            cfg["Lq"] = w.Lq
         cfg.update({"Lmax": w.L, "kv_lens": "uniform [%d, %d]" % w.kv_range if w.kv_range else list(w.kv_lens),
                     "kv_tokens_total": sum(case.lens)})
         if w.extra.get("page_size"):
@@ -475,13 +508,13 @@ def run_ours(args):
     if case.kind == "hbm":
         peak, peak_src = pk["hbm_gbs"], pk["source"]
         roof = {"bound": "hbm", "achieved": per_gpu, "peak": peak, "unit": "GB/s", "frac": per_gpu / peak,
-                "traffic": read_traffic("decode_split", case.w.name), "peak_source": peak_src,
-                "kernel": "decode_split_kernel (one attn_decode call: split pass with the combine fused, event-timed)"}
+                "traffic": read_traffic(case.kernel, case.w.name), "peak_source": peak_src,
+                "kernel": case.kernel_desc}
     else:
         peak, peak_src = pk["bf16_tflops"], pk["source"]
         roof = {"bound": "tensor", "achieved": per_gpu, "peak": peak, "unit": "TFLOP/s", "frac": per_gpu / peak,
-                "traffic": read_traffic("prefill_fwd", case.w.name), "peak_source": peak_src,
-                "kernel": "prefill_fwd_kernel (one attn_fwd call, event-timed)"}
+                "traffic": read_traffic(case.kernel, case.w.name), "peak_source": peak_src,
+                "kernel": case.kernel_desc}
 
     line = {
         "metric": METRIC,
@@ -576,7 +609,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="decode_gqa")
-    ap.add_argument("--also", default="decode_long,prefill_causal",
+    ap.add_argument("--also", default="decode_long,decode_multi_gqa,prefill_causal",
                     help="comma-separated extra workloads measured in the same run (rank 0, N=1 style)")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of host work for cpu_baseline")
     ap.add_argument("--ref-budget", type=float, default=5.0, help="seconds of host work per reference step")

@@ -212,6 +212,52 @@ typedef struct attn_decode_paged_params {
 int attn_decode_paged(const attn_decode_paged_params* p);
 
 /*
+ * attn_decode_multi_params / attn_decode_multi -- decode of several new tokens
+ * per sequence at once (multi-token or speculative decode), on the tensor
+ * cores.  The decoder page ("Оптимизация Decoder Attention для LLM на GPU",
+ * "Техника выжимания производительности", item 1: token-level parallelism)
+ * processes several query tokens of a step together so that each K/V block is
+ * loaded once for all of them and the tensor cores have work.
+ *
+ *   q        bf16 [B, Hq, Lq, D]   the Lq new tokens of every sequence
+ *   kcache   bf16 [B, Hkv, Lmax, D]
+ *   vcache   bf16 [B, Hkv, Lmax, D]
+ *   kv_lens  DEVICE int32 [B]: the number of cached keys of sequence b,
+ *            INCLUDING the Lq new tokens, whose keys and values must already
+ *            be in rows kv_len-Lq .. kv_len-1.  New token t (0-based) sits at
+ *            position kv_len - Lq + t and attends to keys 0 .. kv_len - Lq + t
+ *            (the bottom-right causal mask of attn_fwd with Lkv = kv_len).
+ *            Rows at or past kv_len are never read.  A value outside
+ *            [0, Lmax] is clamped and flagged ATTN_ERR_DEVICE_BOUNDS; a token
+ *            that sees no key (kv_len < Lq) gets O = 0, lse = -inf.
+ *   out      [B, Hq, Lq, D]  bf16, or fp32 when out_dtype = ATTN_DTYPE_F32
+ *   lse      fp32 [B, Hq, Lq]  may be NULL
+ *   Lq       1 .. 128 / (Hq / Hkv): every query row of one kv head (the heads
+ *            of its group times the tokens) forms one 128-row MMA tile;
+ *            larger products return ATTN_ERR_UNSUPPORTED.
+ * B * Hkv must stay at or below 65534 and B * Hq * Lq below 2^31
+ * (ATTN_ERR_UNSUPPORTED otherwise).  Uses the split-KV workspace of
+ * attn_decode (same growth, capture and concurrency rules).  One kernel is
+ * enqueued: persistent CTAs (one per SM) each stream an equal share of all
+ * sequences' 128-key tiles, and the CTA that lands an item's last partial
+ * merges its partials.
+ */
+typedef struct attn_decode_multi_params {
+  const void* q;
+  const void* kcache;
+  const void* vcache;
+  const int* kv_lens;
+  void* out;
+  float* lse;
+  int B, Hq, Hkv, Lq, Lmax, D;
+  float scale;
+  int out_dtype;
+  void* stream;
+} attn_decode_multi_params;
+
+int attn_decode_multi(const attn_decode_multi_params* p);
+
+/*
  * attn_decode_workspace_bytes -- bytes of split-KV workspace a decode call
  * with these sizes needs (0 on invalid sizes).  It depends on Hq / Hkv, D and
  * the current device's SM count (148 assumed when no device is visible), not

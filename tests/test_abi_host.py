@@ -122,10 +122,39 @@ def test_decode_chunk_validation(lib):
     assert lib.attn_decode_ex(ctypes.byref(p)) == B.ATTN_ERR_INVALID_ARG
 
 
+def multi(lib, **kw):
+    p = B.attn_decode_multi_params()
+    p.q = p.kcache = p.vcache = p.kv_lens = p.out = FAKE
+    p.B, p.Hq, p.Hkv, p.Lq, p.Lmax, p.D, p.scale = 2, 8, 2, 4, 64, 128, 0.1
+    for k, v in kw.items():
+        setattr(p, k, v)
+    return lib.attn_decode_multi(ctypes.byref(p))
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), B.ATTN_ERR_INVALID_ARG),
+    (dict(kv_lens=None), B.ATTN_ERR_INVALID_ARG),
+    (dict(Lq=0), B.ATTN_ERR_INVALID_ARG),
+    (dict(Lq=-3), B.ATTN_ERR_INVALID_ARG),
+    (dict(Hq=6, Hkv=4), B.ATTN_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), B.ATTN_ERR_INVALID_ARG),
+    (dict(out_dtype=5), B.ATTN_ERR_INVALID_ARG),
+    (dict(D=96), B.ATTN_ERR_UNSUPPORTED),
+    (dict(Lq=33), B.ATTN_ERR_UNSUPPORTED),           # 4 heads x 33 tokens > one 128-row tile
+    (dict(Hq=32, Hkv=2, Lq=9), B.ATTN_ERR_UNSUPPORTED),
+    (dict(B=65535, Hkv=2, Hq=2, Lq=1), B.ATTN_ERR_UNSUPPORTED),  # more items than counter slots
+    (dict(out=FAKE + 4), B.ATTN_ERR_ALIGNMENT),
+    (dict(kv_lens=FAKE + 2), B.ATTN_ERR_ALIGNMENT),
+])
+def test_decode_multi_validation(lib, kw, code):
+    assert multi(lib, **kw) == code
+
+
 def test_empty_inputs_are_noops(lib):
     assert fwd(lib, B=0) == B.ATTN_OK
     assert fwd(lib, Lq=0) == B.ATTN_OK
     assert dec(lib, B=0) == B.ATTN_OK
+    assert multi(lib, B=0) == B.ATTN_OK
 
 
 def test_no_cpu_fallback(lib):
@@ -135,6 +164,7 @@ def test_no_cpu_fallback(lib):
         pytest.skip("a GPU is present")
     assert fwd(lib) in (B.ATTN_ERR_UNSUPPORTED, B.ATTN_ERR_CUDA)
     assert dec(lib) in (B.ATTN_ERR_UNSUPPORTED, B.ATTN_ERR_CUDA)
+    assert multi(lib) in (B.ATTN_ERR_UNSUPPORTED, B.ATTN_ERR_CUDA)
 
 
 def test_workspace_bytes_formula(lib):
