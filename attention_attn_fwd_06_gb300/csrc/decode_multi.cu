@@ -91,7 +91,7 @@ struct MultiArgs {
   void* out;
   float* lse;
   float* part_o;       // fp32 [2 * grid][R][D]: unnormalised O of a partial piece
-  float* part_ml;      // fp32 [2 * grid][R][2]: (m in log2 units, l)
+  float* part_ml;      // fp32 [2 * grid][R][2]: (m in log2 units, l); 8-byte aligned
   unsigned* counters;  // [2 + b * Hkv + hk]: partials landed per item; zero between calls
   int B, Hq, Hkv, Lq, Lmax;
   int GP;              // query heads per kv head
@@ -287,27 +287,58 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kWarpTMA) {
     // ---------------- TMA producer ----------------
+    // A piece's Q load must wait until every S MMA of the previous piece has completed (one Q buffer), but its
+    // K/V tiles need only free ring slots: they are issued as soon as slots free up, and the Q load goes out
+    // from inside the slot waits the moment the previous piece releases the buffer, so a piece boundary does
+    // not drain the ring.
     if (lane == 0) {
       tc::tma_prefetch_desc(&tmq);
       tc::tma_prefetch_desc(&tmk);
       tc::tma_prefetch_desc(&tmv);
-      int kv = 0;  // K/V tiles issued (ring position)
-      int qj = 0;  // pieces whose Q was loaded
+      int kv = 0;        // K/V tiles issued (ring position)
+      int q_issued = 0;  // Q loads issued (one per piece)
+      bool q_pending = false;
+      int q_row = 0;     // first q row of the piece whose Q is pending
       bool ok = true;
-      while (ok && walk_next(walk, a, pc)) {
-        if (qj > 0 && !mbar_wait(q_empty, (qj - 1) & 1, a.status, abort_flag)) {
-          ok = false;
-          break;
-        }
+      auto issue_q = [&]() {
         mbar_arrive_expect_tx(q_full, (uint32_t)a.q_box_bytes);
-        const int qrow = (pc.b * a.Hq + pc.hk * a.GP) * a.Lq;
-        for (int db = 0; db < C::NDB; ++db) tc::tma_load_3d(Qs + db * C::BLOCK_BYTES, &tmq, db * 64, qrow, 0, q_full);
-        ++qj;
+        for (int db = 0; db < C::NDB; ++db) tc::tma_load_3d(Qs + db * C::BLOCK_BYTES, &tmq, db * 64, q_row, 0, q_full);
+        ++q_issued;
+        q_pending = false;
+      };
+      auto poll_q = [&]() {
+        if (q_pending && (q_issued == 0 || mbar_try_wait(q_empty, (q_issued - 1) & 1))) issue_q();
+      };
+      // Bounded wait on a ring barrier that keeps issuing the pending Q load when it becomes possible.
+      auto wait_slot = [&](uint64_t* bar, uint32_t parity) -> bool {
+        const uint64_t t0 = globaltimer_ns();
+        while (true) {
+          poll_q();
+          if (mbar_try_wait(bar, parity)) return true;
+          if (*abort_flag) return false;
+          if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            record_status(a.status, ATTN_ERR_DEVICE_TIMEOUT);
+            *abort_flag = 1;
+            return false;
+          }
+        }
+      };
+      while (ok && walk_next(walk, a, pc)) {
+        if (q_pending) {  // the previous piece's Q is still waiting for the buffer: it goes first
+          if (!mbar_wait(q_empty, (q_issued - 1) & 1, a.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          issue_q();
+        }
+        q_row = (pc.b * a.Hq + pc.hk * a.GP) * a.Lq;
+        q_pending = true;
+        poll_q();
         const int khead = pc.b * a.Hkv + pc.hk;
         for (int tt = pc.t0; tt < pc.t1; ++tt) {
           const int slot = kv % C::NS;
           const int krow = (tt == pc.T - 1) ? pc.n - BN : tt * BN;  // the last tile ends at key n
-          if (kv >= C::NS && !mbar_wait(&k_empty[slot], ((kv / C::NS) - 1) & 1, a.status, abort_flag)) {
+          if (kv >= C::NS && !wait_slot(&k_empty[slot], ((kv / C::NS) - 1) & 1)) {
             ok = false;
             break;
           }
@@ -315,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int db = 0; db < C::NDB; ++db)
             tc::tma_load_3d(Ks + slot * C::TILE_BYTES + db * C::BLOCK_BYTES, &tmk, db * 64, krow, khead,
                             &k_full[slot]);
-          if (kv >= C::NS && !mbar_wait(&v_empty[slot], ((kv / C::NS) - 1) & 1, a.status, abort_flag)) {
+          if (kv >= C::NS && !wait_slot(&v_empty[slot], ((kv / C::NS) - 1) & 1)) {
             mbar_wait(&k_full[slot], (kv / C::NS) & 1, a.status, nullptr);  // K is in flight: let it land
             ok = false;
             break;
@@ -327,8 +358,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++kv;
         }
       }
+      if (ok && q_pending) {
+        if (mbar_wait(q_empty, (q_issued - 1) & 1, a.status, abort_flag)) issue_q();
+      }
       if (*abort_flag) {  // let in-flight copies land before shared memory is released
-        if (qj > 0) mbar_wait(q_full, (qj - 1) & 1, a.status, nullptr);
+        if (q_issued > 0) mbar_wait(q_full, (q_issued - 1) & 1, a.status, nullptr);
         for (int g = (kv > C::NS ? kv - C::NS : 0); g < kv; ++g) {
           mbar_wait(&k_full[g % C::NS], (g / C::NS) & 1, a.status, nullptr);
           mbar_wait(&v_full[g % C::NS], (g / C::NS) & 1, a.status, nullptr);
@@ -559,10 +593,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     __uint_as_float(orr[4 * v4 + 2]), __uint_as_float(orr[4 * v4 + 3]));
           }
         }
-        if (real) {
-          a.part_ml[prow * 2] = m_ref;
-          a.part_ml[prow * 2 + 1] = l;
-        }
+        if (real) reinterpret_cast<float2*>(a.part_ml)[prow] = make_float2(m_ref, l);
       }
       // Publish (the barrier orders every softmax thread's stores before thread 0's release atomic); the CTA
       // that lands the item's last partial merges them all.  After a failure nothing is published.
@@ -579,50 +610,82 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       named_bar_sync(1, kSoftmaxThreads);
       if (*last_flag) {
-        // Merge: warp sw takes rows sw, sw+4, ...; each lane D/32 consecutive columns.
-        constexpr int VPT = D / 32;
-        for (int r = sw; r < a.R; r += 4) {
-          float M = -INFINITY;
-          for (int i = lane; i < pc.np; i += 32)
-            M = fmaxf(M, __ldcg(a.part_ml + ((size_t)slot_of(pc, i) * a.R + r) * 2));
+        // Merge: the 128 threads split the item's rows into 32-column chunks; each thread folds the partials of
+        // its chunks in slot order with a running max (fixed order: bitwise reproducible), two partials' loads
+        // in flight at a time.
+        constexpr int CPR = D / 32;  // chunks per row
+        for (int e = stid; e < a.R * CPR; e += kSoftmaxThreads) {
+          const int r = e / CPR;
+          const int ch = e - r * CPR;
+          float M = -INFINITY, L = 0.f;
+          float4 acc[8];
 #pragma unroll
-          for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-          float L = 0.f;
-          float acc[VPT];
+          for (int j = 0; j < 8; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+          auto fold = [&](float2 ml, const float4 (&o)[8]) {
+            if (ml.x > M) {  // new running max: rescale what was folded so far (nothing while M is -inf)
+              const float sc = (M == -INFINITY) ? 0.f : ex2_approx(M - ml.x);
 #pragma unroll
-          for (int v = 0; v < VPT; ++v) acc[v] = 0.f;
-          for (int i = 0; i < pc.np; ++i) {
-            const size_t pr = (size_t)slot_of(pc, i) * a.R + r;
-            const float mi = __ldcg(a.part_ml + pr * 2);
-            const float li = __ldcg(a.part_ml + pr * 2 + 1);
-            const float wgt = (mi == -INFINITY) ? 0.f : ex2_approx(mi - M);
-            L = fmaf(wgt, li, L);
-            const float* src = a.part_o + pr * D + lane * VPT;
-            if constexpr (VPT == 4) {
-              const float4 o4 = __ldcg(reinterpret_cast<const float4*>(src));
-              acc[0] = fmaf(wgt, o4.x, acc[0]);
-              acc[1] = fmaf(wgt, o4.y, acc[1]);
-              acc[2] = fmaf(wgt, o4.z, acc[2]);
-              acc[3] = fmaf(wgt, o4.w, acc[3]);
-            } else {
-              const float2 o2 = __ldcg(reinterpret_cast<const float2*>(src));
-              acc[0] = fmaf(wgt, o2.x, acc[0]);
-              acc[1] = fmaf(wgt, o2.y, acc[1]);
+              for (int j = 0; j < 8; ++j)
+                acc[j] = make_float4(acc[j].x * sc, acc[j].y * sc, acc[j].z * sc, acc[j].w * sc);
+              L *= sc;
+              M = ml.x;
             }
+            const float w = (ml.x == -INFINITY) ? 0.f : ex2_approx(ml.x - M);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              acc[j].x = fmaf(w, o[j].x, acc[j].x);
+              acc[j].y = fmaf(w, o[j].y, acc[j].y);
+              acc[j].z = fmaf(w, o[j].z, acc[j].z);
+              acc[j].w = fmaf(w, o[j].w, acc[j].w);
+            }
+            L = fmaf(w, ml.y, L);
+          };
+          int i = 0;
+          for (; i + 1 < pc.np; i += 2) {
+            const size_t p0 = (size_t)slot_of(pc, i) * a.R + r;
+            const size_t p1 = (size_t)slot_of(pc, i + 1) * a.R + r;
+            const float2 ml0 = __ldcg(reinterpret_cast<const float2*>(a.part_ml) + p0);
+            const float2 ml1 = __ldcg(reinterpret_cast<const float2*>(a.part_ml) + p1);
+            const float4* s0 = reinterpret_cast<const float4*>(a.part_o + p0 * D + ch * 32);
+            const float4* s1 = reinterpret_cast<const float4*>(a.part_o + p1 * D + ch * 32);
+            float4 o0[8], o1[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              o0[j] = __ldcg(s0 + j);
+              o1[j] = __ldcg(s1 + j);
+            }
+            fold(ml0, o0);
+            fold(ml1, o1);
+          }
+          if (i < pc.np) {
+            const size_t p0 = (size_t)slot_of(pc, i) * a.R + r;
+            const float2 ml0 = __ldcg(reinterpret_cast<const float2*>(a.part_ml) + p0);
+            const float4* s0 = reinterpret_cast<const float4*>(a.part_o + p0 * D + ch * 32);
+            float4 o0[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) o0[j] = __ldcg(s0 + j);
+            fold(ml0, o0);
           }
           const float inv_L = (L > 0.f) ? 1.f / L : 0.f;
           const size_t orow = row0 + r;
           if (a.out_f32) {
-            float* dst = reinterpret_cast<float*>(a.out) + orow * D + lane * VPT;
+            float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(a.out) + orow * D + ch * 32);
 #pragma unroll
-            for (int v = 0; v < VPT; ++v) dst[v] = acc[v] * inv_L;
+            for (int j = 0; j < 8; ++j)
+              dst[j] = make_float4(acc[j].x * inv_L, acc[j].y * inv_L, acc[j].z * inv_L, acc[j].w * inv_L);
           } else {
-            __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(a.out) + orow * D + lane * VPT;
+            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.out) + orow * D + ch * 32);
 #pragma unroll
-            for (int v = 0; v < VPT; v += 2)
-              *reinterpret_cast<uint32_t*>(dst + v) = tc::pack_bf16x2(acc[v] * inv_L, acc[v + 1] * inv_L);
+            for (int j = 0; j < 4; ++j) {
+              uint4 wv;
+              wv.x = tc::pack_bf16x2(acc[2 * j].x * inv_L, acc[2 * j].y * inv_L);
+              wv.y = tc::pack_bf16x2(acc[2 * j].z * inv_L, acc[2 * j].w * inv_L);
+              wv.z = tc::pack_bf16x2(acc[2 * j + 1].x * inv_L, acc[2 * j + 1].y * inv_L);
+              wv.w = tc::pack_bf16x2(acc[2 * j + 1].z * inv_L, acc[2 * j + 1].w * inv_L);
+              dst[j] = wv;
+            }
           }
-          if (lane == 0 && a.lse != nullptr) a.lse[orow] = (L > 0.f) ? (M + log2f(L)) * kLn2 : -INFINITY;
+          if (ch == 0 && a.lse != nullptr) a.lse[orow] = (L > 0.f) ? (M + log2f(L)) * kLn2 : -INFINITY;
         }
       }
       named_bar_sync(1, kSoftmaxThreads);  // last_flag is reused by the next piece
