@@ -19,7 +19,7 @@ from dataclasses import dataclass, field
 import torch
 
 __all__ = ["Workload", "WORKLOADS", "make_prefill", "make_decode", "make_decode_multi", "make_varlen", "make_pages",
-           "randn_bf16"]
+           "randn_bf16", "rope_tables"]
 
 
 @dataclass(frozen=True)
@@ -177,3 +177,11 @@ def make_pages(kcache, vcache, page_size, seed, spare_pages=3, fill_unused=float
             kp[pid, :, : hi - lo] = kcache[b, :, lo:hi]
             vp[pid, :, : hi - lo] = vcache[b, :, lo:hi]
     return kp, vp, table
+
+
+def rope_tables(max_pos: int, D: int, base: float = 10000.0):
+    """Rotary-embedding tables (model constants handed to the kernels as data): fp32 [max_pos, D/2] cosines
+    and sines of the angles p * base^(-2i/D), the usual frequency ladder, evaluated in fp64."""
+    inv = base ** (-torch.arange(0, D // 2, dtype=torch.float64) * 2.0 / D)
+    ang = torch.arange(max_pos, dtype=torch.float64)[:, None] * inv[None, :]
+    return torch.cos(ang).float().contiguous(), torch.sin(ang).float().contiguous()

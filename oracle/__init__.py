@@ -18,6 +18,7 @@ from .sdpa import (  # noqa: F401
     decode,
     decode_multi,
     kv_head_of,
+    rope_rotate,
     log_sum_exp,
     scores,
     softmax_two_pass,

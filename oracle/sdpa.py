@@ -35,6 +35,16 @@ design notes of the repository):
   ``exp(S - m)`` -- the two quantities the §3.4 online listing carries.
 * A row with no visible key (only possible for causal Lq > Lkv, or a decode
   sequence with kv_len == 0) yields O = 0 and lse = -inf.
+* RoPE (rotary position embedding), which "Что такое kernel fusion и как он
+  применяется в LLM serving?" §3.5 and the Operator Fusion page's exercise 1
+  name as fusable into the attention kernel without giving its formula, is
+  read as the standard rotary embedding: pair i of a row at position p is
+  turned by the angle whose cosine and sine the caller's tables hold at
+  [p, i], ``(a, b) -> (a cos - b sin, b cos + a sin)``, the pairs being
+  dims (i, i + D/2) ("half") or (2i, 2i + 1) ("interleaved").  Queries and
+  keys take the positions the causal alignment gives them: key j sits at j,
+  query i of Lq at ``Lkv - Lq + i``; a decode token at ``kv_len - Lq + t``.
+  Cached keys are stored already rotated (decode rotates only q).
 
 Inputs are taken as given (typically bf16 values already rounded, passed as
 float32/float64 arrays or CPU torch tensors) and promoted to fp64.
@@ -57,6 +67,7 @@ __all__ = [
     "attention_varlen_rows",
     "decode",
     "decode_multi",
+    "rope_rotate",
 ]
 
 
@@ -131,27 +142,69 @@ def log_sum_exp(m: np.ndarray, l: np.ndarray) -> np.ndarray:
         return np.where(l > 0, m + np.log(np.where(l > 0, l, 1.0)), -np.inf)
 
 
+def rope_rotate(x, positions, cos, sin, style: str) -> np.ndarray:
+    """Rotary position embedding of the rows of ``x`` (fp64).
+
+    x [..., L, D]; positions [L] (row r sits at positions[r]); cos/sin
+    [max_pos, D/2] tables whose row p holds the cosines and sines of the
+    angles of the D/2 pairs at position p.  Pair i of a row, (a, b), becomes
+    ``(a cos - b sin, b cos + a sin)`` -- a plane rotation of the pair.  Pairs
+    are dims (i, i + D/2) for ``style == "half"`` and (2i, 2i + 1) for
+    ``style == "interleaved"``.
+    """
+    x = to_f64(x)
+    D = x.shape[-1]
+    pos = np.asarray(positions, dtype=np.int64)
+    c = to_f64(cos)[pos]  # [L, D/2]
+    s = to_f64(sin)[pos]
+    if style == "half":
+        a, b = x[..., : D // 2], x[..., D // 2:]
+        return np.concatenate([a * c - b * s, b * c + a * s], axis=-1)
+    if style == "interleaved":
+        a, b = x[..., 0::2], x[..., 1::2]
+        out = np.empty_like(x)
+        out[..., 0::2] = a * c - b * s
+        out[..., 1::2] = b * c + a * s
+        return out
+    raise ValueError(f"unknown rope style {style!r}")
+
+
+def _rope_q_k(Qh, Kh, Lq, Lkv, rope, rotate_k=True):
+    """Rotate a head's query rows (positions Lkv - Lq + i) and key rows (positions j) when ``rope`` is given."""
+    if rope is None:
+        return Qh, Kh
+    cos, sin, style = rope
+    Qh = rope_rotate(Qh, np.arange(Lq) + (Lkv - Lq), cos, sin, style)
+    if rotate_k:
+        Kh = rope_rotate(Kh, np.arange(Lkv), cos, sin, style)
+    return Qh, Kh
+
+
 def _check_heads(Hq: int, Hkv: int):
     if Hkv <= 0 or Hq % Hkv != 0:
         raise ValueError(f"Hq={Hq} must be a positive multiple of Hkv={Hkv}")
 
 
-def attention(q, k, v, scale: float, causal: bool):
-    """Dense prefill: q [B,Hq,Lq,D], k/v [B,Hkv,Lkv,D] -> O [B,Hq,Lq,D], lse [B,Hq,Lq]."""
+def attention(q, k, v, scale: float, causal: bool, rope=None):
+    """Dense prefill: q [B,Hq,Lq,D], k/v [B,Hkv,Lkv,D] -> O [B,Hq,Lq,D], lse [B,Hq,Lq].
+
+    ``rope = (cos, sin, style)`` rotates q and k first (see :func:`rope_rotate`).
+    """
     q, k, v = to_f64(q), to_f64(k), to_f64(v)
     B, Hq, Lq, D = q.shape
-    Hkv = k.shape[1]
+    Hkv, Lkv = k.shape[1], k.shape[2]
     _check_heads(Hq, Hkv)
     O = np.zeros((B, Hq, Lq, v.shape[3]))
     lse = np.zeros((B, Hq, Lq))
     for b in range(B):
         for h in range(Hq):
             hk = kv_head_of(h, Hq, Hkv)
-            O[b, h], lse[b, h] = attention_head(q[b, h], k[b, hk], v[b, hk], scale, causal)
+            Qh, Kh = _rope_q_k(q[b, h], k[b, hk], Lq, Lkv, rope)
+            O[b, h], lse[b, h] = attention_head(Qh, Kh, v[b, hk], scale, causal)
     return O, lse
 
 
-def attention_rows(q, k, v, scale: float, causal: bool, b: int, h: int, rows):
+def attention_rows(q, k, v, scale: float, causal: bool, b: int, h: int, rows, rope=None):
     """Selected query rows of one (batch, head) of :func:`attention`.
 
     Each row is computed from its own definition (its scores against every
@@ -165,10 +218,15 @@ def attention_rows(q, k, v, scale: float, causal: bool, b: int, h: int, rows):
     hk = kv_head_of(h, Hq, Hkv)
     vis = visible_mask(Lq, Lkv, causal)[rows]
     Qh = to_f64(q[b, h])[rows]  # promote only the slices this row set reads
-    return attention_head(Qh, to_f64(k[b, hk]), to_f64(v[b, hk]), scale, causal, visible=vis)
+    Kh = to_f64(k[b, hk])
+    if rope is not None:
+        cos, sin, style = rope
+        Qh = rope_rotate(Qh, rows + (Lkv - Lq), cos, sin, style)
+        Kh = rope_rotate(Kh, np.arange(Lkv), cos, sin, style)
+    return attention_head(Qh, Kh, to_f64(v[b, hk]), scale, causal, visible=vis)
 
 
-def attention_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, scale: float, causal: bool):
+def attention_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, scale: float, causal: bool, rope=None):
     """Packed variable-length prefill.
 
     q [total_q, Hq, D], k/v [total_k, Hkv, D]; sequence s owns rows
@@ -187,14 +245,15 @@ def attention_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, scale: float, causal: 
         qs, qe, ks, ke = cq[s], cq[s + 1], ck[s], ck[s + 1]
         for h in range(Hq):
             hk = kv_head_of(h, Hq, Hkv)
-            o, ls = attention_head(q[qs:qe, h], k[ks:ke, hk], v[ks:ke, hk], scale, causal)
+            Qh, Kh = _rope_q_k(q[qs:qe, h], k[ks:ke, hk], qe - qs, ke - ks, rope)
+            o, ls = attention_head(Qh, Kh, v[ks:ke, hk], scale, causal)
             O[qs:qe, h] = o
             lse[qs:qe, h] = ls
     return O, lse
 
 
 def attention_varlen_rows(q, k, v, cu_seqlens_q, cu_seqlens_k, scale: float, causal: bool,
-                          seq: int, h: int, rows):
+                          seq: int, h: int, rows, rope=None):
     """Selected rows (relative to the start of sequence ``seq``) of :func:`attention_varlen`."""
     cq = np.asarray(cu_seqlens_q, dtype=np.int64)
     ck = np.asarray(cu_seqlens_k, dtype=np.int64)
@@ -205,17 +264,24 @@ def attention_varlen_rows(q, k, v, cu_seqlens_q, cu_seqlens_k, scale: float, cau
     hk = kv_head_of(h, Hq, Hkv)
     vis = visible_mask(qe - qs, ke - ks, causal)[rows]
     Qh = to_f64(q[qs:qe, h])[rows]
-    return attention_head(Qh, to_f64(k[ks:ke, hk]), to_f64(v[ks:ke, hk]), scale, causal, visible=vis)
+    Kh = to_f64(k[ks:ke, hk])
+    if rope is not None:
+        cos, sin, style = rope
+        Qh = rope_rotate(Qh, rows + ((ke - ks) - (qe - qs)), cos, sin, style)
+        Kh = rope_rotate(Kh, np.arange(ke - ks), cos, sin, style)
+    return attention_head(Qh, Kh, to_f64(v[ks:ke, hk]), scale, causal, visible=vis)
 
 
-def decode(q, kcache, vcache, kv_lens, scale: float, heads=None):
+def decode(q, kcache, vcache, kv_lens, scale: float, heads=None, rope=None):
     """Single-token decode over a KV cache.
 
     q [B,Hq,D], kcache/vcache [B,Hkv,Lmax,D], kv_lens [B].  The new token of
     sequence b attends to cached keys ``0 .. kv_lens[b]-1`` (decoder-attention
     page, "structure of attention in decoding mode").  Returns O [B,Hq,D] and
     lse [B,Hq].  ``heads`` optionally restricts the work to a list of (b, hq)
-    pairs; the other entries are left as NaN.
+    pairs; the other entries are left as NaN.  With ``rope = (cos, sin,
+    style)`` the query is rotated to its position kv_lens[b] - 1; the cached
+    keys are used as stored (already rotated).
     """
     q = to_f64(q)
     lens = np.asarray(kv_lens, dtype=np.int64)
@@ -230,13 +296,13 @@ def decode(q, kcache, vcache, kv_lens, scale: float, heads=None):
         n = int(lens[b])
         hk = kv_head_of(h, Hq, Hkv)
         # promote only the cache rows this sequence attends to
-        o, ls = attention_head(q[b, h][None, :], to_f64(kcache[b, hk, :n]), to_f64(vcache[b, hk, :n]), scale,
-                               causal=False)
+        Qh, _ = _rope_q_k(q[b, h][None, :], None, 1, n, rope, rotate_k=False)
+        o, ls = attention_head(Qh, to_f64(kcache[b, hk, :n]), to_f64(vcache[b, hk, :n]), scale, causal=False)
         O[b, h], lse[b, h] = o[0], ls[0]
     return O, lse
 
 
-def decode_multi(q, kcache, vcache, kv_lens, scale: float, heads=None):
+def decode_multi(q, kcache, vcache, kv_lens, scale: float, heads=None, rope=None):
     """Decode of several new tokens per sequence over a KV cache.
 
     q [B,Hq,Lq,D], kcache/vcache [B,Hkv,Lmax,D], kv_lens [B].  Rows
@@ -250,7 +316,9 @@ def decode_multi(q, kcache, vcache, kv_lens, scale: float, heads=None):
     against K/V blocks loaded once; what each token computes is the single
     decode above over its own visible prefix.  Returns O [B,Hq,Lq,D] and
     lse [B,Hq,Lq]; ``heads`` optionally restricts the work to (b, hq) pairs,
-    the other entries being NaN.
+    the other entries being NaN.  With ``rope = (cos, sin, style)`` token t
+    is rotated to its position kv_lens[b] - Lq + t; cached keys are used as
+    stored (already rotated).
     """
     q = to_f64(q)
     lens = np.asarray(kv_lens, dtype=np.int64)
@@ -264,6 +332,7 @@ def decode_multi(q, kcache, vcache, kv_lens, scale: float, heads=None):
     for b, h in heads:
         n = int(lens[b])
         hk = kv_head_of(h, Hq, Hkv)
-        O[b, h], lse[b, h] = attention_head(q[b, h], to_f64(kcache[b, hk, :n]), to_f64(vcache[b, hk, :n]), scale,
+        Qh, _ = _rope_q_k(q[b, h], None, Lq, n, rope, rotate_k=False)
+        O[b, h], lse[b, h] = attention_head(Qh, to_f64(kcache[b, hk, :n]), to_f64(vcache[b, hk, :n]), scale,
                                             causal=True)
     return O, lse

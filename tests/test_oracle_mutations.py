@@ -13,7 +13,30 @@ from tests.test_oracle_pins import PINS
 
 _orig = {name: getattr(OA, name) for name in
          ("scores", "visible_mask", "kv_head_of", "softmax_two_pass", "log_sum_exp", "attention_head",
-          "decode_multi")}
+          "decode_multi", "rope_rotate", "_rope_q_k")}
+
+
+def _rope_backwards(x, positions, cos, sin, style):
+    return _orig["rope_rotate"](x, positions, cos, -np.asarray(sin), style)
+
+
+def _rope_styles_swapped(x, positions, cos, sin, style):
+    return _orig["rope_rotate"](x, positions, cos, sin, "interleaved" if style == "half" else "half")
+
+
+def _rope_query_from_zero(Qh, Kh, Lq, Lkv, rope, rotate_k=True):
+    # queries rotated to positions 0 .. Lq-1 instead of Lkv-Lq .. Lkv-1
+    if rope is None:
+        return Qh, Kh
+    cos, sin, style = rope
+    Qh = OA.rope_rotate(Qh, np.arange(Lq), cos, sin, style)
+    if rotate_k:
+        Kh = OA.rope_rotate(Kh, np.arange(Lkv), cos, sin, style)
+    return Qh, Kh
+
+
+def _rope_keys_not_rotated(Qh, Kh, Lq, Lkv, rope, rotate_k=True):
+    return _orig["_rope_q_k"](Qh, Kh, Lq, Lkv, rope, rotate_k=False)
 
 
 def _softmax_wrong_axis(S, visible):
@@ -41,7 +64,7 @@ def _attention_head_k_for_v(Qh, Kh, Vh, scale, causal, visible=None):
 
 def _multi_with_mask(mask_of):
     """decode_multi with the visible set of token t over n keys given by mask_of(Lq, n) instead."""
-    def bad(q, kcache, vcache, kv_lens, scale, heads=None):
+    def bad(q, kcache, vcache, kv_lens, scale, heads=None, rope=None):
         q = OA.to_f64(q)
         B, Hq, Lq, D = q.shape
         Hkv = kcache.shape[1]
@@ -77,6 +100,10 @@ MUTATIONS = {
         lambda Lq, n: np.arange(n)[None, :] <= np.arange(Lq)[:, None])),
     "multi_excludes_own_key": ("decode_multi", _multi_with_mask(
         lambda Lq, n: np.arange(n)[None, :] < np.arange(Lq)[:, None] + (n - Lq))),
+    "rope_backwards": ("rope_rotate", _rope_backwards),
+    "rope_styles_swapped": ("rope_rotate", _rope_styles_swapped),
+    "rope_query_from_zero": ("_rope_q_k", _rope_query_from_zero),
+    "rope_keys_not_rotated": ("_rope_q_k", _rope_keys_not_rotated),
 }
 
 

@@ -31,6 +31,7 @@ from oracle import sdpa as OA
 from oracle.brute import attention_loops
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "hand_worked.json")
+GOLDEN_ROPE = os.path.join(os.path.dirname(__file__), "golden", "rope_hand_worked.json")
 
 
 def _rng(seed):
@@ -315,6 +316,131 @@ def pin_decode_multi_golden():
     np.testing.assert_allclose(lse, np.array(c["lse"]), rtol=0, atol=1e-14)
 
 
+def _tables(max_pos, D, base=10000.0):
+    ang = np.arange(max_pos)[:, None] * base ** (-np.arange(D // 2) * 2.0 / D)[None, :]
+    return np.cos(ang), np.sin(ang)
+
+
+def pin_rope_golden():
+    """Rotations and one rotated attention worked by hand (tests/golden/rope_hand_worked.json)."""
+    with open(GOLDEN_ROPE) as f:
+        g = json.load(f)
+    for c in g["rotate"]:
+        out = OA.rope_rotate(np.array([c["x"]]), [0], np.array([c["cos"]]), np.array([c["sin"]]), c["style"])
+        np.testing.assert_allclose(out[0], c["out"], rtol=0, atol=1e-15, err_msg=c["name"])
+    for c in g["attention"]:
+        rope = (np.array(c["cos"]), np.array(c["sin"]), c["style"])
+        O, lse = OA.attention(np.array(c["q"]), np.array(c["k"]), np.array(c["v"]), c["scale"], c["causal"], rope=rope)
+        np.testing.assert_allclose(O, np.array(c["O"]), rtol=0, atol=1e-13, err_msg=c["name"])
+        np.testing.assert_allclose(lse, np.array(c["lse"]), rtol=0, atol=1e-13, err_msg=c["name"])
+
+
+def pin_rope_complex_form():
+    """Interleaved RoPE == multiplying each pair, read as a complex number, by cos + i sin (numpy complex)."""
+    r = _rng(170)
+    L, D = 7, 10
+    x = r.standard_normal((L, D))
+    cos, sin = _tables(20, D)
+    pos = r.integers(0, 20, L)
+    z = (x[:, 0::2] + 1j * x[:, 1::2]) * (cos[pos] + 1j * sin[pos])
+    want = np.empty_like(x)
+    want[:, 0::2], want[:, 1::2] = z.real, z.imag
+    np.testing.assert_allclose(OA.rope_rotate(x, pos, cos, sin, "interleaved"), want, atol=1e-14)
+
+
+def pin_rope_half_is_permuted_interleaved():
+    """Half-split RoPE == interleaved RoPE on the dims reordered (0, D/2, 1, D/2+1, ...) and back."""
+    r = _rng(171)
+    L, D = 5, 8
+    x = r.standard_normal((L, D))
+    cos, sin = _tables(9, D)
+    pos = r.integers(0, 9, L)
+    perm = np.stack([np.arange(D // 2), np.arange(D // 2) + D // 2], axis=1).reshape(-1)
+    got = OA.rope_rotate(x, pos, cos, sin, "half")
+    via = np.empty_like(x)
+    via[:, perm] = OA.rope_rotate(x[:, perm], pos, cos, sin, "interleaved")
+    np.testing.assert_allclose(got, via, atol=1e-15)
+
+
+def pin_rope_norms_and_relative_positions():
+    """A rotation keeps every pair's length, and rotated dot products depend only on the position difference."""
+    r = _rng(172)
+    D = 16
+    cos, sin = _tables(64, D)
+    q, k = r.standard_normal((3, D)), r.standard_normal((3, D))
+    for style in ("half", "interleaved"):
+        rq = OA.rope_rotate(q, [5, 9, 30], cos, sin, style)
+        np.testing.assert_allclose(np.linalg.norm(rq, axis=1), np.linalg.norm(q, axis=1), atol=1e-13)
+        for s in (1, 17):
+            a = OA.rope_rotate(q, [5, 9, 30], cos, sin, style) @ OA.rope_rotate(k, [2, 9, 12], cos, sin, style).T
+            b = OA.rope_rotate(q, [5 + s, 9 + s, 30 + s], cos, sin, style) @ \
+                OA.rope_rotate(k, [2 + s, 9 + s, 12 + s], cos, sin, style).T
+            np.testing.assert_allclose(np.diag(a), np.diag(b), atol=1e-12)
+
+
+def pin_rope_decode_is_last_prefill_row():
+    """Decode with RoPE over a cache of rotated keys == the last row of rotated causal prefill."""
+    r = _rng(173)
+    B, Hq, Hkv, Lmax, D = 2, 4, 2, 12, 8
+    lens = [12, 5]
+    cos, sin = _tables(16, D)
+    for style in ("half", "interleaved"):
+        rope = (cos, sin, style)
+        qd = r.standard_normal((B, Hq, D))
+        k = r.standard_normal((B, Hkv, Lmax, D))
+        v = r.standard_normal((B, Hkv, Lmax, D))
+        kc = OA.rope_rotate(k, np.arange(Lmax), cos, sin, style)
+        O, lse = OA.decode(qd, kc, v, lens, 0.4, rope=rope)
+        Om, lsem = OA.decode_multi(qd[:, :, None], kc, v, lens, 0.4, rope=rope)
+        for b, n in enumerate(lens):
+            qp = r.standard_normal((1, Hq, n, D))
+            qp[0, :, n - 1] = qd[b]
+            Op, lsep = OA.attention(qp, k[b:b + 1, :, :n], v[b:b + 1, :, :n], 0.4, True, rope=rope)
+            np.testing.assert_allclose(O[b], Op[0, :, n - 1], atol=1e-13)
+            np.testing.assert_allclose(lse[b], lsep[0, :, n - 1], atol=1e-13)
+            np.testing.assert_allclose(Om[b, :, 0], Op[0, :, n - 1], atol=1e-13)
+
+
+def pin_rope_multi_tokens_are_prefill_rows():
+    """Multi-token decode with RoPE == the last Lq rows of rotated causal prefill over each sequence's keys."""
+    r = _rng(174)
+    B, Hq, Hkv, Lq, Lmax, D = 2, 4, 2, 3, 10, 8
+    lens = [10, 6]
+    cos, sin = _tables(12, D)
+    rope = (cos, sin, "half")
+    q = r.standard_normal((B, Hq, Lq, D))
+    k = r.standard_normal((B, Hkv, Lmax, D))
+    v = r.standard_normal((B, Hkv, Lmax, D))
+    kc = OA.rope_rotate(k, np.arange(Lmax), cos, sin, "half")
+    O, lse = OA.decode_multi(q, kc, v, lens, 0.6, rope=rope)
+    for b, n in enumerate(lens):
+        Op, lsep = OA.attention(q[b:b + 1], k[b:b + 1, :, :n], v[b:b + 1, :, :n], 0.6, True, rope=rope)
+        np.testing.assert_allclose(O[b], Op[0], atol=1e-13)
+        np.testing.assert_allclose(lse[b], lsep[0], atol=1e-13)
+
+
+def pin_rope_rows_and_varlen_agree_with_dense():
+    """The row-sampled and packed forms rotate with the same positions as dense prefill."""
+    r = _rng(175)
+    Hq, Hkv, D = 4, 2, 8
+    cos, sin = _tables(32, D)
+    rope = (cos, sin, "interleaved")
+    lens = [9, 14]
+    cu = [0, 9, 23]
+    q, k, v = r.standard_normal((23, Hq, D)), r.standard_normal((23, Hkv, D)), r.standard_normal((23, Hkv, D))
+    Ov, lv = OA.attention_varlen(q, k, v, cu, cu, 0.5, True, rope=rope)
+    for s, n in enumerate(lens):
+        a, e = cu[s], cu[s + 1]
+        qd, kd, vd = (x[a:e].transpose(1, 0, 2)[None] for x in (q, k, v))
+        Od, ld = OA.attention(qd, kd, vd, 0.5, True, rope=rope)
+        np.testing.assert_allclose(Ov[a:e].transpose(1, 0, 2), Od[0], atol=1e-13)
+        rows = np.array([0, n - 1, n // 2])
+        Orr, lrr = OA.attention_rows(qd, kd, vd, 0.5, True, 0, 3, rows, rope=rope)
+        np.testing.assert_allclose(Orr, Od[0, 3, rows], atol=1e-13)
+        Ovr, lvr = OA.attention_varlen_rows(q, k, v, cu, cu, 0.5, True, s, 3, rows, rope=rope)
+        np.testing.assert_allclose(Ovr, Od[0, 3, rows], atol=1e-13)
+
+
 PINS = [
     pin_brute_force,
     pin_rows_sum_to_one,
@@ -336,6 +462,13 @@ PINS = [
     pin_decode_multi_rows_are_single_decodes,
     pin_decode_multi_brute_force,
     pin_decode_multi_golden,
+    pin_rope_golden,
+    pin_rope_complex_form,
+    pin_rope_half_is_permuted_interleaved,
+    pin_rope_norms_and_relative_positions,
+    pin_rope_decode_is_last_prefill_row,
+    pin_rope_multi_tokens_are_prefill_rows,
+    pin_rope_rows_and_varlen_agree_with_dense,
 ]
 
 
