@@ -47,6 +47,16 @@ EXPORTED = (
 )
 
 
+ATTN_ROPE_NONE = 0
+ATTN_ROPE_HALF = 1
+ATTN_ROPE_INTERLEAVED = 2
+_ROPE_STYLES = {"half": ATTN_ROPE_HALF, "interleaved": ATTN_ROPE_INTERLEAVED}
+
+
+class attn_rope(ctypes.Structure):
+    _fields_ = [("cos", ctypes.c_void_p), ("sin", ctypes.c_void_p), ("max_pos", ctypes.c_int), ("style", ctypes.c_int)]
+
+
 class AttnError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
@@ -63,6 +73,7 @@ class attn_fwd_params(ctypes.Structure):
         ("cu_seqlens_q", ctypes.c_void_p), ("cu_seqlens_k", ctypes.c_void_p),
         ("total_q", ctypes.c_int), ("total_k", ctypes.c_int),
         ("stream", ctypes.c_void_p),
+        ("rope", attn_rope),
     ]
 
 
@@ -75,6 +86,7 @@ class attn_decode_paged_params(ctypes.Structure):
         ("page_size", ctypes.c_int), ("max_pages", ctypes.c_int), ("num_pages", ctypes.c_int),
         ("scale", ctypes.c_float), ("out_dtype", ctypes.c_int), ("chunk", ctypes.c_int),
         ("stream", ctypes.c_void_p),
+        ("rope", attn_rope),
     ]
 
 
@@ -86,6 +98,7 @@ class attn_decode_multi_params(ctypes.Structure):
         ("Lmax", ctypes.c_int), ("D", ctypes.c_int),
         ("scale", ctypes.c_float), ("out_dtype", ctypes.c_int),
         ("stream", ctypes.c_void_p),
+        ("rope", attn_rope),
     ]
 
 
@@ -97,6 +110,7 @@ class attn_decode_params(ctypes.Structure):
         ("Lmax", ctypes.c_int), ("D", ctypes.c_int),
         ("scale", ctypes.c_float), ("out_dtype", ctypes.c_int), ("chunk", ctypes.c_int),
         ("stream", ctypes.c_void_p),
+        ("rope", attn_rope),
     ]
 
 
@@ -174,9 +188,30 @@ def _need(t, name, dtype, ndim):
         raise ValueError(f"{name} must be contiguous")
 
 
+def _set_rope(p, rope, D, device):
+    """rope = (cos, sin, style): fp32 device tables [max_pos, D/2] and "half" or "interleaved" (None: off)."""
+    if rope is None:
+        return
+    cos, sin, style = rope
+    for t, name in ((cos, "rope cos"), (sin, "rope sin")):
+        _need(t, name, torch.float32, 2)
+        if t.device != device or t.shape[1] != D // 2:
+            raise ValueError(f"{name} must be [max_pos, D/2] on {device}")
+    if cos.shape != sin.shape:
+        raise ValueError("rope cos and sin tables differ in shape")
+    if style not in _ROPE_STYLES:
+        raise ValueError("rope style must be 'half' or 'interleaved'")
+    p.rope.cos, p.rope.sin = _ptr(cos), _ptr(sin)
+    p.rope.max_pos = cos.shape[0]
+    p.rope.style = _ROPE_STYLES[style]
+
+
 def attn_fwd(q, k, v, out=None, lse=None, causal=True, scale=None, out_dtype=torch.bfloat16,
-             want_lse=True, stream=None):
-    """Dense prefill: q [B,Hq,Lq,D], k/v [B,Hkv,Lkv,D] bf16 -> (out [B,Hq,Lq,D], lse [B,Hq,Lq] fp32)."""
+             want_lse=True, stream=None, rope=None):
+    """Dense prefill: q [B,Hq,Lq,D], k/v [B,Hkv,Lkv,D] bf16 -> (out [B,Hq,Lq,D], lse [B,Hq,Lq] fp32).
+
+    ``rope = (cos, sin, style)`` rotates q and k in the kernel (fp32 device tables [max_pos, D/2];
+    style "half" or "interleaved"); every call of this module takes the same argument."""
     _need(q, "q", torch.bfloat16, 4)
     _need(k, "k", torch.bfloat16, 4)
     _need(v, "v", torch.bfloat16, 4)
@@ -198,12 +233,13 @@ def attn_fwd(q, k, v, out=None, lse=None, causal=True, scale=None, out_dtype=tor
     p.causal = int(bool(causal))
     p.out_dtype = ATTN_DTYPE_F32 if out_dtype == torch.float32 else ATTN_DTYPE_BF16
     p.stream = _stream_handle(stream, q.device)
+    _set_rope(p, rope, D, q.device)
     _check(load().attn_fwd_ex(ctypes.byref(p)), "attn_fwd")
     return out, lse
 
 
 def attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, out=None, lse=None,
-                    causal=True, scale=None, out_dtype=torch.bfloat16, want_lse=True, stream=None):
+                    causal=True, scale=None, out_dtype=torch.bfloat16, want_lse=True, stream=None, rope=None):
     """Packed prefill: q [total_q,Hq,D], k/v [total_k,Hkv,D] bf16, cu_seqlens int32 [B+1] on the device."""
     _need(q, "q", torch.bfloat16, 3)
     _need(k, "k", torch.bfloat16, 3)
@@ -231,12 +267,13 @@ def attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqle
     p.cu_seqlens_q, p.cu_seqlens_k = _ptr(cu_seqlens_q), _ptr(cu_seqlens_k)
     p.total_q, p.total_k = total_q, total_k
     p.stream = _stream_handle(stream, q.device)
+    _set_rope(p, rope, D, q.device)
     _check(load().attn_fwd_ex(ctypes.byref(p)), "attn_fwd_ex")
     return out, lse
 
 
 def attn_decode(q, kcache, vcache, kv_lens, out=None, lse=None, scale=None, chunk=0,
-                out_dtype=torch.bfloat16, want_lse=True, stream=None):
+                out_dtype=torch.bfloat16, want_lse=True, stream=None, rope=None):
     """Decode: q [B,Hq,D], caches [B,Hkv,Lmax,D] bf16, kv_lens int32 [B] -> (out [B,Hq,D], lse [B,Hq])."""
     _need(q, "q", torch.bfloat16, 3)
     _need(kcache, "kcache", torch.bfloat16, 4)
@@ -262,12 +299,13 @@ def attn_decode(q, kcache, vcache, kv_lens, out=None, lse=None, scale=None, chun
     p.out_dtype = ATTN_DTYPE_F32 if out_dtype == torch.float32 else ATTN_DTYPE_BF16
     p.chunk = int(chunk)
     p.stream = _stream_handle(stream, q.device)
+    _set_rope(p, rope, D, q.device)
     _check(load().attn_decode_ex(ctypes.byref(p)), "attn_decode")
     return out, lse
 
 
 def attn_decode_paged(q, kpages, vpages, block_table, kv_lens, out=None, lse=None, scale=None, chunk=0,
-                      out_dtype=torch.bfloat16, want_lse=True, stream=None):
+                      out_dtype=torch.bfloat16, want_lse=True, stream=None, rope=None):
     """Decode over a paged cache: pages [num_pages,Hkv,page_size,D] bf16, block_table int32 [B,max_pages]."""
     _need(q, "q", torch.bfloat16, 3)
     _need(kpages, "kpages", torch.bfloat16, 4)
@@ -296,12 +334,13 @@ def attn_decode_paged(q, kpages, vpages, block_table, kv_lens, out=None, lse=Non
     p.out_dtype = ATTN_DTYPE_F32 if out_dtype == torch.float32 else ATTN_DTYPE_BF16
     p.chunk = int(chunk)
     p.stream = _stream_handle(stream, q.device)
+    _set_rope(p, rope, D, q.device)
     _check(load().attn_decode_paged(ctypes.byref(p)), "attn_decode_paged")
     return out, lse
 
 
 def attn_decode_multi(q, kcache, vcache, kv_lens, out=None, lse=None, scale=None, out_dtype=torch.bfloat16,
-                      want_lse=True, stream=None):
+                      want_lse=True, stream=None, rope=None):
     """Multi-token decode: q [B,Hq,Lq,D], caches [B,Hkv,Lmax,D] bf16, kv_lens int32 [B] counting the new tokens'
     own keys -> (out [B,Hq,Lq,D], lse [B,Hq,Lq])."""
     _need(q, "q", torch.bfloat16, 4)
@@ -327,11 +366,12 @@ def attn_decode_multi(q, kcache, vcache, kv_lens, out=None, lse=None, scale=None
     p.scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
     p.out_dtype = ATTN_DTYPE_F32 if out_dtype == torch.float32 else ATTN_DTYPE_BF16
     p.stream = _stream_handle(stream, q.device)
+    _set_rope(p, rope, D, q.device)
     _check(load().attn_decode_multi(ctypes.byref(p)), "attn_decode_multi")
     return out, lse
 
 
-def attn_decode_noalloc(q, kcache, vcache, kv_lens, out, lse=None, scale=None, chunk=0, stream=None):
+def attn_decode_noalloc(q, kcache, vcache, kv_lens, out, lse=None, scale=None, chunk=0, stream=None, rope=None):
     """Decode through the entry point that allocates no device memory.
 
     For callers that cannot allocate (inside CUDA graph capture, engines that
@@ -364,6 +404,7 @@ def attn_decode_noalloc(q, kcache, vcache, kv_lens, out, lse=None, scale=None, c
     p.out_dtype = ATTN_DTYPE_F32 if out.dtype == torch.float32 else ATTN_DTYPE_BF16
     p.chunk = int(chunk)
     p.stream = _stream_handle(stream, q.device)
+    _set_rope(p, rope, D, q.device)
     _check(load().attn_decode_noalloc(ctypes.byref(p)), "attn_decode_noalloc")
     return out, lse
 

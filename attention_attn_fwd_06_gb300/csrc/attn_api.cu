@@ -183,6 +183,28 @@ int validate_fwd(const attn_fwd_params* p) {
   return ATTN_OK;
 }
 
+// Checks a rotary-embedding argument whose largest position is max_needed - 1 (0: nothing rotated).
+int validate_rope(const attn_rope& r, int D, long long max_needed) {
+  if (r.style == ATTN_ROPE_NONE || r.cos == nullptr) return ATTN_OK;
+  if (r.style != ATTN_ROPE_HALF && r.style != ATTN_ROPE_INTERLEAVED) return ATTN_ERR_INVALID_ARG;
+  if (r.sin == nullptr || r.max_pos <= 0) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(r.cos) || !aligned16(r.sin)) return ATTN_ERR_ALIGNMENT;
+  if (max_needed > r.max_pos) return ATTN_ERR_INVALID_ARG;
+  if ((long long)r.max_pos * (D / 2) > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+  return ATTN_OK;
+}
+
+attn::RopeArgs rope_args(const attn_rope& r) {
+  attn::RopeArgs a{};
+  if (r.style != ATTN_ROPE_NONE && r.cos != nullptr) {
+    a.cos = r.cos;
+    a.sin = r.sin;
+    a.max_pos = r.max_pos;
+    a.style = r.style;
+  }
+  return a;
+}
+
 bool is_empty_fwd(const attn_fwd_params* p) {
   const bool varlen = p->cu_seqlens_q != nullptr;
   return p->B == 0 || p->Lq == 0 || (varlen && p->total_q == 0);
@@ -228,6 +250,8 @@ unsigned long long attn_decode_workspace_bytes(int B, int Hq, int Hkv, int Lmax,
 int attn_decode_ex(const attn_decode_params* p) {
   int st = validate_decode(p);
   if (st != ATTN_OK) return st;
+  st = validate_rope(p->rope, p->D, p->Lmax);
+  if (st != ATTN_OK) return st;
   if (p->B == 0) return ATTN_OK;
   cudaStream_t stream = static_cast<cudaStream_t>(p->stream);
   std::lock_guard<std::mutex> lock(g_mu);
@@ -257,12 +281,15 @@ int attn_decode_ex(const attn_decode_params* p) {
   L.scale = p->scale;
   L.out_f32 = p->out_dtype == ATTN_DTYPE_F32;
   L.status = s->status;
+  L.rope = rope_args(p->rope);
   L.stream = stream;
   return map_cuda(attn::launch_decode(L, s->num_sms));
 }
 
 int attn_decode_noalloc(const attn_decode_params* p) {
   int st = validate_decode(p);
+  if (st != ATTN_OK) return st;
+  st = validate_rope(p->rope, p->D, p->Lmax);
   if (st != ATTN_OK) return st;
   if (p->B == 0) return ATTN_OK;
   std::lock_guard<std::mutex> lock(g_mu);
@@ -310,6 +337,7 @@ int attn_decode_noalloc(const attn_decode_params* p) {
   L.scale = p->scale;
   L.out_f32 = p->out_dtype == ATTN_DTYPE_F32;
   L.status = s->status;
+  L.rope = rope_args(p->rope);
   L.stream = static_cast<cudaStream_t>(p->stream);
   return map_cuda(attn::launch_decode(L, s->num_sms));
 }
@@ -337,7 +365,10 @@ int attn_decode_paged(const attn_decode_paged_params* pp) {
   p.out_dtype = pp->out_dtype;
   p.chunk = pp->chunk;
   p.stream = pp->stream;
+  p.rope = pp->rope;
   int st = validate_decode(&p);
+  if (st != ATTN_OK) return st;
+  st = validate_rope(p.rope, p.D, p.Lmax);
   if (st != ATTN_OK) return st;
   if (p.B == 0) return ATTN_OK;
   if (pp->block_table == nullptr) return ATTN_ERR_INVALID_ARG;
@@ -374,6 +405,7 @@ int attn_decode_paged(const attn_decode_paged_params* pp) {
   L.scale = p.scale;
   L.out_f32 = p.out_dtype == ATTN_DTYPE_F32;
   L.status = s->status;
+  L.rope = rope_args(p.rope);
   L.stream = stream;
   return map_cuda(attn::launch_decode(L, s->num_sms));
 }
@@ -398,6 +430,8 @@ int attn_decode_multi(const attn_decode_multi_params* p) {
   d.out_dtype = p->out_dtype;
   d.stream = p->stream;
   int st = validate_decode(&d);
+  if (st != ATTN_OK) return st;
+  st = validate_rope(p->rope, p->D, p->Lmax);
   if (st != ATTN_OK) return st;
   if (p->B == 0) return ATTN_OK;
   const long long rows = (long long)(p->Hq / p->Hkv) * p->Lq;
@@ -434,6 +468,7 @@ int attn_decode_multi(const attn_decode_multi_params* p) {
   L.out_f32 = p->out_dtype == ATTN_DTYPE_F32;
   L.num_sms = s->num_sms;
   L.status = s->status;
+  L.rope = rope_args(p->rope);
   L.stream = stream;
   return map_cuda(attn::launch_decode_multi(L));
 }
@@ -462,6 +497,11 @@ int attn_decode(const void* q, const void* kcache, const void* vcache, const int
 int attn_fwd_ex(const attn_fwd_params* p) {
   int st = validate_fwd(p);
   if (st != ATTN_OK) return st;
+  // positions reach Lkv - 1 (keys and the last query); a dense call with Lq > Lkv would place queries before 0
+  st = validate_rope(p->rope, p->D, p->Lkv);
+  if (st != ATTN_OK) return st;
+  const bool rope_on = p->rope.style != ATTN_ROPE_NONE && p->rope.cos != nullptr;
+  if (rope_on && p->cu_seqlens_q == nullptr && p->Lq > p->Lkv) return ATTN_ERR_INVALID_ARG;
   if (is_empty_fwd(p)) return ATTN_OK;
   cudaStream_t stream = static_cast<cudaStream_t>(p->stream);
   DeviceState* s = nullptr;
@@ -491,6 +531,7 @@ int attn_fwd_ex(const attn_fwd_params* p) {
   L.total_k = p->total_k;
   L.num_sms = s->num_sms;
   L.status = s->status;
+  L.rope = rope_args(p->rope);
   L.stream = stream;
   return map_cuda(attn::launch_prefill(L));
 }

@@ -68,15 +68,17 @@ struct DecodeCfg {
   static constexpr int MINB = (GP >= 8) ? 2 : 3;             // resident CTAs per SM (register budget)
   static constexpr int NS = (MINB == 3) ? 2 : 3;              // ring stages
   static constexpr int THREADS = 32 * (NW + 1);
-  static constexpr int LENS_CACHE = (GP >= 8) ? 128 : 512;   // kv_lens kept in shared memory for the walk
+  static constexpr int LENS_CACHE = (GP >= 8) ? 64 : 512;    // kv_lens kept in shared memory for the walk
   static constexpr int TILE_ELEMS = SK * D;
   static constexpr int TILE_BYTES = TILE_ELEMS * 2;
   static constexpr int Q_BYTES = GP * D * 2;                  // q of the group's heads (bf16)
   // shared-memory layout (bytes)
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + NS * TILE_BYTES;
+  static constexpr int ROPE_BYTES = 4 * D;                     // cos and sin rows (D/2 fp32 each) of the q position
   static constexpr int OFF_Q = OFF_V + NS * TILE_BYTES;
-  static constexpr int OFF_O = OFF_Q + NS * Q_BYTES;          // obuf[2][GP][D] fp32 (merge; also combine weights)
+  static constexpr int OFF_R = OFF_Q + NS * Q_BYTES;          // rope rows per stage
+  static constexpr int OFF_O = OFF_R + NS * ROPE_BYTES;       // obuf[2][GP][D] fp32 (merge; also combine weights)
   static constexpr int OFF_BAR = OFF_O + 2 * GP * D * 4;      // full[NS], empty[NS]
   static constexpr int OFF_INFO = OFF_BAR + 2 * NS * 8;       // StageInfo[NS]
   static constexpr int OFF_P = OFF_INFO + NS * 32;            // pbuf[NW][32]
@@ -118,6 +120,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS, DecodeCfg<D, GP>::M
   __nv_bfloat16* Ks = reinterpret_cast<__nv_bfloat16*>(smem + C::OFF_K);
   __nv_bfloat16* Vs = reinterpret_cast<__nv_bfloat16*>(smem + C::OFF_V);
   uint8_t* Qs = smem + C::OFF_Q;
+  float* Rs = reinterpret_cast<float*>(smem + C::OFF_R);
   float* obuf = reinterpret_cast<float*>(smem + C::OFF_O);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* empty = full + C::NS;
@@ -134,6 +137,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS, DecodeCfg<D, GP>::M
   const int lane = threadIdx.x & 31;
   const int Hg = p.Hkv * ngroups;  // rows per sequence
   const int cta = blockIdx.x;
+  const bool rope_on = p.rope.style != 0;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::NS; ++s) {
@@ -143,6 +147,8 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS, DecodeCfg<D, GP>::M
     *abort_flag = 0;
     fence_mbar_init();
   }
+  // The producer's first kv_lens load is issued before the barrier, so its latency overlaps the set-up.
+  const int len_first = (warp == C::NW && lane < p.B) ? p.kv_lens[lane] : 0;
   for (int i = threadIdx.x; i < 2 * GP * D; i += blockDim.x) obuf[i] = 0.f;
   __syncthreads();
 
@@ -150,22 +156,29 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS, DecodeCfg<D, GP>::M
     // ---------------- producer: walk this CTA's slice of the key space ----------------
     // Total keys W = Hg * sum_b len_b (the whole warp sums the lengths).
     long long wsum = 0;
+    int nonempty = 0;  // sequences with keys
     for (int b = lane; b < p.B; b += 32) {
-      const int raw = p.kv_lens[b];
+      const int raw = (b == lane) ? len_first : p.kv_lens[b];
       const int len = clamp_len(raw, p.Lmax);
       if (raw != len && cta == 0) record_status(p.status, ATTN_ERR_DEVICE_BOUNDS);
       if (b < C::LENS_CACHE) lens_s[b] = len;
       wsum += len;
+      nonempty += len > 0 ? 1 : 0;
     }
 #pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, off);
+    for (int off = 16; off >= 1; off >>= 1) {
+      wsum += __shfl_xor_sync(0xffffffffu, wsum, off);
+      nonempty += __shfl_xor_sync(0xffffffffu, nonempty, off);
+    }
     __syncwarp();
     // The whole producer warp walks the slice in lock-step (lane 0 issues copies and barrier operations;
     // the other lanes fetch page-table windows for the paged layout).
     auto seq_len = [&](int b) -> int { return b < C::LENS_CACHE ? lens_s[b] : clamp_len(p.kv_lens[b], p.Lmax); };
     const long long W = wsum * Hg;
-    // At least min_keys keys per CTA; CTAs past the effective grid only handle empty sequences.
+    // Slices of at least min_keys keys, but never fewer slices than rows with keys (a CTA per row of a short
+    // problem rather than one CTA walking many rows); CTAs past the effective grid only handle empty sequences.
     long long geff = (W + p.min_keys - 1) / p.min_keys;
+    if (geff < (long long)nonempty * Hg) geff = (long long)nonempty * Hg;
     if (geff > (long long)gridDim.x) geff = gridDim.x;
     if (geff < 1) geff = 1;
     const long long per = (W + geff - 1) / geff;
@@ -249,8 +262,17 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS, DecodeCfg<D, GP>::M
           si.cta_lo = cta_lo;
           si.lo_odd = lo_odd;
           info[slot_r] = si;
-          mbar_arrive_expect_tx(&full[slot_r], 2u * (uint32_t)nk * D * 2 + (u == 0 ? (uint32_t)C::Q_BYTES : 0u));
+          // the first stage of a piece carries q, and with RoPE the table rows of its position (kv_len - 1)
+          const bool rope_rows = (u == 0) && rope_on && nkeys > 0;
+          mbar_arrive_expect_tx(&full[slot_r], 2u * (uint32_t)nk * D * 2 + (u == 0 ? (uint32_t)C::Q_BYTES : 0u) +
+                                                   (rope_rows ? (uint32_t)C::ROPE_BYTES : 0u));
           if (u == 0) bulk_g2s(Qs + slot_r * C::Q_BYTES, qg, C::Q_BYTES, &full[slot_r]);
+          if (rope_rows) {
+            const size_t pos = (size_t)(seq_len(b) - 1);
+            float* rdst = Rs + slot_r * (C::ROPE_BYTES / 4);
+            bulk_g2s(rdst, p.rope.cos + pos * (D / 2), D * 2, &full[slot_r]);
+            bulk_g2s(rdst + D / 2, p.rope.sin + pos * (D / 2), D * 2, &full[slot_r]);
+          }
         }
         if (nk > 0)
           copy_keys(b, hkv, kb + u * C::SK, nk, Ks + slot_r * C::TILE_ELEMS, Vs + slot_r * C::TILE_ELEMS, &full[slot_r]);
@@ -293,10 +315,12 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS, DecodeCfg<D, GP>::M
         }
       }
     }
-    // Sequences with no keys: O = 0, lse = -inf, spread over the CTAs.
-    for (int b = cta; ok && b < p.B; b += gridDim.x) {
-      if (seq_len(b) != 0) continue;
-      for (int hg = 0; ok && hg < Hg; ++hg) ok = emit(b, hg, 0, 0, 0, 0, 0, 0);
+    // Rows of sequences with no keys: O = 0, lse = -inf, one row per CTA in turn.
+    if (nonempty < p.B) {
+      for (long long e = cta; ok && e < (long long)p.B * Hg; e += gridDim.x) {
+        const int b = (int)(e / Hg);
+        if (seq_len(b) == 0) ok = emit(b, (int)(e - (long long)b * Hg), 0, 0, 0, 0, 0, 0);
+      }
     }
     if (ok) {
       // end-of-work marker
@@ -339,15 +363,48 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS, DecodeCfg<D, GP>::M
     const __nv_bfloat16* Vt = Vs + slot * C::TILE_ELEMS;
     if (si.flags & 1) {
       const __nv_bfloat16* qsm = reinterpret_cast<const __nv_bfloat16*>(Qs + slot * C::Q_BYTES);
+      const float* rc = Rs + slot * (C::ROPE_BYTES / 4);  // cos row of the q position; sin row at + D/2
 #pragma unroll
       for (int g = 0; g < GP; ++g) {
-        const uint4 raw = lds128(qsm + g * D + 8 * sub);
-        const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+        float qv[8];
+        {
+          const uint4 raw = lds128(qsm + g * D + 8 * sub);
+          const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) bf16x2_to_f32(w4[j], qv[2 * j], qv[2 * j + 1]);
+        }
+        if (rope_on && si.nk > 0) {
+          // rotate this lane's 8 dims of q to position kv_len - 1 (pair (a, b) -> (a c - b s, b c + a s)), in fp32
+          if (p.rope.style == 1) {
+            // pairs (i, i + D/2): the partner dims sit in the other half of the row
+            const int d0 = 8 * sub;
+            const bool low = d0 < D / 2;
+            const int i0 = low ? d0 : d0 - D / 2;
+            float pv[8];
+            const uint4 raw = lds128(qsm + g * D + (low ? d0 + D / 2 : d0 - D / 2));
+            const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) bf16x2_to_f32(w4[j], pv[2 * j], pv[2 * j + 1]);
+            const float sg = low ? -1.f : 1.f;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) qv[j] = fmaf(qv[j], rc[i0 + j], sg * pv[j] * rc[D / 2 + i0 + j]);
+          } else {
+            // pairs (2i, 2i + 1): this lane holds pairs 4 sub .. 4 sub + 3 whole
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const float c = rc[4 * sub + k], sn = rc[D / 2 + 4 * sub + k];
+              const float a = qv[2 * k], b2 = qv[2 * k + 1];
+              qv[2 * k] = fmaf(a, c, -b2 * sn);
+              qv[2 * k + 1] = fmaf(b2, c, a * sn);
+            }
+          }
+          // the rotated q is held in bf16, like the tensor the unfused RoPE op would hand to attention
+#pragma unroll
+          for (int j = 0; j < 8; ++j) qv[j] = __bfloat162float(__float2bfloat16_rn(qv[j]));
+        }
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          float lo, hi;
-          bf16x2_to_f32(w4[j], lo, hi);
-          qf[g][j] = make_float2(lo * qscale, hi * qscale);
+          qf[g][j] = make_float2(qv[2 * j] * qscale, qv[2 * j + 1] * qscale);
           o[g][j] = make_float2(0.f, 0.f);
         }
       }
@@ -527,10 +584,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS, DecodeCfg<D, GP>::M
       } else {
         const size_t prow = (size_t)si.slot * GP + g;
         p.part_o[prow * D + d] = O;
-        if (d == 0) {
-          p.part_ml[prow * 2] = M;
-          p.part_ml[prow * 2 + 1] = L;
-        }
+        if (d == 0) reinterpret_cast<float2*>(p.part_ml)[prow] = make_float2(M, L);
       }
     }
     if (si.np > 1) {
@@ -548,75 +602,61 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS, DecodeCfg<D, GP>::M
       }
       named_bar_sync(1, nct);
       if (*last_flag) {
-        // Merge the row's partials.  Partial slots of the row: CTA c holds slot 2c (+1 for the first CTA when the
-        // row starts inside its slice).  Per round of up to D partials: stage their maxima in shared memory
-        // (obuf is free here), one thread per head turns them into weights 2^(m - M) and the running sum, then
-        // every thread sums its O entries with all of a round's loads in flight.
-        constexpr int KP = (GP * D + C::NW * 32 - 1) / (C::NW * 32);
-        float* wgt = obuf;               // [D][GP] weights of the round
-        float* msum_s = obuf + GP * D;   // [GP] running max
-        float* lsum_s = msum_s + GP;     // [GP] running sum
-        float* rsc_s = lsum_s + GP;      // [GP] rescale of earlier rounds
-        float acc[KP];
-#pragma unroll
-        for (int k = 0; k < KP; ++k) acc[k] = 0.f;
-        const int npart = si.np;
-        for (int i0 = 0; i0 < npart; i0 += D) {
-          const int chunk = min(npart - i0, D);
-          for (int e = ctid; e < chunk * GP; e += nct) {
-            const int i = i0 + e / GP, g = e % GP;
-            const int sl = 2 * (si.cta_lo + i) + (i == 0 ? si.lo_odd : 0);
-            wgt[e] = __ldcg(p.part_ml + ((size_t)sl * GP + g) * 2);
-          }
-          named_bar_sync(1, nct);
-          if (ctid < GP) {
-            const int g = ctid;
-            const float Mold = (i0 == 0) ? -INFINITY : msum_s[g];
-            float M = Mold;
-            for (int i = 0; i < chunk; ++i) M = fmaxf(M, wgt[i * GP + g]);
-            const float rsc = (i0 == 0) ? 0.f : ex2_approx(Mold - M);
-            float L = (i0 == 0) ? 0.f : lsum_s[g] * rsc;
-            for (int i = 0; i < chunk; ++i) {
-              const int ii = i0 + i;
-              const int sl = 2 * (si.cta_lo + ii) + (ii == 0 ? si.lo_odd : 0);
-              const float w = ex2_approx(wgt[i * GP + g] - M);
-              wgt[i * GP + g] = w;
-              L = fmaf(w, __ldcg(p.part_ml + ((size_t)sl * GP + g) * 2 + 1), L);
+        // Merge the row's partials: each thread takes a run of 4 columns of one head and folds every partial of
+        // the row into it in slot order with a running max (a fixed order: bitwise reproducible), the loads of
+        // four partials in flight at a time.  Partial slots of the row: CTA c holds slot 2c (+1 for the first
+        // CTA when the row starts inside its slice).
+        constexpr int RUNS = GP * D / 4;
+        const float2* ml_base = reinterpret_cast<const float2*>(p.part_ml);
+        for (int e = ctid; e < RUNS; e += nct) {
+          const int g = (e * 4) / D;
+          const int d = e * 4 - g * D;
+          float M = -INFINITY, L = 0.f;
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+          auto fold = [&](float2 ml, float4 o) {
+            if (ml.x > M) {  // new running max: rescale what was folded so far (nothing while M is -inf)
+              const float sc = (M == -INFINITY) ? 0.f : ex2_approx(M - ml.x);
+              acc = make_float4(acc.x * sc, acc.y * sc, acc.z * sc, acc.w * sc);
+              L *= sc;
+              M = ml.x;
             }
-            msum_s[g] = M;
-            lsum_s[g] = L;
-            rsc_s[g] = rsc;
-          }
-          named_bar_sync(1, nct);
+            const float w = (ml.x == -INFINITY) ? 0.f : ex2_approx(ml.x - M);
+            acc = make_float4(fmaf(w, o.x, acc.x), fmaf(w, o.y, acc.y), fmaf(w, o.z, acc.z), fmaf(w, o.w, acc.w));
+            L = fmaf(w, ml.y, L);
+          };
+          auto slot_of = [&](int i) { return 2 * (si.cta_lo + i) + (i == 0 ? si.lo_odd : 0); };
+          int i = 0;
+          for (; i + 3 < si.np; i += 4) {
+            float2 ml[4];
+            float4 o[4];
 #pragma unroll
-          for (int k = 0; k < KP; ++k) {
-            const int idx = ctid + k * nct;
-            if (idx >= GP * D) continue;
-            const int g = idx / D;
-            const int d = idx - g * D;
-            float a = acc[k] * rsc_s[g];
-#pragma unroll 8
-            for (int i = 0; i < chunk; ++i) {
-              const int ii = i0 + i;
-              const int sl = 2 * (si.cta_lo + ii) + (ii == 0 ? si.lo_odd : 0);
-              a = fmaf(wgt[i * GP + g], __ldcg(p.part_o + ((size_t)sl * GP + g) * D + d), a);
+            for (int u = 0; u < 4; ++u) {
+              const size_t prow = (size_t)slot_of(i + u) * GP + g;
+              ml[u] = __ldcg(ml_base + prow);
+              o[u] = __ldcg(reinterpret_cast<const float4*>(p.part_o + prow * D + d));
             }
-            acc[k] = a;
-          }
-          named_bar_sync(1, nct);  // the next round overwrites wgt
-        }
 #pragma unroll
-        for (int k = 0; k < KP; ++k) {
-          const int idx = ctid + k * nct;
-          if (idx >= GP * D) continue;
-          const int g = idx / D;
-          const int d = idx - g * D;
+            for (int u = 0; u < 4; ++u) fold(ml[u], o[u]);
+          }
+          for (; i < si.np; ++i) {
+            const size_t prow = (size_t)slot_of(i) * GP + g;
+            fold(__ldcg(ml_base + prow), __ldcg(reinterpret_cast<const float4*>(p.part_o + prow * D + d)));
+          }
+          const float inv = 1.f / L;  // L > 0: the row has keys
           const size_t bh = (size_t)si.b * p.Hq + hq0 + g;
-          store_out<float>(p.out, bh * D + d, acc[k] / lsum_s[g], p.out_f32);
-          if (d == 0 && p.lse != nullptr) p.lse[bh] = (msum_s[g] + log2f(lsum_s[g])) * kLn2;
+          if (p.out_f32) {
+            *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + bh * D + d) =
+                make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+          } else {
+            __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+            __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+            uint2 w2;
+            w2.x = *reinterpret_cast<uint32_t*>(&lo);
+            w2.y = *reinterpret_cast<uint32_t*>(&hi);
+            *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.out) + bh * D + d) = w2;
+          }
+          if (d == 0 && p.lse != nullptr) p.lse[bh] = (M + log2f(L)) * kLn2;
         }
-        named_bar_sync(1, nct);
-        for (int e = ctid; e < 2 * GP * D; e += nct) obuf[e] = 0.f;
       }
     }
     named_bar_sync(1, nct);  // mbuf/lbuf/obuf/last_flag are reused by the next piece

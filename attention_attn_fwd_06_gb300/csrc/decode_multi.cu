@@ -43,6 +43,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "rope.cuh"
 #include "tcgen05.cuh"
 #include "tmap.h"
 
@@ -72,8 +73,8 @@ struct MCfg {
   static constexpr int OFF_V = OFF_K + NS * TILE_BYTES;
   static constexpr int OFF_BAR = OFF_V + NS * TILE_BYTES;
   // barriers: q_full, q_empty, k_full[NS], v_full[NS], k_empty[NS], v_empty[NS], s_full[2], p_full[2],
-  // o_done[2], drain
-  static constexpr int NBAR = 2 + 4 * NS + 2 + 2 + 2 + 1;
+  // o_done[2], drain, q_ready
+  static constexpr int NBAR = 2 + 4 * NS + 2 + 2 + 2 + 1 + 1;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // tmem address, abort flag, last-partial flag
   static constexpr int SMEM_USED = OFF_MISC + 16;
   static constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // slack to align the base to 1024
@@ -100,6 +101,7 @@ struct MultiArgs {
   float scale_log2;    // scale * log2(e)
   int out_f32;
   unsigned* status;
+  RopeArgs rope;       // style != 0: the softmax threads rotate the Q tile's rows before the S MMAs
 };
 
 __device__ __forceinline__ int clamp_len(int len, int Lmax) { return len < 0 ? 0 : (len > Lmax ? Lmax : len); }
@@ -257,6 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* p_full = s_full + 2;        // [2] per S buffer (128 arrivals)
   uint64_t* o_done = p_full + 2;        // [2] P V of even / odd tiles completed
   uint64_t* drain = o_done + 2;
+  uint64_t* q_ready = drain + 1;        // with RoPE: the piece's Q rows are rotated (128 arrivals)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   volatile int* last_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
@@ -266,8 +269,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::NBAR; ++i) {
-      const bool is_p = (&bars[i] >= p_full) && (&bars[i] < p_full + 2);
-      mbar_init(&bars[i], is_p ? kSoftmaxThreads : 1);
+      const bool many = ((&bars[i] >= p_full) && (&bars[i] < p_full + 2)) || &bars[i] == q_ready;
+      mbar_init(&bars[i], many ? kSoftmaxThreads : 1);
     }
     *abort_flag = 0;
     *last_flag = 0;
@@ -397,7 +400,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       while (ok && walk_next(walk, a, pc)) {
         const int nt = pc.t1 - pc.t0;
-        if (!mbar_wait(q_full, qj & 1, a.status, abort_flag)) {
+        // the piece's Q: landed, and with RoPE rotated by the softmax threads
+        if (!mbar_wait(a.rope.style != 0 ? q_ready : q_full, qj & 1, a.status, abort_flag)) {
           ok = false;
           break;
         }
@@ -458,6 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float c = a.scale_log2;
     const int t_row = row % a.Lq;  // which new token this row is (padding rows: meaningless)
     int g = 0;
+    int sp = 0;  // pieces seen (q_full / q_ready phases)
     bool ok = true;
 
     // After a failed wait the softmax threads keep walking their pieces without touching TMEM or waiting, so
@@ -467,6 +472,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int horizon = pc.n - a.Lq + t_row;  // last key this row sees
       float m_ref = -INFINITY;                  // running max, scaled log2 units
       float l = 0.f;
+      if (a.rope.style != 0) {
+        // Rotate this thread's query row to its position n - Lq + t (rows that see no key stay as they are),
+        // then hand the tile to the MMA warp.
+        if (ok) ok = mbar_wait(q_full, sp & 1, a.status, abort_flag);
+        if (ok && row < a.R && horizon >= 0) {
+          const size_t off = (size_t)horizon * (D / 2);
+          rope_rotate_row_sw128<D>(Qs, C::BLOCK_BYTES, row, a.rope.cos + off, a.rope.sin + off, a.rope.style);
+        }
+        fence_proxy_async_smem();  // the rotated rows are read by the tensor cores (async proxy)
+        mbar_arrive(q_ready);
+      }
+      ++sp;
       for (int i = 0; ok && i < nt; ++i) {
         const int gi = g + i;
         const int buf = gi & 1;
@@ -769,6 +786,7 @@ cudaError_t launch_d(const DecodeMultiLaunch& p) {
   a.scale_log2 = p.scale * kLog2e;
   a.out_f32 = p.out_f32;
   a.status = p.status;
+  a.rope = p.rope;
   decode_multi_kernel<D><<<decode_multi_grid(p.num_sms), kThreads, C::SMEM_ALLOC, p.stream>>>(tmq, tmk, tmv, a);
   return cudaGetLastError();
 }

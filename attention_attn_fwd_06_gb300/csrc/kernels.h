@@ -6,6 +6,14 @@
 
 namespace attn {
 
+// Rotary position embedding tables (see attn_rope in include/attn.h); style 0 = off.
+struct RopeArgs {
+  const float* cos;  // fp32 [max_pos, D/2]
+  const float* sin;
+  int max_pos;
+  int style;         // 1: pairs (i, i + D/2); 2: pairs (2i, 2i + 1)
+};
+
 // Split-KV decode (the split pass writes fp32 partials, the combine merges them).
 struct DecodeLaunch {
   const void* q;        // bf16 [B, Hq, D]
@@ -24,6 +32,7 @@ struct DecodeLaunch {
   float scale;
   int out_f32;
   unsigned* status;     // device status word
+  RopeArgs rope;        // rotates q (to kv_len - 1) when style != 0
   cudaStream_t stream;
 };
 
@@ -55,6 +64,7 @@ struct DecodeMultiLaunch {
   int out_f32;
   int num_sms;
   unsigned* status;
+  RopeArgs rope;        // rotates q (token t to kv_len - Lq + t) when style != 0
   cudaStream_t stream;
 };
 
@@ -78,6 +88,7 @@ struct PrefillLaunch {
   int total_q, total_k;
   int num_sms;      // persistent grid size
   unsigned* status;
+  RopeArgs rope;    // rotates q (query i to Lkv - Lq + i) and k (key j to j) when style != 0
   cudaStream_t stream;
 };
 

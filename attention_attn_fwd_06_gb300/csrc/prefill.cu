@@ -34,6 +34,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "rope.cuh"
 #include "tcgen05.cuh"
 #include "tmap.h"
 
@@ -43,10 +44,11 @@ namespace {
 constexpr int BM = 128;  // query rows per tile (TMEM lanes)
 constexpr int BN = 128;  // keys per K/V tile
 constexpr int NQ = 2;    // query tiles per CTA (ping-pong)
-constexpr int kThreads = 32 * (2 + 4 * NQ);  // TMA warp, MMA warp, one 4-warp softmax group per query tile
+constexpr int kThreads = 32 * (3 + 4 * NQ);  // TMA warp, MMA warp, a 4-warp softmax group per query tile, RoPE warp
 constexpr int kWarpTMA = 0;
 constexpr int kWarpMMA = 1;
 constexpr int kFirstSoftmaxWarp = 2;
+constexpr int kWarpRope = 2 + 4 * NQ;  // rotates each K tile when RoPE is on (idle otherwise)
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -63,8 +65,8 @@ struct Cfg {
   static constexpr int OFF_V = OFF_K + NS * TILE_BYTES;
   static constexpr int OFF_BAR = OFF_V + NS * TILE_BYTES;
   // barriers: q_full, q_empty, k_full[NS], v_full[NS], k_empty[NS], v_empty[NS], s_full[NQ], p_full[NQ],
-  // o_done[NQ], drain
-  static constexpr int NBAR = 2 + 4 * NS + 3 * NQ + 1;
+  // o_done[NQ], drain, q_ready, k_ready[NS]
+  static constexpr int NBAR = 2 + 4 * NS + 3 * NQ + 1 + 1 + NS;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // tmem address, abort flag
   static constexpr int SMEM_USED = OFF_MISC + 16;
   static constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // slack to align the base to 1024
@@ -92,6 +94,7 @@ struct PrefillArgs {
   int total_items;   // B * Hq * ns
   int total_q, total_k;  // packed layout: rows of q/out and of k/v
   unsigned* status;
+  RopeArgs rope;         // style != 0: q rows rotated by the softmax groups, K tiles by the RoPE warp
 };
 
 // One job = one pair of 128-row query tiles of one (sequence, head).
@@ -183,16 +186,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* p_full = s_full + NQ;
   uint64_t* o_done = p_full + NQ;
   uint64_t* drain = o_done + NQ;
+  uint64_t* q_ready = drain + 1;    // with RoPE: both Q tiles of the job rotated (one arrival per softmax thread)
+  uint64_t* k_ready = q_ready + 1;  // with RoPE: [NS] the K slot's rows rotated
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const bool rope = a.rope.style != 0;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::NBAR; ++i) {
       const bool is_p = (&bars[i] >= p_full) && (&bars[i] < p_full + NQ);
-      mbar_init(&bars[i], is_p ? 128 : 1);
+      mbar_init(&bars[i], is_p ? 128 : (&bars[i] == q_ready ? 128 * NQ : 1));
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -305,8 +311,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           Job jb;
           if (!make_job(a, item, half, jb) || jb.n == 0) continue;
           const int g0 = kv;
-          if (!mbar_wait(q_full, qjobs & 1, a.status, abort_flag) ||
-              !mbar_wait(&k_full[g0 % C::NS], (g0 / C::NS) & 1, a.status, abort_flag)) {
+          // with RoPE, wait for the rotated Q tiles and K slots instead of the raw ones
+          if (!mbar_wait(rope ? q_ready : q_full, qjobs & 1, a.status, abort_flag) ||
+              !mbar_wait(rope ? &k_ready[g0 % C::NS] : &k_full[g0 % C::NS], (g0 / C::NS) & 1, a.status,
+                         abort_flag)) {
             ok = false;
             break;
           }
@@ -339,7 +347,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               tc::fence_after_sync();
               issue_pv(t, g, j == 0);
               if (j + 1 < jb.nt[t]) {
-                if (!mbar_wait(&k_full[(g + 1) % C::NS], ((g + 1) / C::NS) & 1, a.status, abort_flag)) {
+                if (!mbar_wait(rope ? &k_ready[(g + 1) % C::NS] : &k_full[(g + 1) % C::NS], ((g + 1) / C::NS) & 1,
+                               a.status, abort_flag)) {
                   ok = false;
                   break;
                 }
@@ -361,6 +370,39 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::mma_commit(drain);
       mbar_wait(drain, 0, a.status, nullptr);
     }
+  } else if (warp == kWarpRope) {
+    // ---------------- RoPE: rotate every K tile once it lands (key j of a sequence sits at position j) --------
+    if (rope) {
+      int kv = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; ok && item < a.total_items; item += gridDim.x) {
+        for (int half = 0; ok && half < 2; ++half) {
+          Job jb;
+          if (!make_job(a, item, half, jb) || jb.n == 0) continue;
+          for (int j = 0; j < jb.n; ++j) {
+            const int g = kv + j;
+            const int slot = g % C::NS;
+            if (!mbar_wait(&k_full[slot], (g / C::NS) & 1, a.status, abort_flag)) {
+              ok = false;
+              break;
+            }
+            uint8_t* tile = Ks + slot * C::TILE_BYTES;
+#pragma unroll 1
+            for (int r = lane; r < BN; r += 32) {
+              const int key = j * BN + r;
+              if (key < jb.Lkv_s) {  // rows past the sequence are masked out anyway
+                const size_t off = (size_t)key * (D / 2);
+                rope_rotate_row_sw128<D>(tile, C::BLOCK_BYTES, r, a.rope.cos + off, a.rope.sin + off, a.rope.style);
+              }
+            }
+            fence_proxy_async_smem();  // the rotated rows are read by the tensor cores (async proxy)
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&k_ready[slot]);
+          }
+          kv += jb.n;
+        }
+      }
+    }
   } else {
     // ---------------- softmax + correction + epilogue: one thread per query row ----------------
     const int t = (warp - kFirstSoftmaxWarp) >> 2;  // which query tile of each job this group owns
@@ -371,6 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t s_addr = tbase + lane_addr + C::tm_s(t);
     const uint32_t o_addr = tbase + lane_addr + C::tm_o(t);
     int ss = 0;  // S steps of this tile consumed so far (s_full / o_done phases)
+    int qj = 0;  // jobs with work seen (q_full / q_ready phases)
     bool ok = true;
 
     for (int item = blockIdx.x; ok && item < a.total_items; item += gridDim.x) {
@@ -378,6 +421,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         Job jb;
         if (!make_job(a, item, half, jb)) continue;
         const int q0 = jb.q00 + t * BM;
+        if (rope && jb.n > 0) {
+          // Rotate this thread's query row of tile t to position qi + (Lkv - Lq), then hand the tiles to the
+          // MMA warp (every softmax thread arrives, also for a tile past the sequence end).
+          if (!mbar_wait(q_full, qj & 1, a.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const int qi_r = q0 + row;
+          if (jb.nt[t] > 0 && qi_r < jb.Lq_s) {
+            const int pos = qi_r + jb.off;
+            if (pos < 0) {
+              record_status(a.status, ATTN_ERR_DEVICE_BOUNDS);  // a packed sequence with more queries than keys
+            } else {
+              const size_t off = (size_t)pos * (D / 2);
+              rope_rotate_row_sw128<D>(Qs + t * C::TILE_BYTES, C::BLOCK_BYTES, row, a.rope.cos + off,
+                                       a.rope.sin + off, a.rope.style);
+            }
+          }
+          fence_proxy_async_smem();
+          mbar_arrive(q_ready);
+        }
+        if (jb.n > 0) ++qj;
         if (q0 >= jb.Lq_s) continue;                    // this tile lies past the sequence end
         const int qi = q0 + row;                         // query index within its sequence
         const int horizon = qi + jb.off;                 // last visible key under the causal mask
@@ -597,6 +662,7 @@ cudaError_t launch_d(const PrefillLaunch& p) {
   a.total_q = p.total_q;
   a.total_k = p.total_k;
   a.status = p.status;
+  a.rope = p.rope;
   const long long items = (long long)p.B * p.Hq * a.ns;
   if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
   a.total_items = (int)items;

@@ -60,6 +60,39 @@ typedef enum attn_status {
 typedef enum attn_dtype { ATTN_DTYPE_BF16 = 0, ATTN_DTYPE_F32 = 1 } attn_dtype;
 
 /*
+ * attn_rope -- rotary position embedding (RoPE) applied inside the kernels,
+ * as "Что такое kernel fusion и как он применяется в LLM serving?" §3.5 and
+ * Operator Fusion's exercise 1 (RoPE fused into the attention kernel)
+ * describe; the pages give no formula, so the standard rotary embedding is
+ * used: pair i of a row at position p, (a, b), becomes
+ *     (a * cos[p][i] - b * sin[p][i],  b * cos[p][i] + a * sin[p][i]),
+ * the pairs being dims (i, i + D/2) for ATTN_ROPE_HALF and (2i, 2i + 1) for
+ * ATTN_ROPE_INTERLEAVED.
+ *
+ *   cos, sin  DEVICE fp32 [max_pos, D/2] tables (row p: position p), 16-byte
+ *             aligned; read-only.
+ *   max_pos   rows of both tables.
+ *   style     ATTN_ROPE_NONE (or cos == NULL): no rotation.
+ *
+ * Positions follow the causal alignment.  Prefill: key j of a sequence sits
+ * at j and query i at Lkv - Lq + i; q and k are rotated as they are loaded
+ * (a dense call with Lq > Lkv returns ATTN_ERR_INVALID_ARG; a packed sequence
+ * with more queries than keys is flagged ATTN_ERR_DEVICE_BOUNDS).  Decode:
+ * only the query is rotated, to kv_len - 1 (token t of attn_decode_multi to
+ * kv_len - Lq + t); cached keys must be stored already rotated.  Every
+ * position must be below max_pos: calls whose Lkv (prefill) or Lmax (decode)
+ * exceeds max_pos return ATTN_ERR_INVALID_ARG.
+ */
+typedef enum attn_rope_style { ATTN_ROPE_NONE = 0, ATTN_ROPE_HALF = 1, ATTN_ROPE_INTERLEAVED = 2 } attn_rope_style;
+
+typedef struct attn_rope {
+  const float* cos;
+  const float* sin;
+  int max_pos;
+  int style;
+} attn_rope;
+
+/*
  * attn_fwd -- prefill attention over dense [batch, heads, seq_len, head_dim]
  * tensors (the Q/K/V shape of "Что такое kernel fusion и как он применяется в
  * LLM serving?", §2, and the chain of Operator Fusion §3.4).
@@ -111,6 +144,7 @@ typedef struct attn_fwd_params {
   const int* cu_seqlens_k;
   int total_q, total_k;
   void* stream;
+  attn_rope rope;  /* optional; zero-initialised = no rotation */
 } attn_fwd_params;
 
 int attn_fwd_ex(const attn_fwd_params* p);
@@ -152,7 +186,9 @@ int attn_decode(const void* q, const void* kcache, const void* vcache, const int
  *   chunk         0 = default; otherwise the smallest number of keys one CTA's
  *                 slice of the key space may hold (default 64), in
  *                 [1, 1048576]: smaller values spread short problems over more
- *                 CTAs and split rows into more partials
+ *                 CTAs and split rows into more partials.  The slices never
+ *                 number fewer than the rows that have keys (while CTAs
+ *                 last), so a short problem still runs a row per CTA.
  * Rows: B * Hkv * (Hq / Hkv / g) must stay at or below 65534, g being the
  * number of query heads one CTA serves (the largest of 8, 4, 2, 1 dividing
  * Hq / Hkv); otherwise ATTN_ERR_UNSUPPORTED.
@@ -169,6 +205,7 @@ typedef struct attn_decode_params {
   int out_dtype;
   int chunk;
   void* stream;
+  attn_rope rope;  /* optional; zero-initialised = no rotation */
 } attn_decode_params;
 
 int attn_decode_ex(const attn_decode_params* p);
@@ -207,6 +244,7 @@ typedef struct attn_decode_paged_params {
   int out_dtype;
   int chunk;
   void* stream;
+  attn_rope rope;  /* optional; zero-initialised = no rotation */
 } attn_decode_paged_params;
 
 int attn_decode_paged(const attn_decode_paged_params* p);
@@ -253,6 +291,7 @@ typedef struct attn_decode_multi_params {
   float scale;
   int out_dtype;
   void* stream;
+  attn_rope rope;  /* optional; zero-initialised = no rotation */
 } attn_decode_multi_params;
 
 int attn_decode_multi(const attn_decode_multi_params* p);

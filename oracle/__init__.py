@@ -19,6 +19,7 @@ from .sdpa import (  # noqa: F401
     decode_multi,
     kv_head_of,
     rope_rotate,
+    round_bf16,
     log_sum_exp,
     scores,
     softmax_two_pass,

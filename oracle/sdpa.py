@@ -44,7 +44,11 @@ design notes of the repository):
   dims (i, i + D/2) ("half") or (2i, 2i + 1) ("interleaved").  Queries and
   keys take the positions the causal alignment gives them: key j sits at j,
   query i of Lq at ``Lkv - Lq + i``; a decode token at ``kv_len - Lq + t``.
-  Cached keys are stored already rotated (decode rotates only q).
+  Cached keys are stored already rotated (decode rotates only q).  The
+  rotated q and k are rounded to bf16 (nearest, ties to even) before the
+  attention chain uses them: Operator Fusion's exercise 1 lists RoPE and
+  attention as two ops of the unfused chain, and the tensor between them is
+  held in the inputs' bf16, so that is the result a fused kernel reproduces.
 
 Inputs are taken as given (typically bf16 values already rounded, passed as
 float32/float64 arrays or CPU torch tensors) and promoted to fp64.
@@ -68,6 +72,7 @@ __all__ = [
     "decode",
     "decode_multi",
     "rope_rotate",
+    "round_bf16",
 ]
 
 
@@ -169,14 +174,31 @@ def rope_rotate(x, positions, cos, sin, style: str) -> np.ndarray:
     raise ValueError(f"unknown rope style {style!r}")
 
 
+def round_bf16(x) -> np.ndarray:
+    """Round fp64 values to the nearest bf16 value (ties to even), returned as fp64.
+
+    bf16 keeps the top 16 bits of an fp32 word; the value is first rounded to
+    fp32 (exact for every value that is then representable in bf16), then its
+    low 16 bits are rounded away with ties going to the even neighbour.
+    """
+    f = np.asarray(x, dtype=np.float64).astype(np.float32)
+    u = f.view(np.uint32).astype(np.uint64)
+    finite = np.isfinite(f)
+    lsb = (u >> 16) & 1
+    r = ((u + 0x7FFF + lsb) >> 16) << 16
+    out = np.where(finite, r, u).astype(np.uint32).view(np.float32)
+    return out.astype(np.float64)
+
+
 def _rope_q_k(Qh, Kh, Lq, Lkv, rope, rotate_k=True):
-    """Rotate a head's query rows (positions Lkv - Lq + i) and key rows (positions j) when ``rope`` is given."""
+    """Rotate a head's query rows (positions Lkv - Lq + i) and key rows (positions j) when ``rope`` is given,
+    rounding the rotated values to bf16 (the dtype of the tensor between RoPE and attention)."""
     if rope is None:
         return Qh, Kh
     cos, sin, style = rope
-    Qh = rope_rotate(Qh, np.arange(Lq) + (Lkv - Lq), cos, sin, style)
+    Qh = round_bf16(rope_rotate(Qh, np.arange(Lq) + (Lkv - Lq), cos, sin, style))
     if rotate_k:
-        Kh = rope_rotate(Kh, np.arange(Lkv), cos, sin, style)
+        Kh = round_bf16(rope_rotate(Kh, np.arange(Lkv), cos, sin, style))
     return Qh, Kh
 
 
@@ -221,8 +243,8 @@ def attention_rows(q, k, v, scale: float, causal: bool, b: int, h: int, rows, ro
     Kh = to_f64(k[b, hk])
     if rope is not None:
         cos, sin, style = rope
-        Qh = rope_rotate(Qh, rows + (Lkv - Lq), cos, sin, style)
-        Kh = rope_rotate(Kh, np.arange(Lkv), cos, sin, style)
+        Qh = round_bf16(rope_rotate(Qh, rows + (Lkv - Lq), cos, sin, style))
+        Kh = round_bf16(rope_rotate(Kh, np.arange(Lkv), cos, sin, style))
     return attention_head(Qh, Kh, to_f64(v[b, hk]), scale, causal, visible=vis)
 
 
@@ -267,8 +289,8 @@ def attention_varlen_rows(q, k, v, cu_seqlens_q, cu_seqlens_k, scale: float, cau
     Kh = to_f64(k[ks:ke, hk])
     if rope is not None:
         cos, sin, style = rope
-        Qh = rope_rotate(Qh, rows + ((ke - ks) - (qe - qs)), cos, sin, style)
-        Kh = rope_rotate(Kh, np.arange(ke - ks), cos, sin, style)
+        Qh = round_bf16(rope_rotate(Qh, rows + ((ke - ks) - (qe - qs)), cos, sin, style))
+        Kh = round_bf16(rope_rotate(Kh, np.arange(ke - ks), cos, sin, style))
     return attention_head(Qh, Kh, to_f64(v[ks:ke, hk]), scale, causal, visible=vis)
 
 

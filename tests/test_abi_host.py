@@ -180,3 +180,53 @@ def test_workspace_bytes_formula(lib):
     assert lib.attn_decode_workspace_bytes(64, 8, 2, 99999, 128, 0) == want
     # too many rows for the counter area
     assert lib.attn_decode_workspace_bytes(65535, 64, 64, 16, 128, 0) == 0
+
+
+def _fwd_params(**kw):
+    p = B.attn_fwd_params()
+    p.q = p.k = p.v = p.out = FAKE
+    p.B, p.Hq, p.Hkv, p.Lq, p.Lkv, p.D = 1, 4, 2, 16, 16, 128
+    p.scale, p.causal = 0.1, 1
+    p.rope.cos, p.rope.sin, p.rope.max_pos, p.rope.style = FAKE, FAKE, 64, B.ATTN_ROPE_HALF
+    for k, v in kw.items():
+        if k.startswith("rope_"):
+            setattr(p.rope, k[5:], v)
+        else:
+            setattr(p, k, v)
+    return p
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(rope_style=3), B.ATTN_ERR_INVALID_ARG),
+    (dict(rope_sin=None), B.ATTN_ERR_INVALID_ARG),
+    (dict(rope_max_pos=0), B.ATTN_ERR_INVALID_ARG),
+    (dict(rope_max_pos=15), B.ATTN_ERR_INVALID_ARG),          # positions reach Lkv - 1 = 15
+    (dict(rope_cos=FAKE + 4), B.ATTN_ERR_ALIGNMENT),
+    (dict(Lq=32, Lkv=16), B.ATTN_ERR_INVALID_ARG),            # dense queries would sit before position 0
+])
+def test_fwd_rope_validation(lib, kw, code):
+    assert lib.attn_fwd_ex(ctypes.byref(_fwd_params(**kw))) == code
+
+
+def test_rope_off_when_style_none_or_no_table(lib):
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    # no rotation requested: the bad table fields are not looked at (fails only for want of a device)
+    for kw in (dict(rope_style=B.ATTN_ROPE_NONE, rope_max_pos=1), dict(rope_cos=None, rope_max_pos=1)):
+        assert lib.attn_fwd_ex(ctypes.byref(_fwd_params(**kw))) in (B.ATTN_ERR_UNSUPPORTED, B.ATTN_ERR_CUDA)
+
+
+def test_decode_rope_validation(lib):
+    p = B.attn_decode_params()
+    p.q = p.kcache = p.vcache = p.kv_lens = p.out = FAKE
+    p.B, p.Hq, p.Hkv, p.Lmax, p.D, p.scale = 1, 4, 4, 128, 128, 0.1
+    p.rope.cos, p.rope.sin, p.rope.max_pos, p.rope.style = FAKE, FAKE, 127, B.ATTN_ROPE_INTERLEAVED
+    assert lib.attn_decode_ex(ctypes.byref(p)) == B.ATTN_ERR_INVALID_ARG  # kv_len may reach Lmax = 128
+    assert lib.attn_decode_noalloc(ctypes.byref(p)) == B.ATTN_ERR_INVALID_ARG
+    m = B.attn_decode_multi_params()
+    m.q = m.kcache = m.vcache = m.kv_lens = m.out = FAKE
+    m.B, m.Hq, m.Hkv, m.Lq, m.Lmax, m.D, m.scale = 1, 4, 4, 2, 128, 128, 0.1
+    m.rope.cos, m.rope.sin, m.rope.max_pos, m.rope.style = FAKE, FAKE, 127, B.ATTN_ROPE_HALF
+    assert lib.attn_decode_multi(ctypes.byref(m)) == B.ATTN_ERR_INVALID_ARG

@@ -58,6 +58,16 @@ def test_decode_small(B, Hq, Hkv, Lmax, D, lens):
         assert_attn_close(O, lse, O_ref, lse_ref, f"chunk={chunk}")
 
 
+def test_decode_tiny_lengths_many_rows():
+    # Rows with one to three keys: one CTA per row, not one CTA walking them all.
+    lens = [1, 2, 3, 1, 1, 2, 3, 3, 2, 1, 1, 1, 2, 2, 3, 1]
+    q, kc, vc, _ = make_decode(len(lens), 32, 8, 8, 128, seed=5)
+    for chunk in (0, 64):
+        O, lse = run(q, kc, vc, torch.tensor(lens, dtype=torch.int32), 0.088, chunk=chunk)
+        O_ref, lse_ref = oracle.decode(q, kc, vc, lens, 0.088)
+        assert_attn_close(O, lse, O_ref, lse_ref, f"chunk={chunk}")
+
+
 def test_decode_all_sequences_empty():
     q, kc, vc, _ = make_decode(2, 8, 2, 64, 128, seed=4)
     O, lse = run(q, kc, vc, torch.zeros(2, dtype=torch.int32), 0.088)

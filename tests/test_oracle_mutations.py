@@ -35,6 +35,16 @@ def _rope_query_from_zero(Qh, Kh, Lq, Lkv, rope, rotate_k=True):
     return Qh, Kh
 
 
+def _rope_unrounded(Qh, Kh, Lq, Lkv, rope, rotate_k=True):
+    if rope is None:
+        return Qh, Kh
+    cos, sin, style = rope
+    Qh = OA.rope_rotate(Qh, np.arange(Lq) + (Lkv - Lq), cos, sin, style)
+    if rotate_k:
+        Kh = OA.rope_rotate(Kh, np.arange(Lkv), cos, sin, style)
+    return Qh, Kh
+
+
 def _rope_keys_not_rotated(Qh, Kh, Lq, Lkv, rope, rotate_k=True):
     return _orig["_rope_q_k"](Qh, Kh, Lq, Lkv, rope, rotate_k=False)
 
@@ -104,6 +114,7 @@ MUTATIONS = {
     "rope_styles_swapped": ("rope_rotate", _rope_styles_swapped),
     "rope_query_from_zero": ("_rope_q_k", _rope_query_from_zero),
     "rope_keys_not_rotated": ("_rope_q_k", _rope_keys_not_rotated),
+    "rope_unrounded": ("_rope_q_k", _rope_unrounded),
 }
 
 

@@ -328,11 +328,21 @@ def pin_rope_golden():
     for c in g["rotate"]:
         out = OA.rope_rotate(np.array([c["x"]]), [0], np.array([c["cos"]]), np.array([c["sin"]]), c["style"])
         np.testing.assert_allclose(out[0], c["out"], rtol=0, atol=1e-15, err_msg=c["name"])
+    for c in g["bf16_rounding"]:
+        assert OA.round_bf16(np.array([c["x"]]))[0] == c["out"], c
     for c in g["attention"]:
         rope = (np.array(c["cos"]), np.array(c["sin"]), c["style"])
         O, lse = OA.attention(np.array(c["q"]), np.array(c["k"]), np.array(c["v"]), c["scale"], c["causal"], rope=rope)
         np.testing.assert_allclose(O, np.array(c["O"]), rtol=0, atol=1e-13, err_msg=c["name"])
         np.testing.assert_allclose(lse, np.array(c["lse"]), rtol=0, atol=1e-13, err_msg=c["name"])
+
+
+def pin_round_bf16_matches_torch():
+    """Rounding to bf16 agrees with torch's fp32 -> bf16 cast (library routine) on random and edge values."""
+    r = _rng(176)
+    x = np.concatenate([r.standard_normal(5000) * 10.0 ** r.integers(-6, 6, 5000), [0.0, -0.0, 65504.0, 1e-40]])
+    want = torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16).double().numpy()
+    np.testing.assert_array_equal(OA.round_bf16(x), want)
 
 
 def pin_rope_complex_form():
@@ -389,7 +399,7 @@ def pin_rope_decode_is_last_prefill_row():
         qd = r.standard_normal((B, Hq, D))
         k = r.standard_normal((B, Hkv, Lmax, D))
         v = r.standard_normal((B, Hkv, Lmax, D))
-        kc = OA.rope_rotate(k, np.arange(Lmax), cos, sin, style)
+        kc = OA.round_bf16(OA.rope_rotate(k, np.arange(Lmax), cos, sin, style))  # the cache holds bf16 rotated keys
         O, lse = OA.decode(qd, kc, v, lens, 0.4, rope=rope)
         Om, lsem = OA.decode_multi(qd[:, :, None], kc, v, lens, 0.4, rope=rope)
         for b, n in enumerate(lens):
@@ -411,7 +421,7 @@ def pin_rope_multi_tokens_are_prefill_rows():
     q = r.standard_normal((B, Hq, Lq, D))
     k = r.standard_normal((B, Hkv, Lmax, D))
     v = r.standard_normal((B, Hkv, Lmax, D))
-    kc = OA.rope_rotate(k, np.arange(Lmax), cos, sin, "half")
+    kc = OA.round_bf16(OA.rope_rotate(k, np.arange(Lmax), cos, sin, "half"))
     O, lse = OA.decode_multi(q, kc, v, lens, 0.6, rope=rope)
     for b, n in enumerate(lens):
         Op, lsep = OA.attention(q[b:b + 1], k[b:b + 1, :, :n], v[b:b + 1, :, :n], 0.6, True, rope=rope)
@@ -463,6 +473,7 @@ PINS = [
     pin_decode_multi_brute_force,
     pin_decode_multi_golden,
     pin_rope_golden,
+    pin_round_bf16_matches_torch,
     pin_rope_complex_form,
     pin_rope_half_is_permuted_interleaved,
     pin_rope_norms_and_relative_positions,
