@@ -51,6 +51,9 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+// Cost, in keys, charged to every row with keys when the key space is split: the piece-end work of a row
+// (warp merge, output or partial, publish) takes about as long as streaming one 64-key stage.
+constexpr int kRowCost = 64;
 
 template <int D, int GP>
 struct DecodeCfg {
@@ -181,9 +184,14 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS, DecodeCfg<D, GP>::M
     if (geff < (long long)nonempty * Hg) geff = (long long)nonempty * Hg;
     if (geff > (long long)gridDim.x) geff = gridDim.x;
     if (geff < 1) geff = 1;
-    const long long per = (W + geff - 1) / geff;
+    // The split is made in a cost space where every row with keys also costs kRowCost keys' worth of time for
+    // its piece-end work (warp merge, output or partial, publish): a row occupies [rs, rs + kRowCost + len),
+    // its keys the last len positions, so a slice that takes on a row start also takes fewer keys.  Slices
+    // that fall inside a row's cost-only head take no keys of that row.
+    const long long Wc = W + (long long)kRowCost * nonempty * Hg;
+    const long long per = (Wc + geff - 1) / geff;
     const long long lo = (long long)cta * per;
-    const long long hi = min(lo + per, W);
+    const long long hi = min(lo + per, Wc);
 
     int t = 0;  // stages issued
     bool ok = true;
@@ -281,37 +289,40 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS, DecodeCfg<D, GP>::M
     };
 
     if (lo < hi) {
-      // locate the row holding key `lo`
-      long long acc = 0;  // first flattened key of sequence b
+      // locate the row whose cost interval holds position `lo`
+      long long acc = 0;  // first cost position of sequence b
       int b = 0, len = 0;
       for (; b < p.B; ++b) {
         len = seq_len(b);
-        if (acc + (long long)Hg * len > lo) break;
-        acc += (long long)Hg * len;
+        const long long rc = len > 0 ? (long long)len + kRowCost : 0;
+        if (acc + (long long)Hg * rc > lo) break;
+        acc += (long long)Hg * rc;
       }
-      int hg = (int)((lo - acc) / len);
-      long long row_start = acc + (long long)hg * len;
+      long long rcost = (long long)len + kRowCost;
+      int hg = (int)((lo - acc) / rcost);
+      long long rs = acc + (long long)hg * rcost;  // cost interval of row (b, hg): [rs, rs + rcost)
       long long pos = lo;
       while (ok && pos < hi) {
-        const int kb = (int)(pos - row_start);
-        const int ke = (int)min((long long)len, hi - row_start);
-        const long long cta_lo = row_start / per;
-        const long long cta_hi = (row_start + len - 1) / per;
-        const int np = (int)(cta_hi - cta_lo + 1);
-        const int slot = 2 * cta + (pos == lo ? 0 : 1);
-        const int lo_odd = (row_start != cta_lo * per) ? 1 : 0;
-        ok = emit(b, hg, kb, ke, np, slot, (int)cta_lo, lo_odd);
-        pos = row_start + ke;
+        const long long ks = rs + kRowCost;  // its keys: cost positions [ks, ks + len)
+        const long long a = max(pos, ks), e = min(hi, ks + len);
+        if (a < e) {
+          const long long cta_lo = ks / per;
+          const long long cta_hi = (ks + len - 1) / per;
+          const int np = (int)(cta_hi - cta_lo + 1);
+          const int slot = 2 * cta + (a == lo ? 0 : 1);
+          const int lo_odd = (ks != cta_lo * per) ? 1 : 0;
+          ok = emit(b, hg, (int)(a - ks), (int)(e - ks), np, slot, (int)cta_lo, lo_odd);
+        }
+        pos = rs + rcost;
         // next row (skip sequences with no keys)
-        row_start += len;
+        rs += rcost;
         if (++hg == Hg) {
           hg = 0;
-          acc += (long long)Hg * len;
           for (++b; b < p.B; ++b) {
             len = seq_len(b);
             if (len > 0) break;
           }
-          row_start = acc;
+          rcost = (long long)len + kRowCost;
         }
       }
     }

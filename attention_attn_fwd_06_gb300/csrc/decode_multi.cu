@@ -116,9 +116,15 @@ struct Piece {
   int lo_odd;  // 1 when the item starts inside (not at the start of) cta_lo's share
 };
 
-// Walks this CTA's share [lo, hi) of the flattened tile space.  Every role keeps its own copy.
+// Cost, in tiles, charged to every item with keys when the tile space is split: its piece-end work
+// (epilogue or partial, publish) takes about as long as streaming one K/V tile.
+constexpr int kItemCost = 1;
+
+// Walks this CTA's share [lo, hi) of the flattened cost space.  Item (b, hk) occupies [start, start + kItemCost
+// + T): its tiles are the last T positions, so a share that takes on an item start also takes fewer tiles, and a
+// share that falls inside an item's cost-only head takes none of its tiles.  Every role keeps its own copy.
 struct Walk {
-  long long per, lo, hi, pos, start;  // start: first flattened tile of the current item
+  long long per, lo, hi, pos, start;  // start: first cost position of the current item
   int b, hk, n, T;
 };
 
@@ -130,7 +136,7 @@ __device__ Walk walk_init(const MultiArgs& a, int lane) {
     const int raw = a.kv_lens[b];
     const int n = clamp_len(raw, a.Lmax);
     if (raw != n && blockIdx.x == 0) record_status(a.status, ATTN_ERR_DEVICE_BOUNDS);
-    part += tiles_of(n);
+    part += n > 0 ? tiles_of(n) + kItemCost : 0;
   }
 #pragma unroll
   for (int off = 16; off >= 1; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
@@ -150,11 +156,15 @@ __device__ Walk walk_init(const MultiArgs& a, int lane) {
     w.pos = w.hi;
     return w;
   }
-  // find the sequence holding tile lo: prefix sums of Hkv * tiles, 32 sequences per step
+  // find the sequence holding cost position lo: prefix sums of Hkv * (tiles + kItemCost), 32 sequences per step
   long long base = 0;
   for (int c0 = 0; c0 < a.B; c0 += 32) {
     const int b = c0 + lane;
-    const long long v = (b < a.B) ? (long long)tiles_of(clamp_len(a.kv_lens[b], a.Lmax)) * a.Hkv : 0;
+    long long v = 0;
+    if (b < a.B) {
+      const int n = clamp_len(a.kv_lens[b], a.Lmax);
+      v = n > 0 ? (long long)(tiles_of(n) + kItemCost) * a.Hkv : 0;
+    }
     long long incl = v;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -169,9 +179,9 @@ __device__ Walk walk_init(const MultiArgs& a, int lane) {
       w.b = c0 + src;
       w.n = clamp_len(a.kv_lens[w.b], a.Lmax);
       w.T = tiles_of(w.n);
-      const long long first = base + excl;  // first tile of sequence w.b
-      w.hk = (int)((w.lo - first) / w.T);
-      w.start = first + (long long)w.hk * w.T;
+      const long long first = base + excl;  // first cost position of sequence w.b
+      w.hk = (int)((w.lo - first) / (w.T + kItemCost));
+      w.start = first + (long long)w.hk * (w.T + kItemCost);
       break;
     }
     base += tot;
@@ -180,36 +190,40 @@ __device__ Walk walk_init(const MultiArgs& a, int lane) {
 }
 
 __device__ __forceinline__ bool walk_next(Walk& w, const MultiArgs& a, Piece& p) {
-  if (w.pos >= w.hi) return false;
-  p.b = w.b;
-  p.hk = w.hk;
-  p.n = w.n;
-  p.T = w.T;
-  p.t0 = (int)(w.pos - w.start);
-  p.t1 = (int)min((long long)w.T, w.hi - w.start);
-  const long long clo = w.start / w.per;
-  const long long chi = (w.start + w.T - 1) / w.per;
-  p.np = (int)(chi - clo + 1);
-  p.cta_lo = (int)clo;
-  p.lo_odd = (w.start != clo * w.per) ? 1 : 0;
-  p.slot = 2 * (int)blockIdx.x + (w.pos == w.lo ? 0 : 1);
-  w.pos = w.start + p.t1;
-  if (w.pos < w.hi) {  // advance to the next item that has keys
-    w.start += w.T;
-    if (++w.hk == a.Hkv) {
-      w.hk = 0;
-      for (++w.b; w.b < a.B; ++w.b) {
-        w.n = clamp_len(a.kv_lens[w.b], a.Lmax);
-        if (w.n > 0) break;
-      }
-      if (w.b >= a.B) {  // cannot happen while pos < hi; stop rather than read past kv_lens
-        w.pos = w.hi;
-        return true;
-      }
-      w.T = tiles_of(w.n);
+  while (w.pos < w.hi) {
+    const long long ts = w.start + kItemCost;  // the item's tiles: cost positions [ts, ts + T)
+    const long long s = max(w.pos, ts), e = min(w.hi, ts + w.T);
+    const bool has = s < e;
+    if (has) {
+      p.b = w.b;
+      p.hk = w.hk;
+      p.n = w.n;
+      p.T = w.T;
+      p.t0 = (int)(s - ts);
+      p.t1 = (int)(e - ts);
+      const long long clo = ts / w.per;
+      const long long chi = (ts + w.T - 1) / w.per;
+      p.np = (int)(chi - clo + 1);
+      p.cta_lo = (int)clo;
+      p.lo_odd = (ts != clo * w.per) ? 1 : 0;
+      p.slot = 2 * (int)blockIdx.x + (s == w.lo ? 0 : 1);
     }
+    w.pos = w.start + w.T + kItemCost;
+    if (w.pos < w.hi) {  // advance to the next item that has keys
+      w.start = w.pos;
+      if (++w.hk == a.Hkv) {
+        w.hk = 0;
+        for (++w.b; w.b < a.B; ++w.b) {
+          w.n = clamp_len(a.kv_lens[w.b], a.Lmax);
+          if (w.n > 0) break;
+        }
+        if (w.b >= a.B) w.pos = w.hi;  // cannot happen while pos < hi; stop rather than read past kv_lens
+        w.T = tiles_of(w.n);
+      }
+    }
+    if (has) return true;
   }
-  return true;
+  return false;
 }
 
 // Partial slot of the i-th CTA holding a piece of an item.

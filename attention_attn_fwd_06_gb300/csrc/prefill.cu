@@ -44,29 +44,34 @@ namespace {
 constexpr int BM = 128;  // query rows per tile (TMEM lanes)
 constexpr int BN = 128;  // keys per K/V tile
 constexpr int NQ = 2;    // query tiles per CTA (ping-pong)
-constexpr int kThreads = 32 * (3 + 4 * NQ);  // TMA warp, MMA warp, a 4-warp softmax group per query tile, RoPE warp
+constexpr int kRopeWarps = 2;  // warps that rotate each K tile (RoPE variant only)
+// TMA warp, MMA warp, one 4-warp softmax group per query tile, and with RoPE the K-rotation warps
+template <bool ROPE>
+constexpr int kThreads = 32 * (2 + 4 * NQ + (ROPE ? kRopeWarps : 0));
 constexpr int kWarpTMA = 0;
 constexpr int kWarpMMA = 1;
 constexpr int kFirstSoftmaxWarp = 2;
-constexpr int kWarpRope = 2 + 4 * NQ;  // rotates each K tile when RoPE is on (idle otherwise)
+constexpr int kWarpRope = 2 + 4 * NQ;  // first K-rotation warp
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: p <= 2^8 between rescales
 
-template <int D>
+template <int D, bool ROPE>
 struct Cfg {
   static constexpr int NDB = D / 64;             // 128-byte column blocks per row
   static constexpr int TILE_BYTES = BM * D * 2;  // one Q, K or V tile (BM == BN)
   static constexpr int BLOCK_BYTES = BM * 128;   // one 64-column block of a tile
-  static constexpr int NS = (D == 128) ? 2 : 4;  // K/V ring depth
+  static constexpr int NSV = (D == 128) ? 2 : 4;  // V ring depth
+  // K ring depth: with RoPE one slot more, so a K tile lands and is rotated well before its S MMAs
+  static constexpr int NSK = NSV + (ROPE ? 1 : 0);
   static constexpr int OFF_Q = 0;                // NQ query tiles
   static constexpr int OFF_K = OFF_Q + NQ * TILE_BYTES;
-  static constexpr int OFF_V = OFF_K + NS * TILE_BYTES;
-  static constexpr int OFF_BAR = OFF_V + NS * TILE_BYTES;
-  // barriers: q_full, q_empty, k_full[NS], v_full[NS], k_empty[NS], v_empty[NS], s_full[NQ], p_full[NQ],
-  // o_done[NQ], drain, q_ready, k_ready[NS]
-  static constexpr int NBAR = 2 + 4 * NS + 3 * NQ + 1 + 1 + NS;
+  static constexpr int OFF_V = OFF_K + NSK * TILE_BYTES;
+  static constexpr int OFF_BAR = OFF_V + NSV * TILE_BYTES;
+  // barriers: q_full, q_empty, k_full[NSK], v_full[NSV], k_empty[NSK], v_empty[NSV], s_full[NQ], p_full[NQ],
+  // o_done[NQ], drain, q_ready, k_ready[NSK]
+  static constexpr int NBAR = 2 + 3 * NSK + 2 * NSV + 3 * NQ + 2;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // tmem address, abort flag
   static constexpr int SMEM_USED = OFF_MISC + 16;
   static constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // slack to align the base to 1024
@@ -165,11 +170,11 @@ __device__ __forceinline__ bool make_job(const PrefillArgs& a, int item, int hal
   return true;
 }
 
-template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int D, bool ROPE>
+__global__ void __launch_bounds__(kThreads<ROPE>, 1)
     prefill_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                        const __grid_constant__ CUtensorMap tmv, const PrefillArgs a) {
-  using C = Cfg<D>;
+  using C = Cfg<D, ROPE>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* Qs = smem + C::OFF_Q;
@@ -179,10 +184,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* q_full = bars;
   uint64_t* q_empty = bars + 1;         // Q tiles free: every S MMA of the job has completed
   uint64_t* k_full = bars + 2;
-  uint64_t* v_full = k_full + C::NS;
-  uint64_t* k_empty = v_full + C::NS;   // K slot free: every S = Q K^T reading it has completed
-  uint64_t* v_empty = k_empty + C::NS;  // V slot free: every P V reading it has completed
-  uint64_t* s_full = v_empty + C::NS;
+  uint64_t* v_full = k_full + C::NSK;
+  uint64_t* k_empty = v_full + C::NSV;   // K slot free: every S = Q K^T reading it has completed
+  uint64_t* v_empty = k_empty + C::NSK;  // V slot free: every P V reading it has completed
+  uint64_t* s_full = v_empty + C::NSV;
   uint64_t* p_full = s_full + NQ;
   uint64_t* o_done = p_full + NQ;
   uint64_t* drain = o_done + NQ;
@@ -193,12 +198,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const bool rope = a.rope.style != 0;
+  constexpr bool rope = ROPE;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::NBAR; ++i) {
       const bool is_p = (&bars[i] >= p_full) && (&bars[i] < p_full + NQ);
-      mbar_init(&bars[i], is_p ? 128 : (&bars[i] == q_ready ? 128 * NQ : 1));
+      const bool is_kr = (&bars[i] >= k_ready) && (&bars[i] < k_ready + C::NSK);
+      mbar_init(&bars[i], is_p ? 128 : (&bars[i] == q_ready ? 128 * NQ : (is_kr ? kRopeWarps : 1)));
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -219,65 +225,134 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::tma_prefetch_desc(&tmq);
       tc::tma_prefetch_desc(&tmk);
       tc::tma_prefetch_desc(&tmv);
-      int kv = 0;     // K/V steps issued (ring position)
-      int qjobs = 0;  // jobs whose Q was loaded
-      bool q_pending = false;
+      auto issue_q = [&](const Job& jb) {
+        const int qhead = a.varlen ? jb.h : jb.bs * a.Hq + jb.h;
+        uint32_t qbytes = 0;
+#pragma unroll
+        for (int t = 0; t < NQ; ++t) qbytes += jb.nt[t] > 0 ? C::TILE_BYTES : 0;
+        mbar_arrive_expect_tx(q_full, qbytes);
+#pragma unroll
+        for (int t = 0; t < NQ; ++t) {
+          if (jb.nt[t] == 0) continue;
+          const int qrow = jb.q_start + jb.q00 + t * BM;
+          for (int db = 0; db < C::NDB; ++db)
+            tc::tma_load_3d(Qs + t * C::TILE_BYTES + db * C::BLOCK_BYTES, &tmq, db * 64, a.varlen ? qhead : qrow,
+                            a.varlen ? qrow : qhead, q_full);
+        }
+      };
+      // K or V tile j of a job into `slot` of its ring
+      auto issue_kv = [&](const CUtensorMap* map, uint8_t* ring, uint64_t* full, int slot, const Job& jb, int j) {
+        const int khead = a.varlen ? jb.hk : jb.bs * a.Hkv + jb.hk;
+        const int krow = jb.k_start + j * BN;
+        mbar_arrive_expect_tx(&full[slot], C::TILE_BYTES);
+        for (int db = 0; db < C::NDB; ++db)
+          tc::tma_load_3d(ring + slot * C::TILE_BYTES + db * C::BLOCK_BYTES, map, db * 64, a.varlen ? khead : krow,
+                          a.varlen ? krow : khead, &full[slot]);
+      };
+      int ks = 0, vs = 0;  // K and V steps issued (ring positions)
+      int qjobs = 0;       // jobs whose Q was loaded
       bool ok = true;
-      for (int item = blockIdx.x; ok && item < a.total_items; item += gridDim.x) {
-        for (int half = 0; ok && half < 2; ++half) {
+      if constexpr (!ROPE) {
+        for (int item = blockIdx.x; ok && item < a.total_items; item += gridDim.x) {
+          for (int half = 0; ok && half < 2; ++half) {
+            Job jb;
+            if (!make_job(a, item, half, jb) || jb.n == 0) continue;
+            if (qjobs > 0 && !mbar_wait(q_empty, (qjobs - 1) & 1, a.status, abort_flag)) {
+              ok = false;
+              break;
+            }
+            issue_q(jb);
+            ++qjobs;
+            for (int j = 0; j < jb.n; ++j) {
+              // K slots free up after the S MMAs, V slots after the P V MMAs: the two rings refill independently
+              if (ks >= C::NSK &&
+                  !mbar_wait(&k_empty[ks % C::NSK], ((ks / C::NSK) - 1) & 1, a.status, abort_flag)) {
+                ok = false;
+                break;
+              }
+              issue_kv(&tmk, Ks, k_full, ks % C::NSK, jb, j);
+              ++ks;
+              if (vs >= C::NSV &&
+                  !mbar_wait(&v_empty[vs % C::NSV], ((vs / C::NSV) - 1) & 1, a.status, abort_flag)) {
+                ok = false;
+                break;
+              }
+              issue_kv(&tmv, Vs, v_full, vs % C::NSV, jb, j);
+              ++vs;
+            }
+          }
+        }
+      } else {
+        // Three cursors walk the same job sequence -- Q loads (each once the previous job's S MMAs have released
+        // the Q tiles), K loads and V loads (each as soon as its ring slot frees) -- and one thread issues
+        // whichever is ready, so K runs ahead of V and the rotation warps get each K tile well before its S MMAs.
+        struct Cursor {
+          int item, part, j;  // item, which of its two jobs, step within the job
+          bool valid;
           Job jb;
-          if (!make_job(a, item, half, jb) || jb.n == 0) continue;
-          const int qhead = a.varlen ? jb.h : jb.bs * a.Hq + jb.h;
-          const int khead = a.varlen ? jb.hk : jb.bs * a.Hkv + jb.hk;
-          if (qjobs > 0 && !mbar_wait(q_empty, (qjobs - 1) & 1, a.status, abort_flag)) {
-            ok = false;
-            break;
+        };
+        auto seek = [&](Cursor& c) {  // the first job with work at or after (item, part)
+          c.valid = false;
+          c.j = 0;
+          for (; c.item < a.total_items; c.item += gridDim.x, c.part = 0)
+            for (; c.part < 2; ++c.part)
+              if (make_job(a, c.item, c.part, c.jb) && c.jb.n > 0) {
+                c.valid = true;
+                return;
+              }
+        };
+        auto next_job = [&](Cursor& c) {
+          ++c.part;
+          seek(c);
+        };
+        Cursor cq;
+        cq.item = blockIdx.x;
+        cq.part = 0;
+        seek(cq);
+        Cursor ck = cq, cv = cq;
+        uint64_t t_progress = globaltimer_ns();
+        while (cq.valid || ck.valid || cv.valid) {
+          bool progress = false;
+          if (cq.valid && (qjobs == 0 || mbar_try_wait(q_empty, (qjobs - 1) & 1))) {
+            issue_q(cq.jb);
+            ++qjobs;
+            next_job(cq);
+            progress = true;
           }
-          uint32_t qbytes = 0;
-#pragma unroll
-          for (int t = 0; t < NQ; ++t) qbytes += jb.nt[t] > 0 ? C::TILE_BYTES : 0;
-          mbar_arrive_expect_tx(q_full, qbytes);
-#pragma unroll
-          for (int t = 0; t < NQ; ++t) {
-            if (jb.nt[t] == 0) continue;
-            const int qrow = jb.q_start + jb.q00 + t * BM;
-            for (int db = 0; db < C::NDB; ++db)
-              tc::tma_load_3d(Qs + t * C::TILE_BYTES + db * C::BLOCK_BYTES, &tmq, db * 64, a.varlen ? qhead : qrow,
-                              a.varlen ? qrow : qhead, q_full);
+          if (ck.valid && (ks < C::NSK || mbar_try_wait(&k_empty[ks % C::NSK], ((ks / C::NSK) - 1) & 1))) {
+            issue_kv(&tmk, Ks, k_full, ks % C::NSK, ck.jb, ck.j);
+            ++ks;
+            if (++ck.j == ck.jb.n) next_job(ck);
+            progress = true;
           }
-          q_pending = true;
-          ++qjobs;
-          for (int j = 0; j < jb.n; ++j) {
-            // K slots free up after the S MMAs, V slots after the P V MMAs: the two rings refill independently
-            const int slot = kv % C::NS;
-            const int krow = jb.k_start + j * BN;
-            if (kv >= C::NS && !mbar_wait(&k_empty[slot], ((kv / C::NS) - 1) & 1, a.status, abort_flag)) {
+          if (cv.valid && (vs < C::NSV || mbar_try_wait(&v_empty[vs % C::NSV], ((vs / C::NSV) - 1) & 1))) {
+            issue_kv(&tmv, Vs, v_full, vs % C::NSV, cv.jb, cv.j);
+            ++vs;
+            if (++cv.j == cv.jb.n) next_job(cv);
+            progress = true;
+          }
+          if (progress) {
+            t_progress = globaltimer_ns();
+          } else {
+            if (*abort_flag) {
               ok = false;
               break;
             }
-            mbar_arrive_expect_tx(&k_full[slot], C::TILE_BYTES);
-            for (int db = 0; db < C::NDB; ++db)
-              tc::tma_load_3d(Ks + slot * C::TILE_BYTES + db * C::BLOCK_BYTES, &tmk, db * 64,
-                              a.varlen ? khead : krow, a.varlen ? krow : khead, &k_full[slot]);
-            if (kv >= C::NS && !mbar_wait(&v_empty[slot], ((kv / C::NS) - 1) & 1, a.status, abort_flag)) {
-              mbar_wait(&k_full[slot], (kv / C::NS) & 1, a.status, nullptr);  // K is in flight: let it land
+            if (globaltimer_ns() - t_progress > kWaitLimitNs) {
+              record_status(a.status, ATTN_ERR_DEVICE_TIMEOUT);
+              *abort_flag = 1;
               ok = false;
               break;
             }
-            mbar_arrive_expect_tx(&v_full[slot], C::TILE_BYTES);
-            for (int db = 0; db < C::NDB; ++db)
-              tc::tma_load_3d(Vs + slot * C::TILE_BYTES + db * C::BLOCK_BYTES, &tmv, db * 64,
-                              a.varlen ? khead : krow, a.varlen ? krow : khead, &v_full[slot]);
-            ++kv;
           }
         }
       }
-      if (*abort_flag) {  // let in-flight copies land before shared memory is released
-        if (q_pending) mbar_wait(q_full, (qjobs - 1) & 1, a.status, nullptr);
-        for (int g = (kv > C::NS ? kv - C::NS : 0); g < kv; ++g) {
-          mbar_wait(&k_full[g % C::NS], (g / C::NS) & 1, a.status, nullptr);
-          mbar_wait(&v_full[g % C::NS], (g / C::NS) & 1, a.status, nullptr);
-        }
+      if (!ok || *abort_flag) {  // let in-flight copies land before shared memory is released
+        if (qjobs > 0) mbar_wait(q_full, (qjobs - 1) & 1, a.status, nullptr);
+        for (int g = (ks > C::NSK ? ks - C::NSK : 0); g < ks; ++g)
+          mbar_wait(&k_full[g % C::NSK], (g / C::NSK) & 1, a.status, nullptr);
+        for (int g = (vs > C::NSV ? vs - C::NSV : 0); g < vs; ++g)
+          mbar_wait(&v_full[g % C::NSV], (g / C::NSV) & 1, a.status, nullptr);
       }
     }
   } else if (warp == kWarpMMA) {
@@ -285,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       auto issue_s = [&](int t, int g) {
         const uint32_t q_addr = smem_u32(Qs + t * C::TILE_BYTES);
-        const uint32_t k_addr = smem_u32(Ks + (g % C::NS) * C::TILE_BYTES);
+        const uint32_t k_addr = smem_u32(Ks + (g % C::NSK) * C::TILE_BYTES);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t koff = (kk >> 2) * C::BLOCK_BYTES + (kk & 3) * 32;
@@ -295,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::mma_commit(&s_full[t]);
       };
       auto issue_pv = [&](int t, int g, bool first) {
-        const uint32_t v_addr = smem_u32(Vs + (g % C::NS) * C::TILE_BYTES);
+        const uint32_t v_addr = smem_u32(Vs + (g % C::NSV) * C::TILE_BYTES);
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
           tc::mma_ts(tbase + C::tm_o(t), tbase + C::tm_s(t) + kk * 8,
@@ -313,7 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int g0 = kv;
           // with RoPE, wait for the rotated Q tiles and K slots instead of the raw ones
           if (!mbar_wait(rope ? q_ready : q_full, qjobs & 1, a.status, abort_flag) ||
-              !mbar_wait(rope ? &k_ready[g0 % C::NS] : &k_full[g0 % C::NS], (g0 / C::NS) & 1, a.status,
+              !mbar_wait(rope ? &k_ready[g0 % C::NSK] : &k_full[g0 % C::NSK], (g0 / C::NSK) & 1, a.status,
                          abort_flag)) {
             ok = false;
             break;
@@ -323,12 +398,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int t = 0; t < NQ; ++t)
             if (jb.nt[t] > 0) issue_s(t, g0);
-          tc::mma_commit(&k_empty[g0 % C::NS]);
+          tc::mma_commit(&k_empty[g0 % C::NSK]);
           if (jb.n == 1) tc::mma_commit(q_empty);
           for (int j = 0; ok && j < jb.n; ++j) {
             const int g = g0 + j;
-            const int slot = g % C::NS;
-            if (!mbar_wait(&v_full[slot], (g / C::NS) & 1, a.status, abort_flag)) {
+            const int slot = g % C::NSV;
+            if (!mbar_wait(&v_full[slot], (g / C::NSV) & 1, a.status, abort_flag)) {
               ok = false;
               break;
             }
@@ -347,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               tc::fence_after_sync();
               issue_pv(t, g, j == 0);
               if (j + 1 < jb.nt[t]) {
-                if (!mbar_wait(rope ? &k_ready[(g + 1) % C::NS] : &k_full[(g + 1) % C::NS], ((g + 1) / C::NS) & 1,
+                if (!mbar_wait(rope ? &k_ready[(g + 1) % C::NSK] : &k_full[(g + 1) % C::NSK], ((g + 1) / C::NSK) & 1,
                                a.status, abort_flag)) {
                   ok = false;
                   break;
@@ -359,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!ok) break;
             tc::mma_commit(&v_empty[slot]);                         // both P V_j issued
-            if (next_s) tc::mma_commit(&k_empty[(g + 1) % C::NS]);  // every S reading K_{j+1} issued
+            if (next_s) tc::mma_commit(&k_empty[(g + 1) % C::NSK]);  // every S reading K_{j+1} issued
             if (j == jb.n - 2) tc::mma_commit(q_empty);             // the job's last S MMAs are issued
           }
           kv += jb.n;
@@ -370,8 +445,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::mma_commit(drain);
       mbar_wait(drain, 0, a.status, nullptr);
     }
-  } else if (warp == kWarpRope) {
+  } else if (ROPE && warp >= kWarpRope) {
     // ---------------- RoPE: rotate every K tile once it lands (key j of a sequence sits at position j) --------
+    // Each of the kRopeWarps warps takes every kRopeWarps-th row; the K slot is released to the MMA warp when
+    // all of them have arrived.
+    const int rw = warp - kWarpRope;
     if (rope) {
       int kv = 0;
       bool ok = true;
@@ -381,14 +459,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!make_job(a, item, half, jb) || jb.n == 0) continue;
           for (int j = 0; j < jb.n; ++j) {
             const int g = kv + j;
-            const int slot = g % C::NS;
-            if (!mbar_wait(&k_full[slot], (g / C::NS) & 1, a.status, abort_flag)) {
+            const int slot = g % C::NSK;
+            if (!mbar_wait(&k_full[slot], (g / C::NSK) & 1, a.status, abort_flag)) {
               ok = false;
               break;
             }
             uint8_t* tile = Ks + slot * C::TILE_BYTES;
 #pragma unroll 1
-            for (int r = lane; r < BN; r += 32) {
+            for (int r = rw * 32 + lane; r < BN; r += 32 * kRopeWarps) {
               const int key = j * BN + r;
               if (key < jb.Lkv_s) {  // rows past the sequence are masked out anyway
                 const size_t off = (size_t)key * (D / 2);
@@ -602,16 +680,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D>
+template <int D, bool ROPE>
 cudaError_t launch_d(const PrefillLaunch& p) {
-  using C = Cfg<D>;
+  using C = Cfg<D, ROPE>;
   static bool attr_set[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!attr_set[dev]) {
-    e = cudaFuncSetAttribute(prefill_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
+    e = cudaFuncSetAttribute(prefill_fwd_kernel<D, ROPE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
@@ -670,15 +749,16 @@ cudaError_t launch_d(const PrefillLaunch& p) {
   int grid = persistent ? (p.num_sms > 0 ? p.num_sms : 148) : a.total_items;
   if (grid > a.total_items) grid = a.total_items;
   if (grid < 1) grid = 1;
-  prefill_fwd_kernel<D><<<grid, kThreads, C::SMEM_ALLOC, p.stream>>>(tmq, tmk, tmv, a);
+  prefill_fwd_kernel<D, ROPE><<<grid, kThreads<ROPE>, C::SMEM_ALLOC, p.stream>>>(tmq, tmk, tmv, a);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_prefill(const PrefillLaunch& p) {
-  if (p.D == 64) return launch_d<64>(p);
-  if (p.D == 128) return launch_d<128>(p);
+  const bool rope = p.rope.style != 0;
+  if (p.D == 64) return rope ? launch_d<64, true>(p) : launch_d<64, false>(p);
+  if (p.D == 128) return rope ? launch_d<128, true>(p) : launch_d<128, false>(p);
   return cudaErrorNotSupported;
 }
 

@@ -46,50 +46,50 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
 }
 
 // Rotates row `row` of a D-column swizzled tile to the position whose table rows are cos_row / sin_row
-// (global memory, 16-byte aligned, D/2 floats each).
+// (global memory, 16-byte aligned, D/2 floats each).  All of the row's table values are loaded before the
+// tile is touched, so one row costs one memory latency rather than one per chunk.
 template <int D>
-__device__ __forceinline__ void rope_rotate_row_sw128(uint8_t* tile, int block_bytes, int row, const float* cos_row,
-                                                      const float* sin_row, int style) {
+__device__ __forceinline__ void rope_rotate_row_sw128(uint8_t* tile, int block_bytes, int row,
+                                                      const float* __restrict__ cos_row,
+                                                      const float* __restrict__ sin_row, int style) {
+  constexpr int NP = D / 2;  // pairs
+  float4 c4[NP / 4], s4[NP / 4];
+#pragma unroll
+  for (int i = 0; i < NP / 4; ++i) {
+    c4[i] = __ldg(reinterpret_cast<const float4*>(cos_row) + i);
+    s4[i] = __ldg(reinterpret_cast<const float4*>(sin_row) + i);
+  }
+  auto cf = [&](int i) -> float { return reinterpret_cast<const float*>(c4)[i]; };
+  auto sf = [&](int i) -> float { return reinterpret_cast<const float*>(s4)[i]; };
   if (style == 1) {
     // pairs (i, i + D/2): chunk x0 of the first half with the chunk D/2 columns later
-#pragma unroll 2
-    for (int x0 = 0; x0 < D / 2; x0 += 8) {
+#pragma unroll
+    for (int x0 = 0; x0 < NP; x0 += 8) {
       uint4* pa = sw128_chunk(tile, block_bytes, row, x0);
-      uint4* pb = sw128_chunk(tile, block_bytes, row, x0 + D / 2);
-      float a[8], b[8], c[8], s[8];
+      uint4* pb = sw128_chunk(tile, block_bytes, row, x0 + NP);
+      float a[8], b[8], ra[8], rb[8];
       unpack8(*pa, a);
       unpack8(*pb, b);
-      const float4 c0 = __ldg(reinterpret_cast<const float4*>(cos_row + x0));
-      const float4 c1 = __ldg(reinterpret_cast<const float4*>(cos_row + x0 + 4));
-      const float4 s0 = __ldg(reinterpret_cast<const float4*>(sin_row + x0));
-      const float4 s1 = __ldg(reinterpret_cast<const float4*>(sin_row + x0 + 4));
-      c[0] = c0.x; c[1] = c0.y; c[2] = c0.z; c[3] = c0.w; c[4] = c1.x; c[5] = c1.y; c[6] = c1.z; c[7] = c1.w;
-      s[0] = s0.x; s[1] = s0.y; s[2] = s0.z; s[3] = s0.w; s[4] = s1.x; s[5] = s1.y; s[6] = s1.z; s[7] = s1.w;
-      float ra[8], rb[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        ra[j] = fmaf(a[j], c[j], -b[j] * s[j]);
-        rb[j] = fmaf(b[j], c[j], a[j] * s[j]);
+        ra[j] = fmaf(a[j], cf(x0 + j), -b[j] * sf(x0 + j));
+        rb[j] = fmaf(b[j], cf(x0 + j), a[j] * sf(x0 + j));
       }
       *pa = pack8(ra);
       *pb = pack8(rb);
     }
   } else {
     // pairs (2i, 2i + 1): every chunk holds four whole pairs
-#pragma unroll 2
+#pragma unroll
     for (int x0 = 0; x0 < D; x0 += 8) {
       uint4* pc = sw128_chunk(tile, block_bytes, row, x0);
-      float v[8];
+      float v[8], r[8];
       unpack8(*pc, v);
-      const float4 c4 = __ldg(reinterpret_cast<const float4*>(cos_row + x0 / 2));
-      const float4 s4 = __ldg(reinterpret_cast<const float4*>(sin_row + x0 / 2));
-      const float c[4] = {c4.x, c4.y, c4.z, c4.w};
-      const float s[4] = {s4.x, s4.y, s4.z, s4.w};
-      float r[8];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        r[2 * k] = fmaf(v[2 * k], c[k], -v[2 * k + 1] * s[k]);
-        r[2 * k + 1] = fmaf(v[2 * k + 1], c[k], v[2 * k] * s[k]);
+        const int i = x0 / 2 + k;
+        r[2 * k] = fmaf(v[2 * k], cf(i), -v[2 * k + 1] * sf(i));
+        r[2 * k + 1] = fmaf(v[2 * k + 1], cf(i), v[2 * k] * sf(i));
       }
       *pc = pack8(r);
     }

@@ -52,11 +52,15 @@ WORKLOADS = {
         Workload("decode_gqa", "decode", 1001, B=8, Hq=32, Hkv=8, D=128, L=4096, kv_range=(512, 4096)),
         Workload("decode_gqa_paged16", "decode", 1001, B=8, Hq=32, Hkv=8, D=128, L=4096, kv_range=(512, 4096),
                  extra={"page_size": 16}),
+        Workload("decode_gqa_rope", "decode", 1001, B=8, Hq=32, Hkv=8, D=128, L=4096, kv_range=(512, 4096),
+                 extra={"rope": "half"}),
         Workload("decode_long", "decode", 1002, B=4, Hq=32, Hkv=8, D=128, L=131072,
                  kv_lens=(32768, 65536, 98304, 131072)),
         Workload("decode_multi_gqa", "decode_multi", 1006, B=8, Hq=32, Hkv=8, D=128, L=4096, Lq=8,
                  kv_range=(512, 4096)),
         Workload("prefill_causal", "prefill", 1003, B=4, Hq=32, Hkv=32, D=128, L=4096, causal=True),
+        Workload("prefill_causal_rope", "prefill", 1003, B=4, Hq=32, Hkv=32, D=128, L=4096, causal=True,
+                 extra={"rope": "half"}),
         Workload("prefill_ragged_gqa", "varlen", 1004, B=16, Hq=32, Hkv=8, D=128, causal=True,
                  seq_range=(256, 8192)),
         Workload("prefill_noncausal_d64", "prefill", 1005, B=2, Hq=16, Hkv=16, D=64, L=8192, causal=False),

@@ -155,7 +155,20 @@ def _pin(t):
     return t.pin_memory() if torch.cuda.is_available() else t
 
 
-class DecodeCase:
+class _RopeMixin:
+    def _rope_setup(self, w, max_pos, device):
+        """RoPE tables (model constants: resident on the device, not copied per step) when the workload asks."""
+        self.rope_style = w.extra.get("rope")
+        self.rope_dev = self.rope_host = None
+        if self.rope_style:
+            from attention_attn_fwd_06_gb300.inputs import rope_tables
+
+            cos, sin = rope_tables(max_pos, w.D)
+            self.rope_host = (cos.numpy(), sin.numpy(), self.rope_style)
+            self.rope_dev = (cos.to(device), sin.to(device), self.rope_style)
+
+
+class DecodeCase(_RopeMixin):
     def __init__(self, w, device):
         import torch
 
@@ -172,6 +185,7 @@ class DecodeCase:
                                           kv_lens=w.kv_lens or None, kv_range=w.kv_range or None)
         self.page_size = w.extra.get("page_size")
         self.oracle_host = (q, kc, vc)
+        self._rope_setup(w, w.L, device)
         if self.page_size:
             from attention_attn_fwd_06_gb300.inputs import make_pages
 
@@ -203,15 +217,16 @@ class DecodeCase:
     def _call(self):
         from attention_attn_fwd_06_gb300 import binding as AB
 
+        r = self.rope_dev
         if self.page_size:
             q, kp, vp, lens, table = self.dev
-            AB.attn_decode_paged(q, kp, vp, table, lens, out=self.out, lse=self.lse, scale=self.w.scale)
+            AB.attn_decode_paged(q, kp, vp, table, lens, out=self.out, lse=self.lse, scale=self.w.scale, rope=r)
         elif self.multi:
             q, kc, vc, lens = self.dev
-            AB.attn_decode_multi(q, kc, vc, lens, out=self.out, lse=self.lse, scale=self.w.scale)
+            AB.attn_decode_multi(q, kc, vc, lens, out=self.out, lse=self.lse, scale=self.w.scale, rope=r)
         else:
             q, kc, vc, lens = self.dev
-            AB.attn_decode(q, kc, vc, lens, out=self.out, lse=self.lse, scale=self.w.scale)
+            AB.attn_decode(q, kc, vc, lens, out=self.out, lse=self.lse, scale=self.w.scale, rope=r)
 
     def step(self):
         self._call()
@@ -228,13 +243,14 @@ class DecodeCase:
         return run_oracle_pool(self, budget_s)
 
 
-class PrefillCase:
+class PrefillCase(_RopeMixin):
     def __init__(self, w, device):
         import torch
 
         from attention_attn_fwd_06_gb300.inputs import make_prefill, make_varlen
 
         self.w = w
+        self._rope_setup(w, w.L if w.kind != "varlen" else w.seq_range[1], device)
         if w.kind == "varlen":
             q, k, v, cu = make_varlen(w.B, w.Hq, w.Hkv, w.D, w.seed, seq_range=w.seq_range)
             self.cu = cu
@@ -271,11 +287,12 @@ class PrefillCase:
         if w.kind == "varlen":
             q, k, v, cu = self.dev
             mx = max(self.seqlens)
-            AB.attn_fwd_varlen(q, k, v, cu, cu, mx, mx, out=self.out, lse=self.lse, causal=w.causal, scale=w.scale)
+            AB.attn_fwd_varlen(q, k, v, cu, cu, mx, mx, out=self.out, lse=self.lse, causal=w.causal, scale=w.scale,
+                               rope=self.rope_dev)
         else:
             q, k, v = self.dev
             AB.attn_fwd(q, k, v, out=self.out, lse=self.lse, causal=w.causal, scale=w.scale,
-                        out_dtype=torch.float32 if w.out_f32 else torch.bfloat16)
+                        out_dtype=torch.float32 if w.out_f32 else torch.bfloat16, rope=self.rope_dev)
 
     def step(self):
         self._call()
@@ -299,19 +316,18 @@ def _oracle_task(args):
 
     import oracle
 
-    kind, payload = args
+    kind, payload, rope = args
     t0 = time.perf_counter()
+    # one (sequence, head) problem through the oracle's own entry points
     if kind == "decode":
         q, kc, vc, n, scale = payload
-        oracle.attention_head(q[None, :].astype(np.float64), kc[:n].astype(np.float64), vc[:n].astype(np.float64),
-                              scale, causal=False)
+        oracle.decode(q[None, None], kc[None, None, :n], vc[None, None, :n], [n], scale, rope=rope)
     elif kind == "decode_multi":
         q, kc, vc, n, scale = payload  # q [Lq, D]: bottom-right causal over the sequence's n keys
-        oracle.attention_head(q.astype(np.float64), kc[:n].astype(np.float64), vc[:n].astype(np.float64), scale,
-                              causal=True)
+        oracle.decode_multi(q[None, None], kc[None, None, :n], vc[None, None, :n], [n], scale, rope=rope)
     else:
         q, k, v, scale, causal = payload
-        oracle.attention_head(q.astype(np.float64), k.astype(np.float64), v.astype(np.float64), scale, causal)
+        oracle.attention(q[None, None], k[None, None], v[None, None], scale, causal, rope=rope)
     return time.perf_counter() - t0
 
 
@@ -342,7 +358,7 @@ def run_oracle_pool(case, budget_s):
                 n = case.lens[b]
                 hk = h // g
                 bytes_ = n * w.D * 2 * 2 / g + Lq * (w.D * 2 * 2 + 4)
-                units.append(((case.w.kind, (q[b, h], kc[b, hk], vc[b, hk], n, w.scale)), bytes_))
+                units.append(((case.w.kind, (q[b, h], kc[b, hk], vc[b, hk], n, w.scale), case.rope_host), bytes_))
         what = "(b, hq) decode rows" if Lq == 1 else f"(b, hq) decode rows of {Lq} tokens"
     else:
         hosts = [t.float().numpy() for t in case.host[:3]]
@@ -359,7 +375,7 @@ def run_oracle_pool(case, budget_s):
                     qh, kh, vh = hosts[0][a, h], hosts[1][a, hk], hosts[2][a, hk]
                     L = w.L
                 f = 4.0 * w.D * ((L * (L + 1)) // 2 if w.causal else L * L)
-                units.append((("prefill", (qh, kh, vh, w.scale, w.causal)), f))
+                units.append((("prefill", (qh, kh, vh, w.scale, w.causal), case.rope_host), f))
         what = "(sequence, head) prefill problems"
     order = rng.permutation(len(units))
     units = [units[i] for i in order]
@@ -405,6 +421,7 @@ def make_case(name, device):
 def workload_config(case):
     w = case.w
     cfg = {"workload": w.name, "kind": w.kind, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
+           **({"rope": w.extra["rope"]} if w.extra.get("rope") else {}),
            "l2": "flushed between timed steps: a 512 MB buffer written, then read (clean L2; inputs may fit in the 129 MB L2)"}
     if w.kind in ("decode", "decode_multi"):
         if w.kind == "decode_multi":
@@ -621,7 +638,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="decode_gqa")
-    ap.add_argument("--also", default="decode_long,decode_multi_gqa,prefill_causal",
+    ap.add_argument("--also", default="decode_long,decode_multi_gqa,prefill_causal,prefill_causal_rope",
                     help="comma-separated extra workloads measured in the same run (rank 0, N=1 style)")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of host work for cpu_baseline")
     ap.add_argument("--ref-budget", type=float, default=5.0, help="seconds of host work per reference step")
