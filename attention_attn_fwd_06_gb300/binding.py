@@ -54,7 +54,8 @@ _ROPE_STYLES = {"half": ATTN_ROPE_HALF, "interleaved": ATTN_ROPE_INTERLEAVED}
 
 
 class attn_rope(ctypes.Structure):
-    _fields_ = [("cos", ctypes.c_void_p), ("sin", ctypes.c_void_p), ("max_pos", ctypes.c_int), ("style", ctypes.c_int)]
+    _fields_ = [("cos", ctypes.c_void_p), ("sin", ctypes.c_void_p), ("max_pos", ctypes.c_int), ("style", ctypes.c_int),
+                ("k_out", ctypes.c_void_p)]
 
 
 class AttnError(RuntimeError):
@@ -189,10 +190,15 @@ def _need(t, name, dtype, ndim):
 
 
 def _set_rope(p, rope, D, device):
-    """rope = (cos, sin, style): fp32 device tables [max_pos, D/2] and "half" or "interleaved" (None: off)."""
+    """rope = (cos, sin, style) or (cos, sin, style, k_out): fp32 device tables [max_pos, D/2], "half" or
+    "interleaved", and for prefill an optional bf16 tensor shaped like k receiving the rotated keys (None: off)."""
     if rope is None:
         return
-    cos, sin, style = rope
+    cos, sin, style = rope[:3]
+    k_out = rope[3] if len(rope) > 3 else None
+    if k_out is not None:
+        _need(k_out, "rope k_out", torch.bfloat16, k_out.dim())
+        p.rope.k_out = _ptr(k_out)
     for t, name in ((cos, "rope cos"), (sin, "rope sin")):
         _need(t, name, torch.float32, 2)
         if t.device != device or t.shape[1] != D // 2:

@@ -502,6 +502,7 @@ int attn_fwd_ex(const attn_fwd_params* p) {
   if (st != ATTN_OK) return st;
   const bool rope_on = p->rope.style != ATTN_ROPE_NONE && p->rope.cos != nullptr;
   if (rope_on && p->cu_seqlens_q == nullptr && p->Lq > p->Lkv) return ATTN_ERR_INVALID_ARG;
+  if (rope_on && p->rope.k_out != nullptr && !aligned16(p->rope.k_out)) return ATTN_ERR_ALIGNMENT;
   if (is_empty_fwd(p)) return ATTN_OK;
   cudaStream_t stream = static_cast<cudaStream_t>(p->stream);
   DeviceState* s = nullptr;
@@ -510,9 +511,37 @@ int attn_fwd_ex(const attn_fwd_params* p) {
     st = device_state_locked(&s);
   }
   if (st != ATTN_OK) return st;
+  const void* kk = p->k;
+  const bool varlen = p->cu_seqlens_q != nullptr;
+  const long long krows = varlen ? (long long)p->total_k * p->Hkv : (long long)p->B * p->Hkv * p->Lkv;
+  if (rope_on && krows > 0) {
+    // rotate the keys once (into k_out or the workspace), then attend over the rotated copy
+    void* kdst = p->rope.k_out;
+    if (kdst == nullptr) {
+      std::lock_guard<std::mutex> lock(g_mu);
+      st = ensure_workspace_locked(*s, kCounterBytes + (size_t)krows * p->D * 2, stream);
+      if (st != ATTN_OK) return st;
+      kdst = static_cast<char*>(s->ws) + kCounterBytes;
+    }
+    attn::RopeKLaunch R{};
+    R.k = p->k;
+    R.k_out = kdst;
+    R.cu_k = varlen ? p->cu_seqlens_k : nullptr;
+    R.B = p->B;
+    R.Hkv = p->Hkv;
+    R.L = p->Lkv;
+    R.D = p->D;
+    R.total_k = p->total_k;
+    R.rope = rope_args(p->rope);
+    R.status = s->status;
+    R.stream = stream;
+    st = map_cuda(attn::launch_rope_k(R));
+    if (st != ATTN_OK) return st;
+    kk = kdst;
+  }
   attn::PrefillLaunch L{};
   L.q = p->q;
-  L.k = p->k;
+  L.k = kk;
   L.v = p->v;
   L.out = p->out;
   L.lse = p->lse;

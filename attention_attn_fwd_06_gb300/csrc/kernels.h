@@ -94,4 +94,18 @@ struct PrefillLaunch {
 
 cudaError_t launch_prefill(const PrefillLaunch& p);
 
+// Rotary embedding of a prefill call's keys into k_out (same layout as k), once per call.
+struct RopeKLaunch {
+  const void* k;       // bf16 [B, Hkv, L, D] (dense) or [total_k, Hkv, D] (packed)
+  void* k_out;         // bf16, same layout
+  const int* cu_k;     // null for the dense layout; else int32 [B + 1]
+  int B, Hkv, L, D;    // L: keys per sequence (dense)
+  int total_k;         // packed: rows
+  RopeArgs rope;
+  unsigned* status;
+  cudaStream_t stream;
+};
+
+cudaError_t launch_rope_k(const RopeKLaunch& p);
+
 }  // namespace attn

@@ -26,7 +26,12 @@
 //  * per K/V step the MMA warp issues P_A V_j, S_A(j+1), P_B V_j, S_B(j+1):
 //    one tile's softmax runs while the tensor pipe works for the other tile;
 //  * the query tiles of one head launch together (K/V reuse in L2), heaviest
-//    (latest, causal) first.
+//    (latest, causal) first;
+//  * with RoPE (template flag) each softmax thread rotates its own row of the
+//    job's Q tile in shared memory (rope.cuh) and the MMA warp waits for all
+//    of them; the keys arrive already rotated from a pass of their own
+//    (rope_k.cu), since rotating every K tile at every visit would repeat the
+//    work and its table reads for every query tile of the head.
 //
 // Every wait is bounded (common.cuh); on a timeout the CTA records the status,
 // drains its in-flight copies and MMAs, frees TMEM and exits.
@@ -44,14 +49,10 @@ namespace {
 constexpr int BM = 128;  // query rows per tile (TMEM lanes)
 constexpr int BN = 128;  // keys per K/V tile
 constexpr int NQ = 2;    // query tiles per CTA (ping-pong)
-constexpr int kRopeWarps = 2;  // warps that rotate each K tile (RoPE variant only)
-// TMA warp, MMA warp, one 4-warp softmax group per query tile, and with RoPE the K-rotation warps
-template <bool ROPE>
-constexpr int kThreads = 32 * (2 + 4 * NQ + (ROPE ? kRopeWarps : 0));
+constexpr int kThreads = 32 * (2 + 4 * NQ);  // TMA warp, MMA warp, one 4-warp softmax group per query tile
 constexpr int kWarpTMA = 0;
 constexpr int kWarpMMA = 1;
 constexpr int kFirstSoftmaxWarp = 2;
-constexpr int kWarpRope = 2 + 4 * NQ;  // first K-rotation warp
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -63,15 +64,14 @@ struct Cfg {
   static constexpr int TILE_BYTES = BM * D * 2;  // one Q, K or V tile (BM == BN)
   static constexpr int BLOCK_BYTES = BM * 128;   // one 64-column block of a tile
   static constexpr int NSV = (D == 128) ? 2 : 4;  // V ring depth
-  // K ring depth: with RoPE one slot more, so a K tile lands and is rotated well before its S MMAs
-  static constexpr int NSK = NSV + (ROPE ? 1 : 0);
+  static constexpr int NSK = NSV;                  // K ring depth
   static constexpr int OFF_Q = 0;                // NQ query tiles
   static constexpr int OFF_K = OFF_Q + NQ * TILE_BYTES;
   static constexpr int OFF_V = OFF_K + NSK * TILE_BYTES;
   static constexpr int OFF_BAR = OFF_V + NSV * TILE_BYTES;
   // barriers: q_full, q_empty, k_full[NSK], v_full[NSV], k_empty[NSK], v_empty[NSV], s_full[NQ], p_full[NQ],
-  // o_done[NQ], drain, q_ready, k_ready[NSK]
-  static constexpr int NBAR = 2 + 3 * NSK + 2 * NSV + 3 * NQ + 2;
+  // o_done[NQ], drain, q_ready
+  static constexpr int NBAR = 2 + 2 * NSK + 2 * NSV + 3 * NQ + 2;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // tmem address, abort flag
   static constexpr int SMEM_USED = OFF_MISC + 16;
   static constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // slack to align the base to 1024
@@ -99,7 +99,7 @@ struct PrefillArgs {
   int total_items;   // B * Hq * ns
   int total_q, total_k;  // packed layout: rows of q/out and of k/v
   unsigned* status;
-  RopeArgs rope;         // style != 0: q rows rotated by the softmax groups, K tiles by the RoPE warp
+  RopeArgs rope;         // style != 0: the softmax groups rotate their q rows (k arrives rotated)
 };
 
 // One job = one pair of 128-row query tiles of one (sequence, head).
@@ -171,7 +171,7 @@ __device__ __forceinline__ bool make_job(const PrefillArgs& a, int item, int hal
 }
 
 template <int D, bool ROPE>
-__global__ void __launch_bounds__(kThreads<ROPE>, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     prefill_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                        const __grid_constant__ CUtensorMap tmv, const PrefillArgs a) {
   using C = Cfg<D, ROPE>;
@@ -192,7 +192,6 @@ __global__ void __launch_bounds__(kThreads<ROPE>, 1)
   uint64_t* o_done = p_full + NQ;
   uint64_t* drain = o_done + NQ;
   uint64_t* q_ready = drain + 1;    // with RoPE: both Q tiles of the job rotated (one arrival per softmax thread)
-  uint64_t* k_ready = q_ready + 1;  // with RoPE: [NS] the K slot's rows rotated
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
@@ -203,8 +202,7 @@ __global__ void __launch_bounds__(kThreads<ROPE>, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::NBAR; ++i) {
       const bool is_p = (&bars[i] >= p_full) && (&bars[i] < p_full + NQ);
-      const bool is_kr = (&bars[i] >= k_ready) && (&bars[i] < k_ready + C::NSK);
-      mbar_init(&bars[i], is_p ? 128 : (&bars[i] == q_ready ? 128 * NQ : (is_kr ? kRopeWarps : 1)));
+      mbar_init(&bars[i], is_p ? 128 : (&bars[i] == q_ready ? 128 * NQ : 1));
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -252,98 +250,32 @@ __global__ void __launch_bounds__(kThreads<ROPE>, 1)
       int ks = 0, vs = 0;  // K and V steps issued (ring positions)
       int qjobs = 0;       // jobs whose Q was loaded
       bool ok = true;
-      if constexpr (!ROPE) {
-        for (int item = blockIdx.x; ok && item < a.total_items; item += gridDim.x) {
-          for (int half = 0; ok && half < 2; ++half) {
-            Job jb;
-            if (!make_job(a, item, half, jb) || jb.n == 0) continue;
-            if (qjobs > 0 && !mbar_wait(q_empty, (qjobs - 1) & 1, a.status, abort_flag)) {
-              ok = false;
-              break;
-            }
-            issue_q(jb);
-            ++qjobs;
-            for (int j = 0; j < jb.n; ++j) {
-              // K slots free up after the S MMAs, V slots after the P V MMAs: the two rings refill independently
-              if (ks >= C::NSK &&
-                  !mbar_wait(&k_empty[ks % C::NSK], ((ks / C::NSK) - 1) & 1, a.status, abort_flag)) {
-                ok = false;
-                break;
-              }
-              issue_kv(&tmk, Ks, k_full, ks % C::NSK, jb, j);
-              ++ks;
-              if (vs >= C::NSV &&
-                  !mbar_wait(&v_empty[vs % C::NSV], ((vs / C::NSV) - 1) & 1, a.status, abort_flag)) {
-                ok = false;
-                break;
-              }
-              issue_kv(&tmv, Vs, v_full, vs % C::NSV, jb, j);
-              ++vs;
-            }
-          }
-        }
-      } else {
-        // Three cursors walk the same job sequence -- Q loads (each once the previous job's S MMAs have released
-        // the Q tiles), K loads and V loads (each as soon as its ring slot frees) -- and one thread issues
-        // whichever is ready, so K runs ahead of V and the rotation warps get each K tile well before its S MMAs.
-        struct Cursor {
-          int item, part, j;  // item, which of its two jobs, step within the job
-          bool valid;
+      for (int item = blockIdx.x; ok && item < a.total_items; item += gridDim.x) {
+        for (int half = 0; ok && half < 2; ++half) {
           Job jb;
-        };
-        auto seek = [&](Cursor& c) {  // the first job with work at or after (item, part)
-          c.valid = false;
-          c.j = 0;
-          for (; c.item < a.total_items; c.item += gridDim.x, c.part = 0)
-            for (; c.part < 2; ++c.part)
-              if (make_job(a, c.item, c.part, c.jb) && c.jb.n > 0) {
-                c.valid = true;
-                return;
-              }
-        };
-        auto next_job = [&](Cursor& c) {
-          ++c.part;
-          seek(c);
-        };
-        Cursor cq;
-        cq.item = blockIdx.x;
-        cq.part = 0;
-        seek(cq);
-        Cursor ck = cq, cv = cq;
-        uint64_t t_progress = globaltimer_ns();
-        while (cq.valid || ck.valid || cv.valid) {
-          bool progress = false;
-          if (cq.valid && (qjobs == 0 || mbar_try_wait(q_empty, (qjobs - 1) & 1))) {
-            issue_q(cq.jb);
-            ++qjobs;
-            next_job(cq);
-            progress = true;
+          if (!make_job(a, item, half, jb) || jb.n == 0) continue;
+          if (qjobs > 0 && !mbar_wait(q_empty, (qjobs - 1) & 1, a.status, abort_flag)) {
+            ok = false;
+            break;
           }
-          if (ck.valid && (ks < C::NSK || mbar_try_wait(&k_empty[ks % C::NSK], ((ks / C::NSK) - 1) & 1))) {
-            issue_kv(&tmk, Ks, k_full, ks % C::NSK, ck.jb, ck.j);
+          issue_q(jb);
+          ++qjobs;
+          for (int j = 0; j < jb.n; ++j) {
+            // K slots free up after the S MMAs, V slots after the P V MMAs: the two rings refill independently
+            if (ks >= C::NSK &&
+                !mbar_wait(&k_empty[ks % C::NSK], ((ks / C::NSK) - 1) & 1, a.status, abort_flag)) {
+              ok = false;
+              break;
+            }
+            issue_kv(&tmk, Ks, k_full, ks % C::NSK, jb, j);
             ++ks;
-            if (++ck.j == ck.jb.n) next_job(ck);
-            progress = true;
-          }
-          if (cv.valid && (vs < C::NSV || mbar_try_wait(&v_empty[vs % C::NSV], ((vs / C::NSV) - 1) & 1))) {
-            issue_kv(&tmv, Vs, v_full, vs % C::NSV, cv.jb, cv.j);
+            if (vs >= C::NSV &&
+                !mbar_wait(&v_empty[vs % C::NSV], ((vs / C::NSV) - 1) & 1, a.status, abort_flag)) {
+              ok = false;
+              break;
+            }
+            issue_kv(&tmv, Vs, v_full, vs % C::NSV, jb, j);
             ++vs;
-            if (++cv.j == cv.jb.n) next_job(cv);
-            progress = true;
-          }
-          if (progress) {
-            t_progress = globaltimer_ns();
-          } else {
-            if (*abort_flag) {
-              ok = false;
-              break;
-            }
-            if (globaltimer_ns() - t_progress > kWaitLimitNs) {
-              record_status(a.status, ATTN_ERR_DEVICE_TIMEOUT);
-              *abort_flag = 1;
-              ok = false;
-              break;
-            }
           }
         }
       }
@@ -388,7 +320,7 @@ __global__ void __launch_bounds__(kThreads<ROPE>, 1)
           const int g0 = kv;
           // with RoPE, wait for the rotated Q tiles and K slots instead of the raw ones
           if (!mbar_wait(rope ? q_ready : q_full, qjobs & 1, a.status, abort_flag) ||
-              !mbar_wait(rope ? &k_ready[g0 % C::NSK] : &k_full[g0 % C::NSK], (g0 / C::NSK) & 1, a.status,
+              !mbar_wait(&k_full[g0 % C::NSK], (g0 / C::NSK) & 1, a.status,
                          abort_flag)) {
             ok = false;
             break;
@@ -422,7 +354,7 @@ __global__ void __launch_bounds__(kThreads<ROPE>, 1)
               tc::fence_after_sync();
               issue_pv(t, g, j == 0);
               if (j + 1 < jb.nt[t]) {
-                if (!mbar_wait(rope ? &k_ready[(g + 1) % C::NSK] : &k_full[(g + 1) % C::NSK], ((g + 1) / C::NSK) & 1,
+                if (!mbar_wait(&k_full[(g + 1) % C::NSK], ((g + 1) / C::NSK) & 1,
                                a.status, abort_flag)) {
                   ok = false;
                   break;
@@ -444,42 +376,6 @@ __global__ void __launch_bounds__(kThreads<ROPE>, 1)
       // Whatever happened, wait for every MMA issued above before TMEM is released.
       tc::mma_commit(drain);
       mbar_wait(drain, 0, a.status, nullptr);
-    }
-  } else if (ROPE && warp >= kWarpRope) {
-    // ---------------- RoPE: rotate every K tile once it lands (key j of a sequence sits at position j) --------
-    // Each of the kRopeWarps warps takes every kRopeWarps-th row; the K slot is released to the MMA warp when
-    // all of them have arrived.
-    const int rw = warp - kWarpRope;
-    if (rope) {
-      int kv = 0;
-      bool ok = true;
-      for (int item = blockIdx.x; ok && item < a.total_items; item += gridDim.x) {
-        for (int half = 0; ok && half < 2; ++half) {
-          Job jb;
-          if (!make_job(a, item, half, jb) || jb.n == 0) continue;
-          for (int j = 0; j < jb.n; ++j) {
-            const int g = kv + j;
-            const int slot = g % C::NSK;
-            if (!mbar_wait(&k_full[slot], (g / C::NSK) & 1, a.status, abort_flag)) {
-              ok = false;
-              break;
-            }
-            uint8_t* tile = Ks + slot * C::TILE_BYTES;
-#pragma unroll 1
-            for (int r = rw * 32 + lane; r < BN; r += 32 * kRopeWarps) {
-              const int key = j * BN + r;
-              if (key < jb.Lkv_s) {  // rows past the sequence are masked out anyway
-                const size_t off = (size_t)key * (D / 2);
-                rope_rotate_row_sw128<D>(tile, C::BLOCK_BYTES, r, a.rope.cos + off, a.rope.sin + off, a.rope.style);
-              }
-            }
-            fence_proxy_async_smem();  // the rotated rows are read by the tensor cores (async proxy)
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&k_ready[slot]);
-          }
-          kv += jb.n;
-        }
-      }
     }
   } else {
     // ---------------- softmax + correction + epilogue: one thread per query row ----------------
@@ -749,7 +645,7 @@ cudaError_t launch_d(const PrefillLaunch& p) {
   int grid = persistent ? (p.num_sms > 0 ? p.num_sms : 148) : a.total_items;
   if (grid > a.total_items) grid = a.total_items;
   if (grid < 1) grid = 1;
-  prefill_fwd_kernel<D, ROPE><<<grid, kThreads<ROPE>, C::SMEM_ALLOC, p.stream>>>(tmq, tmk, tmv, a);
+  prefill_fwd_kernel<D, ROPE><<<grid, kThreads, C::SMEM_ALLOC, p.stream>>>(tmq, tmk, tmv, a);
   return cudaGetLastError();
 }
 

@@ -75,9 +75,12 @@ typedef enum attn_dtype { ATTN_DTYPE_BF16 = 0, ATTN_DTYPE_F32 = 1 } attn_dtype;
  *   style     ATTN_ROPE_NONE (or cos == NULL): no rotation.
  *
  * Positions follow the causal alignment.  Prefill: key j of a sequence sits
- * at j and query i at Lkv - Lq + i; q and k are rotated as they are loaded
- * (a dense call with Lq > Lkv returns ATTN_ERR_INVALID_ARG; a packed sequence
- * with more queries than keys is flagged ATTN_ERR_DEVICE_BOUNDS).  Decode:
+ * at j and query i at Lkv - Lq + i (a dense call with Lq > Lkv returns
+ * ATTN_ERR_INVALID_ARG; a packed sequence with more queries than keys is
+ * flagged ATTN_ERR_DEVICE_BOUNDS).  The keys are rotated once per call by a
+ * pass of their own into k_out (or the library workspace, grown like the
+ * decode workspace and shared with it), then the attention kernel streams
+ * them; each query tile is rotated where it lands in shared memory.  Decode:
  * only the query is rotated, to kv_len - 1 (token t of attn_decode_multi to
  * kv_len - Lq + t); cached keys must be stored already rotated.  Every
  * position must be below max_pos: calls whose Lkv (prefill) or Lmax (decode)
@@ -90,6 +93,8 @@ typedef struct attn_rope {
   const float* sin;
   int max_pos;
   int style;
+  void* k_out;  /* prefill only, optional: DEVICE bf16 buffer shaped like k (16-byte aligned) that receives the
+                   rotated keys -- e.g. to append them to a KV cache; NULL = the library's workspace holds them */
 } attn_rope;
 
 /*

@@ -1,7 +1,8 @@
 """GPU parity of the fused rotary position embedding against the fp64 oracle.
 
-Prefill rotates q and k as their tiles land (q by the softmax warps, k by a
-dedicated warp); the decode kernels rotate only the query (the cache holds
+Prefill rotates each q tile where it lands (the softmax warps) and the keys
+once per call in a pass of their own (optionally into a caller buffer, which
+is checked too); the decode kernels rotate only the query (the cache holds
 keys already rotated, so any cache contents serve).  Both pair layouts, both
 head dims, Lq < Lkv (queries placed at Lkv - Lq + i), packed sequences, paged
 caches, multi-token decode and the causal prefill workload at full size
@@ -62,6 +63,23 @@ def test_prefill_rope_varlen(style):
     O_ref, lse_ref = oracle.attention_varlen(q, k, v, cu.tolist(), cu.tolist(), 128 ** -0.5, True,
                                              rope=(cos, sin, style))
     assert_attn_close(out.cpu(), lse.cpu(), O_ref, lse_ref)
+
+
+def test_prefill_rope_writes_rotated_keys():
+    # k_out receives the rotated keys (what a serving engine appends to its cache): the oracle's rotation held in
+    # bf16, up to a last-bit difference where fp32 and fp64 arithmetic round to different neighbours
+    q, k, v = make_prefill(2, 4, 2, 300, 300, 128, seed=5)
+    cos, sin, cos_d, sin_d = tables(300, 128)
+    k_out = torch.empty_like(k, device=DEV)
+    O, lse = AB.attn_fwd(q.to(DEV), k.to(DEV), v.to(DEV), causal=True, rope=(cos_d, sin_d, "half", k_out))
+    torch.cuda.synchronize()
+    want = oracle.round_bf16(oracle.rope_rotate(k, np.arange(300), cos, sin, "half"))
+    got = k_out.cpu().double().numpy()
+    ulp = np.abs(want) * 2.0 ** -7 + 1e-30
+    assert np.all(np.abs(got - want) <= ulp), "rotated keys off by more than one bf16 step"
+    assert np.mean(got != want) < 1e-3
+    O_ref, lse_ref = oracle.attention(q, k, v, 128 ** -0.5, True, rope=(cos, sin, "half"))
+    assert_attn_close(O.cpu(), lse.cpu(), O_ref, lse_ref)
 
 
 def test_prefill_rope_rejects_short_tables():
