@@ -426,7 +426,8 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS, DecodeCfg<D, GP>::M
 
 #pragma unroll 1
     for (int it = 0; it < C::ITER; ++it) {
-      const int kb = warp * C::KPW + it * C::KPI;
+      // key groups of KPI keys go round-robin over the warps, so a short last stage of a piece still spreads
+      const int kb = (it * C::NW + warp) * C::KPI;
       if (kb >= nk) break;  // warp-uniform
 
       // Load this iteration's K and V rows up front so the V latency hides behind the reductions.
