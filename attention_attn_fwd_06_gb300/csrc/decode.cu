@@ -52,8 +52,9 @@ namespace {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 // Cost, in keys, charged to every row with keys when the key space is split: the piece-end work of a row
-// (warp merge, output or partial, publish) takes about as long as streaming one 64-key stage.
-constexpr int kRowCost = 64;
+// (warp merge, output or partial, publish, a possible merge of the row) takes about as long as streaming three
+// 64-key stages (a sweep of 64 to 256 on the 8 x 4096 GQA workload put the shortest calls at 192 and above).
+constexpr int kRowCost = 192;
 
 template <int D, int GP>
 struct DecodeCfg {
