@@ -117,8 +117,9 @@ struct Piece {
 };
 
 // Cost, in tiles, charged to every item with keys when the tile space is split: its piece-end work
-// (epilogue or partial, publish) takes about as long as streaming one K/V tile.
-constexpr int kItemCost = 1;
+// (epilogue or partial, publish, a possible merge) takes about as long as streaming two K/V tiles (a sweep of
+// 0 to 3 on the 8-token GQA workload put the shortest calls at 2 and 3).
+constexpr int kItemCost = 2;
 
 // Walks this CTA's share [lo, hi) of the flattened cost space.  Item (b, hk) occupies [start, start + kItemCost
 // + T): its tiles are the last T positions, so a share that takes on an item start also takes fewer tiles, and a
