@@ -15,13 +15,14 @@
 // GB300 design:
 //  * Stream-K split: persistent CTAs (three per SM; two with 8 heads per CTA) each take an equal,
 //    contiguous slice of the flattened key space of all (b, kv head, head
-//    group) rows, so every CTA streams the same number of bytes whatever the
+//    group) rows -- each row also charged a fixed cost for its piece-end
+//    work -- so every CTA streams about the same number of bytes whatever the
 //    mix of sequence lengths, and there are no waves and no work-queue
 //    atomics.  A slice covers the tail of one row, whole rows, and the head of
 //    another; only the first and last pieces of a slice can be partial rows.
 //    One CTA serves ALL the query heads of its group, so every K/V byte is
-//    read from HBM once (the decoder page's "load each K/V block once, reuse it
-//    for all queries of the step").
+//    read from HBM once (the decoder page's fused kernel loads each K/V block
+//    once and reuses it for every query of the step).
 //  * A producer warp walks the slice and streams K and V rows (contiguous
 //    cache, or pages of a paged cache through its block table) (and, on a row
 //    piece's first stage, its q vectors) into a shared-memory ring (2-3 stages)

@@ -274,7 +274,8 @@ class PrefillCase(_RopeMixin):
         self.unit, self.kind = "TFLOP/s", "tensor"
         self.kernel = "prefill_fwd"
         self.kernel_desc = "prefill_fwd_kernel (one attn_fwd call, event-timed)"
-        self.launches_per_step = 1
+        # with RoPE a call launches the key-rotation pass, then the attention kernel
+        self.launches_per_step = 2 if self.rope_style else 1
         self.h2d = sum(t.numel() * t.element_size() for t in self.host)
         self.d2h = self.out.numel() * self.out.element_size() + self.lse.numel() * 4
 

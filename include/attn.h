@@ -177,9 +177,11 @@ int attn_fwd_ex(const attn_fwd_params* p);
  * ATTN_ERR_INVALID_ARG: make one uncaptured call with the largest sizes
  * first).  Decode calls on one device share that workspace, so calls that can
  * overlap on the GPU (different streams with no ordering) race on it.
- * One kernel is enqueued: persistent CTAs (two per SM) each stream an equal
- * slice of the flattened key space of all rows, and the CTA that lands a
- * row's last partial merges that row's partials.
+ * One kernel is enqueued: persistent CTAs (three per SM when a CTA serves up
+ * to 4 query heads, two with 8) each stream an equal slice of the flattened
+ * key space of all rows (every row also charged a fixed cost for its
+ * piece-end work), and the CTA that lands a row's last partial merges that
+ * row's partials.
  */
 int attn_decode(const void* q, const void* kcache, const void* vcache, const int* kv_lens,
                 void* out, float* lse, int B, int Hq, int Hkv, int Lmax, int D, float scale,
