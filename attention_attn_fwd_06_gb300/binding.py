@@ -43,6 +43,7 @@ EXPORTED = (
     "attn_get_device_status",
     "attn_status_string",
     "attn_release_workspace",
+    "attn_selftest_wait_timeout",
     "attn_version",
 )
 
@@ -151,6 +152,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.attn_status_string.restype = ctypes.c_char_p
         lib.attn_release_workspace.argtypes = []
         lib.attn_release_workspace.restype = None
+        lib.attn_selftest_wait_timeout.argtypes = [ctypes.c_uint, P]
+        lib.attn_selftest_wait_timeout.restype = I
         lib.attn_version.argtypes = []
         lib.attn_version.restype = I
         _lib = lib
@@ -431,3 +434,10 @@ def attn_release_workspace():
 
 def attn_version() -> int:
     return int(load().attn_version())
+
+
+def attn_selftest_wait_timeout(limit_us=1000, stream=None):
+    """Run the bounded-wait timeout path on the current device (no fault): afterwards the device status word
+    holds ATTN_ERR_DEVICE_TIMEOUT."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    _check(load().attn_selftest_wait_timeout(int(limit_us), _stream_handle(stream, dev)), "attn_selftest_wait_timeout")

@@ -216,6 +216,19 @@ extern "C" {
 
 int attn_version(void) { return 100; }
 
+int attn_selftest_wait_timeout(unsigned int limit_us, void* stream) {
+  if (limit_us < 1 || limit_us > 1000000) return ATTN_ERR_INVALID_ARG;
+  DeviceState* s = nullptr;
+  int st;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    st = device_state_locked(&s);
+  }
+  if (st != ATTN_OK) return st;
+  return map_cuda(attn::launch_selftest_timeout((unsigned long long)limit_us * 1000ull, s->status,
+                                                static_cast<cudaStream_t>(stream)));
+}
+
 const char* attn_status_string(int status) {
   switch (status) {
     case ATTN_OK: return "ATTN_OK";

@@ -71,13 +71,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // returns false (and raises *abort) when the limit expires or another thread of
 // the CTA has already aborted.  `abort` may be null (then only the timer stops it).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned* status,
-                                          volatile int* abort) {
+                                          volatile int* abort, uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (abort != nullptr && *abort) return false;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (globaltimer_ns() - t0 > limit_ns) {
       record_status(status, ATTN_ERR_DEVICE_TIMEOUT);
       if (abort != nullptr) *abort = 1;
       return false;

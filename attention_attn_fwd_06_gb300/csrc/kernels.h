@@ -108,4 +108,7 @@ struct RopeKLaunch {
 
 cudaError_t launch_rope_k(const RopeKLaunch& p);
 
+// One thread waits on a barrier nothing arrives on, with the kernels' bounded wait and a limit of limit_ns.
+cudaError_t launch_selftest_timeout(unsigned long long limit_ns, unsigned* status, cudaStream_t stream);
+
 }  // namespace attn

@@ -58,6 +58,8 @@ WORKLOADS = {
                  kv_lens=(32768, 65536, 98304, 131072)),
         Workload("decode_multi_gqa", "decode_multi", 1006, B=8, Hq=32, Hkv=8, D=128, L=4096, Lq=8,
                  kv_range=(512, 4096)),
+        Workload("decode_multi_long", "decode_multi", 1007, B=4, Hq=32, Hkv=8, D=128, L=131072, Lq=8,
+                 kv_lens=(32768, 65536, 98304, 131072)),
         Workload("prefill_causal", "prefill", 1003, B=4, Hq=32, Hkv=32, D=128, L=4096, causal=True),
         Workload("prefill_causal_rope", "prefill", 1003, B=4, Hq=32, Hkv=32, D=128, L=4096, causal=True,
                  extra={"rope": "half"}),

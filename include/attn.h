@@ -364,6 +364,19 @@ void attn_release_workspace(void);
  */
 int attn_decode_noalloc(const attn_decode_params* p);
 
+/*
+ * attn_selftest_wait_timeout -- exercises the failure detection every kernel
+ * carries, without a GPU fault.  (The pages have no counterpart; it exists so
+ * that the device-timeout path can be tested.)  Enqueues a one-thread kernel
+ * that waits on an mbarrier nothing arrives on, using the same bounded wait
+ * as every pipeline stage but a limit of limit_us microseconds (1 .. 1000000);
+ * when it expires the kernel records ATTN_ERR_DEVICE_TIMEOUT in the device
+ * status word, exactly as a stalled pipeline would, and returns.  The context
+ * stays usable; attn_get_device_status() then reports and clears the status.
+ * Returns ATTN_ERR_INVALID_ARG for a limit out of range.
+ */
+int attn_selftest_wait_timeout(unsigned int limit_us, void* stream);
+
 /* attn_version -- library version as major*10000 + minor*100 + patch. */
 int attn_version(void);
 

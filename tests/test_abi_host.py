@@ -150,6 +150,11 @@ def test_decode_multi_validation(lib, kw, code):
     assert multi(lib, **kw) == code
 
 
+def test_selftest_limit_validation(lib):
+    assert lib.attn_selftest_wait_timeout(0, None) == B.ATTN_ERR_INVALID_ARG
+    assert lib.attn_selftest_wait_timeout(2000000, None) == B.ATTN_ERR_INVALID_ARG
+
+
 def test_empty_inputs_are_noops(lib):
     assert fwd(lib, B=0) == B.ATTN_OK
     assert fwd(lib, Lq=0) == B.ATTN_OK

@@ -198,3 +198,18 @@ def test_decode_paged_bad_page_id_is_flagged():
     AB.attn_decode_paged(q.to(dev), kp.to(dev), vp.to(dev), table.to(dev), lens.to(dev))
     assert AB.attn_get_device_status() == AB.ATTN_ERR_DEVICE_BOUNDS
     assert AB.attn_get_device_status() == AB.ATTN_OK
+
+
+def test_device_timeout_is_reported_and_context_survives():
+    # The bounded wait every pipeline stage uses, run out on purpose (a barrier nothing arrives on, 2 ms limit):
+    # the status word reports the timeout, and the next call works normally.
+    AB.attn_get_device_status()
+    AB.attn_selftest_wait_timeout(2000)
+    assert AB.attn_get_device_status() == AB.ATTN_ERR_DEVICE_TIMEOUT
+    assert AB.attn_get_device_status() == AB.ATTN_OK  # read-and-clear
+    q, kc, vc, _ = make_decode(2, 8, 2, 300, 128, seed=9)
+    lens = [300, 120]
+    O, lse = run(q, kc, vc, torch.tensor(lens, dtype=torch.int32), 0.088)
+    O_ref, lse_ref = oracle.decode(q, kc, vc, lens, 0.088)
+    assert_attn_close(O, lse, O_ref, lse_ref)
+    assert AB.attn_get_device_status() == AB.ATTN_OK

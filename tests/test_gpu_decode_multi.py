@@ -7,7 +7,8 @@ exact tile multiples, one past them, shorter than a tile, shorter than Lq
 (tokens that see no key) and zero, one long sequence split over every CTA
 (many partials per item, merged in the kernel), fp32 output, logits peaked
 enough to force the O rescale, determinism, Lq = 1 against the single-token
-decode, and the multi-token workload at full size on sampled heads.
+decode, and both multi-token workloads (8 x 4096 and 131k keys) at full size on
+sampled heads.
 """
 import numpy as np
 import pytest
@@ -139,6 +140,18 @@ def test_decode_multi_workload_sampled():
     assert torch.isfinite(O.float()).all() and torch.isfinite(lse).all()
     rng = np.random.default_rng(5)
     heads = [(b, int(h)) for b in range(w.B) for h in rng.choice(w.Hq, 4, replace=False)]
+    O_ref, lse_ref = oracle.decode_multi(q, kc, vc, lens.tolist(), w.scale, heads=heads)
+    idx_b = [b for b, _ in heads]
+    idx_h = [h for _, h in heads]
+    assert_attn_close(O[idx_b, idx_h], lse[idx_b, idx_h], O_ref[idx_b, idx_h], lse_ref[idx_b, idx_h])
+
+
+def test_decode_multi_long_workload_sampled():
+    w = WORKLOADS["decode_multi_long"]
+    q, kc, vc, lens = make_decode_multi(w.B, w.Hq, w.Hkv, w.Lq, w.L, w.D, w.seed, kv_lens=w.kv_lens)
+    O, lse = run(q, kc, vc, lens.tolist())
+    assert torch.isfinite(O.float()).all() and torch.isfinite(lse).all()
+    heads = [(b, h) for b in range(w.B) for h in (0, 13, 31)]
     O_ref, lse_ref = oracle.decode_multi(q, kc, vc, lens.tolist(), w.scale, heads=heads)
     idx_b = [b for b, _ in heads]
     idx_h = [h for _, h in heads]
