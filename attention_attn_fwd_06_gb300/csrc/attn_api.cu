@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 #include "../../include/attn.h"
@@ -44,6 +46,14 @@ __device__ __align__(256) float g_noalloc_scratch[kNoAllocScratchBytes / sizeof(
 float* g_noalloc_ptr[kMaxDevices] = {};
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ATTN_FAULT_INJECT=skip_arrive (read at each decode call): the decode kernel's CTA 0 withholds one pipeline-slot
+// release, so its producer's bounded wait runs out and ATTN_ERR_DEVICE_TIMEOUT is recorded -- a test of the
+// failure path on a real kernel that neither faults nor hangs the GPU.
+int fault_skip_arrive() {
+  const char* v = std::getenv("ATTN_FAULT_INJECT");
+  return (v != nullptr && std::strcmp(v, "skip_arrive") == 0) ? 1 : 0;
+}
 bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
 // Looks up (and on first use probes) the current device.  Caller holds g_mu.
@@ -294,6 +304,7 @@ int attn_decode_ex(const attn_decode_params* p) {
   L.scale = p->scale;
   L.out_f32 = p->out_dtype == ATTN_DTYPE_F32;
   L.status = s->status;
+  L.fault_skip_arrive = fault_skip_arrive();
   L.rope = rope_args(p->rope);
   L.stream = stream;
   return map_cuda(attn::launch_decode(L, s->num_sms));
@@ -350,6 +361,7 @@ int attn_decode_noalloc(const attn_decode_params* p) {
   L.scale = p->scale;
   L.out_f32 = p->out_dtype == ATTN_DTYPE_F32;
   L.status = s->status;
+  L.fault_skip_arrive = fault_skip_arrive();
   L.rope = rope_args(p->rope);
   L.stream = static_cast<cudaStream_t>(p->stream);
   return map_cuda(attn::launch_decode(L, s->num_sms));
@@ -418,6 +430,7 @@ int attn_decode_paged(const attn_decode_paged_params* pp) {
   L.scale = p.scale;
   L.out_f32 = p.out_dtype == ATTN_DTYPE_F32;
   L.status = s->status;
+  L.fault_skip_arrive = fault_skip_arrive();
   L.rope = rope_args(p.rope);
   L.stream = stream;
   return map_cuda(attn::launch_decode(L, s->num_sms));

@@ -33,6 +33,7 @@ struct DecodeLaunch {
   int out_f32;
   unsigned* status;     // device status word
   RopeArgs rope;        // rotates q (to kv_len - 1) when style != 0
+  int fault_skip_arrive;  // test hook: CTA 0 withholds one slot release, so a bounded wait runs out
   cudaStream_t stream;
 };
 

@@ -213,3 +213,22 @@ def test_device_timeout_is_reported_and_context_survives():
     O_ref, lse_ref = oracle.decode(q, kc, vc, lens, 0.088)
     assert_attn_close(O, lse, O_ref, lse_ref)
     assert AB.attn_get_device_status() == AB.ATTN_OK
+
+
+def test_fault_injection_skip_arrive_times_out_and_recovers(monkeypatch):
+    # ATTN_FAULT_INJECT=skip_arrive: CTA 0 withholds one pipeline-slot release, its producer's bounded wait runs
+    # out (about a second), the status word reports the timeout, and the next clean call is correct.
+    w = WORKLOADS["decode_gqa"]
+    q, kc, vc, lens = make_decode(w.B, w.Hq, w.Hkv, w.L, w.D, w.seed, kv_range=w.kv_range)
+    AB.attn_get_device_status()
+    monkeypatch.setenv("ATTN_FAULT_INJECT", "skip_arrive")
+    run(q, kc, vc, lens, w.scale)
+    assert AB.attn_get_device_status() == AB.ATTN_ERR_DEVICE_TIMEOUT
+    monkeypatch.delenv("ATTN_FAULT_INJECT")
+    O, lse = run(q, kc, vc, lens, w.scale)
+    assert AB.attn_get_device_status() == AB.ATTN_OK
+    heads = [(b, h) for b in range(w.B) for h in (0, 31)]
+    O_ref, lse_ref = oracle.decode(q, kc, vc, lens.tolist(), w.scale, heads=heads)
+    idx_b = [b for b, _ in heads]
+    idx_h = [h for _, h in heads]
+    assert_attn_close(O[idx_b, idx_h], lse[idx_b, idx_h], O_ref[idx_b, idx_h], lse_ref[idx_b, idx_h])
