@@ -485,11 +485,13 @@ def barrier():
 
 
 def max_over_ranks(x: float) -> float:
+    """The largest of every rank's value (the slowest replica sets the job's time)."""
     if _dist is None:
         return x
     import torch
 
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    device = "cuda" if _dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=device)
     _dist.all_reduce(t, op=_dist.ReduceOp.MAX)
     return float(t.item())
 
