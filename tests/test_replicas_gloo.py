@@ -42,7 +42,7 @@ def _rank_main(rank, world, port, out):
 
 def test_two_gloo_ranks_reduce_to_the_slowest():
     world, port = 2, _free_port()
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:
         out = m.dict()
         mp.spawn(_rank_main, args=(world, port, out), nprocs=world, join=True)
         assert dict(out) == {0: 2.5, 1: 2.5}
