@@ -290,24 +290,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kWarpMMA) {
     // ---------------- MMA issuer: S_A, S_B, then per step PV_A, S_A', PV_B, S_B' ----------------
     if (lane == 0) {
+      // Descriptor low halves of the first Q, K and V tiles; every MMA below only adds a constant offset.
+      const uint32_t q_lo = tc::sw128_desc_lo(smem_u32(Qs), 16);
+      const uint32_t k_lo = tc::sw128_desc_lo(smem_u32(Ks), 16);
+      const uint32_t v_lo = tc::sw128_desc_lo(smem_u32(Vs), C::BLOCK_BYTES);
+      constexpr uint32_t kHi = tc::sw128_desc_hi(1024);
+      constexpr uint32_t kTile16 = C::TILE_BYTES >> 4;
       auto issue_s = [&](int t, int g) {
-        const uint32_t q_addr = smem_u32(Qs + t * C::TILE_BYTES);
-        const uint32_t k_addr = smem_u32(Ks + (g % C::NSK) * C::TILE_BYTES);
+        const uint32_t qa = q_lo + t * kTile16;
+        const uint32_t ka = k_lo + (g % C::NSK) * kTile16;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t koff = (kk >> 2) * C::BLOCK_BYTES + (kk & 3) * 32;
-          tc::mma_ss(tbase + C::tm_s(t), tc::smem_desc_sw128(q_addr + koff, 16, 1024),
-                     tc::smem_desc_sw128(k_addr + koff, 16, 1024), C::IDESC_S, kk > 0);
+          const uint32_t koff = ((kk >> 2) * C::BLOCK_BYTES + (kk & 3) * 32) >> 4;
+          tc::mma_ss(tbase + C::tm_s(t), tc::desc64(qa + koff, kHi), tc::desc64(ka + koff, kHi), C::IDESC_S, kk > 0);
         }
         tc::mma_commit(&s_full[t]);
       };
       auto issue_pv = [&](int t, int g, bool first) {
-        const uint32_t v_addr = smem_u32(Vs + (g % C::NSV) * C::TILE_BYTES);
+        const uint32_t va = v_lo + (g % C::NSV) * kTile16;
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
-          tc::mma_ts(tbase + C::tm_o(t), tbase + C::tm_s(t) + kk * 8,
-                     tc::smem_desc_sw128(v_addr + kk * 2048, C::BLOCK_BYTES, 1024), C::IDESC_O,
-                     (!first || kk > 0) ? 1u : 0u);
+          tc::mma_ts(tbase + C::tm_o(t), tbase + C::tm_s(t) + kk * 8, tc::desc64(va + kk * (2048 >> 4), kHi),
+                     C::IDESC_O, (!first || kk > 0) ? 1u : 0u);
         tc::mma_commit(&o_done[t]);
       };
       int kv = 0, qjobs = 0;
@@ -464,8 +468,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             l *= alpha;
           }
           // p = 2^(s*c - m_ref): exponent arguments and row sums on packed fp32x2 FMAs/adds
+          // m_ref stays -inf only while every score so far is -inf (masked); then x = -inf and p = 0 with no
+          // special case
           const float neg = (m_ref == -INFINITY) ? 0.f : -m_ref;
-          const bool live = m_ref != -INFINITY;
           const float2 c2 = make_float2(c, c), n2 = make_float2(neg, neg);
           float2 rs[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
           uint32_t pk[2][32];
@@ -475,8 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 16; ++i) {
               const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[cc][2 * i]), __uint_as_float(sr[cc][2 * i + 1])),
                                           c2, n2);
-              float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-              if (!live) pp = make_float2(0.f, 0.f);
+              const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
               rs[i & 1] = __fadd2_rn(rs[i & 1], pp);
               pk[cc >> 1][(cc & 1) * 16 + i] = tc::pack_bf16x2(pp.x, pp.y);
             }

@@ -47,6 +47,19 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
   return d;
 }
 
+// The same descriptor as two 32-bit halves.  The start-address field lies in the low half, so adding
+// (byte offset >> 4) to the low half moves a descriptor within shared memory (every shared address is below
+// 256 KB, so the 14-bit field never carries into the leading-offset field): one integer add per MMA instead
+// of rebuilding the 64-bit word, which matters when the issuing thread shares its SM sub-partition with
+// busy softmax warps.
+__device__ __forceinline__ uint32_t sw128_desc_lo(uint32_t saddr, uint32_t lbo_bytes) {
+  return ((saddr >> 4) & 0x3FFFu) | (((lbo_bytes >> 4) & 0x3FFFu) << 16);
+}
+__host__ __device__ constexpr uint32_t sw128_desc_hi(uint32_t sbo_bytes) {
+  return ((sbo_bytes >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
+}
+__device__ __forceinline__ uint64_t desc64(uint32_t lo, uint32_t hi) { return ((uint64_t)hi << 32) | lo; }
+
 // Instruction descriptor for kind::f16 with bf16 A and B and an fp32 accumulator.
 //   bits 4-5 D format (1 = f32), 7-9 A format (1 = bf16), 10-12 B format (1 = bf16),
 //   bit 15 A major (0 = K-major), bit 16 B major (0 = K-major, 1 = MN-major),

@@ -9,15 +9,21 @@ decode HBM-bandwidth metric is quoted on.  One step = one ``attn_decode`` call
 prefill_causal | prefill_ragged_gqa | prefill_noncausal_d64 | tiny_causal``
 (``decode_multi_gqa``: 8 new tokens per sequence through ``attn_decode_multi``).
 
-Timing: inputs resident in HBM; W untimed warm-up steps; then exactly K
-steps, each bracketed by CUDA events on the launching stream, with a write
-and then a read of a 512 MB buffer (> the 129 MB L2) between steps, so every
-step reads K/V from HBM and finds no dirty lines of the flush left to write
-back; barrier + synchronize on both sides; max over ranks.  ``value`` is
+Timing: inputs resident in HBM; the case keeps enough copies of its inputs
+and outputs that every step reads a copy no step has touched for at least
+4x the L2 size (129 MB) of other traffic, so no step finds its K/V in L2 and
+no flush is needed.  W untimed warm-up steps; then exactly K steps, cycling
+the copies, captured as one CUDA graph; after a few untimed replays of that
+graph, one replay is timed by a pair of CUDA events on the launching stream;
+barrier + synchronize on both sides; max over ranks.  ``value`` is
 algorithmic bytes (decode: K/V rows actually attended, plus q, O and lse) or
 algorithmic FLOPs (prefill: 4*D per visible query/key pair) per second.
+``per_launch_flushed`` repeats the measurement one launch at a time, each
+between its own pair of events with a 512 MB write-then-read L2 flush before
+it (it includes the per-launch event and launch floor).
 ``e2e`` repeats the measurement through the same call with the inputs copied
-from pinned host memory and the outputs copied back inside the timed region.
+from pinned host memory and the outputs copied back inside the timed region
+(one call at a time, L2 flushed before each).
 ``cpu_baseline`` times the fp64 oracle on a bounded sample on the host cores.
 
 ``--impl reference`` times that oracle alone (the only reference this
@@ -43,6 +49,7 @@ if ROOT not in sys.path:
 
 METRIC = "decode attn HBM GB/s (% of peak); prefill attn TFLOP/s (% of tensor peak)"
 FLUSH_BYTES = 512 << 20
+L2_BYTES = 129 * 10**6  # GB300 L2; the device property is used when it reports more
 HBM_FALLBACK_GBS = 6800.0
 BF16_FALLBACK_TFLOPS = 1900.0
 
@@ -132,9 +139,9 @@ class ClockSampler:
             except Exception:
                 self.proc.kill()
 
-    def summary(self, t0, t1):
+    def summary(self, t0, t1, label="timed"):
         inside = [s for s in self.samples if t0 <= s[0] <= t1]
-        window = "timed"
+        window = label
         if not inside:
             inside = [s for s in self.samples if s[0] <= t1 + 0.5]
             window = "warmup+timed (the timed region was shorter than the sampling interval)"
@@ -155,6 +162,42 @@ def _pin(t):
     return t.pin_memory() if torch.cuda.is_available() else t
 
 
+class _Rotation:
+    """Copies of a workload's inputs (and outputs) cycled by ``step``, so that consecutive steps read different
+    addresses: with enough copies every step finds its inputs evicted from L2 by the steps in between."""
+
+    def _init_sets(self):
+        self.sets = [(self.dev, self.out, self.lse)]
+        self._next = 0
+
+    def rotate_inputs(self, l2_bytes):
+        """Enough copies that (copies - 1) steps of other traffic cover at least 4x L2; returns the count."""
+        import torch
+
+        n = max(2, math.ceil(4 * l2_bytes / self.touch_bytes) + 1)
+        self.sets = [(self.dev, self.out, self.lse)] + [
+            ([t.clone() for t in self.dev], torch.empty_like(self.out), torch.empty_like(self.lse))
+            for _ in range(n - 1)]
+        self._next = 0
+        return n
+
+    def set_bytes(self):
+        dev, out, lse = self.sets[0]
+        return sum(t.numel() * t.element_size() for t in dev) + out.numel() * out.element_size() + lse.numel() * 4
+
+    def step(self):
+        dev, out, lse = self.sets[self._next]
+        self._next = (self._next + 1) % len(self.sets)
+        self._call(dev, out, lse)
+
+    def step_e2e(self):
+        for d, h in zip(self.dev, self.host):
+            d.copy_(h, non_blocking=True)
+        self._call(self.dev, self.out, self.lse)
+        self.out_h.copy_(self.out, non_blocking=True)
+        self.lse_h.copy_(self.lse, non_blocking=True)
+
+
 class _RopeMixin:
     def _rope_setup(self, w, max_pos, device):
         """RoPE tables (model constants: resident on the device, not copied per step) when the workload asks."""
@@ -168,7 +211,7 @@ class _RopeMixin:
             self.rope_dev = (cos.to(device), sin.to(device), self.rope_style)
 
 
-class DecodeCase(_RopeMixin):
+class DecodeCase(_Rotation, _RopeMixin):
     def __init__(self, w, device):
         import torch
 
@@ -205,6 +248,8 @@ class DecodeCase(_RopeMixin):
         rows = w.B * w.Hq * self.Lq
         self.alg_bytes = kv_bytes + rows * w.D * 2 * 2 + rows * 4
         self.work = self.alg_bytes
+        self.touch_bytes = self.alg_bytes  # bytes one step reads and writes
+        self._init_sets()
         self.unit, self.kind = "GB/s", "hbm"
         self.kernel = "decode_multi" if self.multi else "decode_split"
         self.kernel_desc = ("decode_multi_kernel (one attn_decode_multi call: tcgen05 split pass with the merge fused, "
@@ -214,36 +259,26 @@ class DecodeCase(_RopeMixin):
         self.h2d = sum(t.numel() * t.element_size() for t in self.host)
         self.d2h = self.out.numel() * 2 + self.lse.numel() * 4
 
-    def _call(self):
+    def _call(self, dev, out, lse):
         from attention_attn_fwd_06_gb300 import binding as AB
 
         r = self.rope_dev
         if self.page_size:
-            q, kp, vp, lens, table = self.dev
-            AB.attn_decode_paged(q, kp, vp, table, lens, out=self.out, lse=self.lse, scale=self.w.scale, rope=r)
+            q, kp, vp, lens, table = dev
+            AB.attn_decode_paged(q, kp, vp, table, lens, out=out, lse=lse, scale=self.w.scale, rope=r)
         elif self.multi:
-            q, kc, vc, lens = self.dev
-            AB.attn_decode_multi(q, kc, vc, lens, out=self.out, lse=self.lse, scale=self.w.scale, rope=r)
+            q, kc, vc, lens = dev
+            AB.attn_decode_multi(q, kc, vc, lens, out=out, lse=lse, scale=self.w.scale, rope=r)
         else:
-            q, kc, vc, lens = self.dev
-            AB.attn_decode(q, kc, vc, lens, out=self.out, lse=self.lse, scale=self.w.scale, rope=r)
-
-    def step(self):
-        self._call()
-
-    def step_e2e(self):
-        for d, h in zip(self.dev, self.host):
-            d.copy_(h, non_blocking=True)
-        self._call()
-        self.out_h.copy_(self.out, non_blocking=True)
-        self.lse_h.copy_(self.lse, non_blocking=True)
+            q, kc, vc, lens = dev
+            AB.attn_decode(q, kc, vc, lens, out=out, lse=lse, scale=self.w.scale, rope=r)
 
     def oracle_sample(self, budget_s):
         """(work units done, seconds, cores, description) for the fp64 oracle on a bounded sample."""
         return run_oracle_pool(self, budget_s)
 
 
-class PrefillCase(_RopeMixin):
+class PrefillCase(_Rotation, _RopeMixin):
     def __init__(self, w, device):
         import torch
 
@@ -278,32 +313,24 @@ class PrefillCase(_RopeMixin):
         self.launches_per_step = 2 if self.rope_style else 1
         self.h2d = sum(t.numel() * t.element_size() for t in self.host)
         self.d2h = self.out.numel() * self.out.element_size() + self.lse.numel() * 4
+        self.touch_bytes = self.h2d + self.d2h  # q, k, v read and O, lse written once per step (at least)
+        self._init_sets()
 
-    def _call(self):
+    def _call(self, dev, out, lse):
         import torch
 
         from attention_attn_fwd_06_gb300 import binding as AB
 
         w = self.w
         if w.kind == "varlen":
-            q, k, v, cu = self.dev
+            q, k, v, cu = dev
             mx = max(self.seqlens)
-            AB.attn_fwd_varlen(q, k, v, cu, cu, mx, mx, out=self.out, lse=self.lse, causal=w.causal, scale=w.scale,
+            AB.attn_fwd_varlen(q, k, v, cu, cu, mx, mx, out=out, lse=lse, causal=w.causal, scale=w.scale,
                                rope=self.rope_dev)
         else:
-            q, k, v = self.dev
-            AB.attn_fwd(q, k, v, out=self.out, lse=self.lse, causal=w.causal, scale=w.scale,
+            q, k, v = dev
+            AB.attn_fwd(q, k, v, out=out, lse=lse, causal=w.causal, scale=w.scale,
                         out_dtype=torch.float32 if w.out_f32 else torch.bfloat16, rope=self.rope_dev)
-
-    def step(self):
-        self._call()
-
-    def step_e2e(self):
-        for d, h in zip(self.dev, self.host):
-            d.copy_(h, non_blocking=True)
-        self._call()
-        self.out_h.copy_(self.out, non_blocking=True)
-        self.lse_h.copy_(self.lse, non_blocking=True)
 
     def oracle_sample(self, budget_s):
         return run_oracle_pool(self, budget_s)
@@ -423,7 +450,7 @@ def workload_config(case):
     w = case.w
     cfg = {"workload": w.name, "kind": w.kind, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
            **({"rope": w.extra["rope"]} if w.extra.get("rope") else {}),
-           "l2": "flushed between timed steps: a 512 MB buffer written, then read (clean L2; inputs may fit in the 129 MB L2)"}
+           "l2": l2_note(case)}
     if w.kind in ("decode", "decode_multi"):
         if w.kind == "decode_multi":
             cfg["Lq"] = w.Lq
@@ -439,6 +466,16 @@ def workload_config(case):
     return cfg
 
 
+def l2_note(case):
+    n = len(case.sets)
+    if n == 1:
+        return "flushed between timed steps: a 512 MB buffer written, then read"
+    return (f"not flushed: inputs larger than L2 -- {n} copies of the inputs and outputs ({n * case.set_bytes() / 1e9:.2f} "
+            f"GB) cycled step by step, so each step reads a copy last touched {n - 1} steps "
+            f"({(n - 1) * case.touch_bytes / 1e6:.0f} MB of other traffic, >= 4x the 129 MB L2) earlier; the K steps "
+            f"run back to back as one CUDA graph replay between one pair of CUDA events")
+
+
 def flush_l2(flush):
     """Evict the inputs from L2: write a buffer larger than L2, then read it back.
 
@@ -451,6 +488,7 @@ def flush_l2(flush):
 
 
 def time_steps(case, steps, warmup, flush, e2e=False):
+    """Each step a launch between its own pair of CUDA events, L2 flushed before it (the per-launch view)."""
     import torch
 
     fn = case.step_e2e if e2e else case.step
@@ -474,6 +512,51 @@ def time_steps(case, steps, warmup, flush, e2e=False):
     t_wall1 = time.time()
     ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     return sum(ms), ms, t_wall0, t_wall1
+
+
+def l2_bytes(device):
+    import torch
+
+    return max(int(getattr(torch.cuda.get_device_properties(device), "L2_cache_size", 0)), L2_BYTES)
+
+
+def time_graph(case, steps, warmup, load_s=0.3):
+    """K steps back to back, cycling the case's input copies, captured as one CUDA graph; one replay is timed
+    by one pair of CUDA events.  W eager warm-up steps come first (they also size the library workspace, so
+    the captured calls allocate nothing), then untimed replays of the same graph for ``load_s`` seconds (graph
+    upload, clocks under this load, and clock samples for a timed region shorter than the sampling interval).
+    Returns (milliseconds for the K steps, wall time of the first loaded replay, wall time after the timed one)."""
+    import torch
+
+    for _ in range(warmup):
+        case.step()
+    torch.cuda.synchronize()
+    case._next = 0
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for _ in range(steps):
+            case.step()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    t_load = time.time()
+    while True:
+        graph.replay()
+        torch.cuda.synchronize()
+        if time.time() - t_load >= load_s:
+            break
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    start.record(stream)
+    graph.replay()
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    t_wall1 = time.time()
+    ms = start.elapsed_time(end)
+    del graph
+    return ms, t_load, t_wall1
 
 
 _dist = None
@@ -517,26 +600,32 @@ def run_ours(args):
     AB.load()
     pk = peaks()
     case = make_case(args.workload, device)
+    case.rotate_inputs(l2_bytes(device))
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
 
     clocks = ClockSampler(device.index if device.index is not None else 0)
     clocks.start()
     time.sleep(0.2)
-    total_ms, per, tw0, tw1 = time_steps(case, args.steps, args.warmup, flush)
+    total_ms, tw0, tw1 = time_graph(case, args.steps, args.warmup)
     if AB.attn_get_device_status() != AB.ATTN_OK:
         raise RuntimeError("device status reported an error during the timed steps")
-    clk = clocks.summary(tw0, tw1)
-    e2e_ms, _, _, _ = time_steps(case, max(3, args.steps // 4), 2, flush, e2e=True)
+    clk = clocks.summary(tw0, tw1, "untimed replays of the timed CUDA graph (same load) and the timed replay")
+    n_side = max(3, args.steps // 4)
+    launch_ms, _, _, _ = time_steps(case, n_side, 3, flush)
+    e2e_ms, _, _, _ = time_steps(case, n_side, 2, flush, e2e=True)
     clocks.stop()
+    if AB.attn_get_device_status() != AB.ATTN_OK:
+        raise RuntimeError("device status reported an error during the per-launch or end-to-end steps")
 
     total_ms = max_over_ranks(total_ms)
+    launch_ms = max_over_ranks(launch_ms)
     e2e_ms = max_over_ranks(e2e_ms)
-    n_e2e = max(3, args.steps // 4)
     sec_per_step = total_ms / 1e3 / args.steps
     scale_unit = 1e9 if case.unit == "GB/s" else 1e12
     value = world * case.work / sec_per_step / scale_unit
     per_gpu = case.work / sec_per_step / scale_unit
-    e2e_value = world * case.work / (e2e_ms / 1e3 / n_e2e) / scale_unit
+    e2e_value = world * case.work / (e2e_ms / 1e3 / n_side) / scale_unit
+    launch_value = case.work / (launch_ms / 1e3 / n_side) / scale_unit
     if case.kind == "hbm":
         peak, peak_src = pk["hbm_gbs"], pk["source"]
         roof = {"bound": "hbm", "achieved": per_gpu, "peak": peak, "unit": "GB/s", "frac": per_gpu / peak,
@@ -566,6 +655,10 @@ def run_ours(args):
                 "d2h_bytes_per_step": case.d2h},
         "gpu_launches": case.launches_per_step * args.steps,
         "roofline": roof,
+        "per_launch_flushed": {"value": launch_value, "unit": case.unit, "ms_per_step": launch_ms / n_side,
+                               "frac": launch_value / peak, "steps": n_side,
+                               "how": "each step one launch between its own pair of CUDA events, L2 flushed "
+                                      "(512 MB written, then read) before it; includes the per-launch event floor"},
         "clocks": clk,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -579,14 +672,18 @@ def run_ours(args):
                 continue
             try:
                 c2 = make_case(name, device)
-                t_ms, _, _, _ = time_steps(c2, max(3, args.steps // 4), 3, flush)
-                s_step = t_ms / 1e3 / max(3, args.steps // 4)
+                c2.rotate_inputs(l2_bytes(device))
+                n2 = max(3, args.steps // 4)
+                t_ms, _, _ = time_graph(c2, n2, 3, load_s=0.05)
+                l_ms, _, _, _ = time_steps(c2, n2, 3, flush)
+                s_step = t_ms / 1e3 / n2
                 su = 1e9 if c2.unit == "GB/s" else 1e12
                 v2 = c2.work / s_step / su
                 pkv = pk["hbm_gbs"] if c2.kind == "hbm" else pk["bf16_tflops"]
                 also[name] = {"value": v2, "unit": c2.unit, "ms_per_step": s_step * 1e3, "frac": v2 / pkv,
-                              "config": workload_config(c2)}
+                              "per_launch_flushed_ms": l_ms / n2, "config": workload_config(c2)}
                 del c2
+                torch.cuda.empty_cache()
             except Exception as e:  # a workload whose kernel is not built yet is reported, not fatal
                 also[name] = {"error": str(e)[:200]}
         line["also"] = also
@@ -627,7 +724,7 @@ def run_reference(args):
         "vs_baseline": None,
         "dtype": "f64",
         "data": "synthetic (seeded N(0,1) rounded to bf16)",
-        "config": workload_config(case),
+        "config": dict(workload_config(case), l2="not applicable: the oracle runs on the host cores"),
         "cpu_baseline": {"value": value, "unit": case.unit, "cores": cores, "kind": "oracle", "sample": desc},
         "e2e": {"value": value, "unit": case.unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }

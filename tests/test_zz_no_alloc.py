@@ -8,7 +8,8 @@ fixed buffer compiled into the library instead of a workspace it allocates.
 
 These tests call it through the C ABI and check its output against the
 regular attn_decode_ex entry point on the same inputs, for two calls in a row
-(the second call finds the buffer holding the first call's contents).  The
+(the second call finds the buffer holding the first call's contents), and a
+call captured into a CUDA graph and replayed on new data.  The
 file sorts last so a run that stops at the first failure has already run
 every other test.
 """
@@ -70,3 +71,31 @@ def test_noalloc_matches_decode_ex_twice(lib, B, Hq, Hkv, Lmax, D, kv_range):
                           f"call {call}")
         results.append(out.cpu())
     assert not torch.equal(results[0], results[1])  # the second call really recomputed
+
+
+@pytest.mark.gpu
+def test_noalloc_replays_from_cuda_graph(lib):
+    # The call a graph-captured decode step makes: capture once, then replay with new queries, cache contents and
+    # lengths written in place -- each replay must match attn_decode_ex on that replay's data.
+    dev = torch.device("cuda:0")
+    B, Hq, Hkv, Lmax, D = 4, 32, 8, 2048, 128
+    q, kc, vc, lens = (t.to(dev) for t in make_decode(B, Hq, Hkv, Lmax, D, seed=81, kv_range=(1, Lmax)))
+    out = torch.empty(B, Hq, D, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(B, Hq, dtype=torch.float32, device=dev)
+    AB.attn_decode_noalloc(q, kc, vc, lens, out, lse)  # first call on the device: outside any capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        AB.attn_decode_noalloc(q, kc, vc, lens, out, lse)
+    for seed in (82, 83):
+        q2, kc2, vc2, lens2 = make_decode(B, Hq, Hkv, Lmax, D, seed=seed, kv_range=(1, Lmax))
+        q.copy_(q2)
+        kc.copy_(kc2)
+        vc.copy_(vc2)
+        lens.copy_(lens2)
+        g.replay()
+        ref_o, ref_lse = AB.attn_decode(q, kc, vc, lens)
+        torch.cuda.synchronize()
+        assert AB.attn_get_device_status() == AB.ATTN_OK
+        assert_attn_close(out.cpu(), lse.cpu(), ref_o.double().cpu().numpy(), ref_lse.double().cpu().numpy(),
+                          f"replay seed {seed}")
