@@ -170,11 +170,14 @@ class _Rotation:
         self.sets = [(self.dev, self.out, self.lse)]
         self._next = 0
 
-    def rotate_inputs(self, l2_bytes):
-        """Enough copies that (copies - 1) steps of other traffic cover at least 4x L2; returns the count."""
+    def rotate_inputs(self, l2_bytes, max_copies):
+        """Enough copies that (copies - 1) steps of other traffic cover at least 4x L2, but no more copies than
+        steps (a copy no step reads is no use); returns the count."""
         import torch
 
         n = max(2, math.ceil(4 * l2_bytes / self.touch_bytes) + 1)
+        n = max(1, min(n, max_copies))
+        self.l2_bytes = l2_bytes
         self.sets = [(self.dev, self.out, self.lse)] + [
             ([t.clone() for t in self.dev], torch.empty_like(self.out), torch.empty_like(self.lse))
             for _ in range(n - 1)]
@@ -468,12 +471,18 @@ def workload_config(case):
 
 def l2_note(case):
     n = len(case.sets)
-    if n == 1:
+    l2 = getattr(case, "l2_bytes", None)
+    if l2 is None:
         return "flushed between timed steps: a 512 MB buffer written, then read"
-    return (f"not flushed: inputs larger than L2 -- {n} copies of the inputs and outputs ({n * case.set_bytes() / 1e9:.2f} "
-            f"GB) cycled step by step, so each step reads a copy last touched {n - 1} steps "
-            f"({(n - 1) * case.touch_bytes / 1e6:.0f} MB of other traffic, >= 4x the 129 MB L2) earlier; the K steps "
-            f"run back to back as one CUDA graph replay between one pair of CUDA events")
+    reuse = (n - 1) * case.touch_bytes
+    how = "the K steps run back to back as one CUDA graph replay between one pair of CUDA events"
+    if reuse >= 4 * l2:
+        return (f"not flushed: inputs larger than L2 -- {n} copies of the inputs and outputs "
+                f"({n * case.set_bytes() / 1e9:.2f} GB) cycled step by step, so each step reads a copy last touched "
+                f"{n - 1} steps ({reuse / 1e6:.0f} MB of other traffic, >= 4x the {l2 / 1e6:.0f} MB L2) earlier; {how}")
+    return (f"not flushed, and inputs may be L2-resident: {n} copies cycled, each step's last touched {n - 1} steps "
+            f"({reuse / 1e6:.1f} MB of other traffic) earlier, less than 4x the {l2 / 1e6:.0f} MB L2 (a small "
+            f"configuration, or fewer steps than copies needed); {how}")
 
 
 def flush_l2(flush):
@@ -600,7 +609,7 @@ def run_ours(args):
     AB.load()
     pk = peaks()
     case = make_case(args.workload, device)
-    case.rotate_inputs(l2_bytes(device))
+    case.rotate_inputs(l2_bytes(device), max_copies=args.steps)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
 
     clocks = ClockSampler(device.index if device.index is not None else 0)
@@ -672,8 +681,8 @@ def run_ours(args):
                 continue
             try:
                 c2 = make_case(name, device)
-                c2.rotate_inputs(l2_bytes(device))
                 n2 = max(3, args.steps // 4)
+                c2.rotate_inputs(l2_bytes(device), max_copies=n2)
                 t_ms, _, _ = time_graph(c2, n2, 3, load_s=0.05)
                 l_ms, _, _, _ = time_steps(c2, n2, 3, flush)
                 s_step = t_ms / 1e3 / n2
