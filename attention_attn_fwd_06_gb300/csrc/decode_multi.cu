@@ -79,6 +79,11 @@ struct MCfg {
   static constexpr int SMEM_USED = OFF_MISC + 16;
   static constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // slack to align the base to 1024
   static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory");
+  // One CTA per SM, always: a warp may only touch the TMEM lanes of its SM sub-partition, and the role code
+  // takes that to be its CTA-local warp index % 4.  That holds when the CTA is alone on its SM (its warps take
+  // hardware slots 0..); a second CTA on the same SM starts at the slot after the first CTA's last warp (measured
+  // with 6-warp CTAs: slot 6), which breaks the mapping.  The shared memory a CTA takes rules out a second one.
+  static_assert(2 * (SMEM_ALLOC + 1024) > 228 * 1024, "the TMEM lane mapping needs one CTA per SM");
   // TMEM columns: S buffers 0 and 1 (fp32 128 x 128, P bf16 aliased in their first 64 columns), then O
   static constexpr uint32_t tm_s(int buf) { return (uint32_t)(buf * BN); }
   static constexpr uint32_t TM_O = 2 * BN;

@@ -76,6 +76,11 @@ struct Cfg {
   static constexpr int SMEM_USED = OFF_MISC + 16;
   static constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // slack to align the base to 1024
   static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory");
+  // One CTA per SM, always: a warp may only touch the TMEM lanes of its SM sub-partition, and the role code
+  // takes that to be its CTA-local warp index % 4.  That holds when the CTA is alone on its SM (its warps take
+  // hardware slots 0..); a second CTA on the same SM starts at the slot after the first CTA's last warp (measured
+  // with 6-warp CTAs: slot 6), which breaks the mapping.  The shared memory a CTA takes rules out a second one.
+  static_assert(2 * (SMEM_ALLOC + 1024) > 228 * 1024, "the TMEM lane mapping needs one CTA per SM");
   // TMEM columns: S_t (fp32 128 x 128, P_t bf16 aliased in its first 64 columns), O_t (fp32 128 x D)
   static constexpr uint32_t tm_s(int t) { return (uint32_t)(t * BN); }
   static constexpr uint32_t tm_o(int t) { return (uint32_t)(NQ * BN + t * D); }
@@ -632,12 +637,13 @@ cudaError_t launch_d(const PrefillLaunch& p) {
   a.out_f32 = p.out_f32;
   a.scale_log2 = p.scale * kLog2e;
   const int npairs = (p.Lq + NQ * BM - 1) / (NQ * BM);
-  // Dense causal: persistent CTAs over items of two mirrored tile pairs (equal cost).  Otherwise item costs
-  // differ (packed sequences) or are all equal (non-causal), and one CTA per tile pair, heaviest first,
-  // balances better.
-  const bool persistent = !varlen && p.causal;
-  a.single = persistent ? 0 : 1;
-  a.ns = persistent ? (npairs + 1) / 2 : npairs;
+  // Dense inputs: persistent CTAs (one per SM) over equal-cost items -- two mirrored tile pairs when causal,
+  // one tile pair otherwise -- so a CTA's start-up is paid once.  Packed sequences differ in cost: one CTA per
+  // tile pair, heaviest first, balances better.
+  const bool persistent = !varlen;
+  const bool mirrored = persistent && p.causal;
+  a.single = mirrored ? 0 : 1;
+  a.ns = mirrored ? (npairs + 1) / 2 : npairs;
   a.total_q = p.total_q;
   a.total_k = p.total_k;
   a.status = p.status;
