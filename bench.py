@@ -747,7 +747,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="decode_gqa")
-    ap.add_argument("--also", default="decode_long,decode_multi_gqa,decode_multi_long,prefill_causal,prefill_causal_rope",
+    ap.add_argument("--also", default="decode_long,decode_gqa_paged16,decode_gqa_rope,decode_multi_gqa,decode_multi_long,"
+                                      "prefill_causal,prefill_causal_rope,prefill_ragged_gqa,prefill_noncausal_d64",
                     help="comma-separated extra workloads measured in the same run (rank 0, N=1 style)")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of host work for cpu_baseline")
     ap.add_argument("--ref-budget", type=float, default=5.0, help="seconds of host work per reference step")
