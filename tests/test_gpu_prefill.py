@@ -6,7 +6,8 @@ in both directions (bottom-right causal alignment, rows that see no key), a
 single query, a single key, no keys at all, fp32 output and logits large
 enough to trigger the O rescale.  The prefill workloads run at full size in
 the bench's launch configuration and are checked on sampled rows that the
-oracle computes one by one.
+oracle computes one by one, as is a shape with more work items than SMs (every
+persistent CTA walks several jobs).
 """
 import numpy as np
 import pytest
@@ -162,3 +163,19 @@ def test_prefill_ragged_workload_sampled():
         O_ref, lse_ref = oracle.attention_varlen_rows(q, k, v, cul, cul, w.scale, True, s, h, rows)
         idx = torch.as_tensor(cul[s] + rows)
         assert_attn_close(out[idx, h], lse[idx, h], O_ref, lse_ref, f"seq {s} (len {lens[s]}) h={h}")
+
+
+@pytest.mark.parametrize("D,causal", [(128, False), (128, True), (64, False)])
+def test_prefill_persistent_many_items(D, causal):
+    # More work items than SMs (B * Hq * tile pairs = 2 * 32 * 5 = 320 non-causal), so every persistent CTA walks
+    # several jobs; GQA 4:1 and a ragged last tile (1200 = 9 * 128 + 48); sampled rows of every head checked
+    B, Hq, Hkv, L = 2, 32, 8, 1200
+    q, k, v = make_prefill(B, Hq, Hkv, L, L, D, seed=90 + D + causal)
+    O, lse = run(q, k, v, causal)
+    assert torch.isfinite(O.float()).all() and torch.isfinite(lse).all()
+    rng = np.random.default_rng(D + causal)
+    for b in range(B):
+        for h in range(0, Hq, 5):
+            rows = np.array(sorted(set(rng.choice(L, 6, replace=False).tolist()) | {0, L - 1}))
+            O_ref, lse_ref = oracle.attention_rows(q, k, v, D ** -0.5, causal, b, h, rows)
+            assert_attn_close(O[b, h, rows], lse[b, h, rows], O_ref, lse_ref, f"b={b} h={h}")
