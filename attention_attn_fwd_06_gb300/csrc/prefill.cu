@@ -25,8 +25,13 @@
 //    is kept, which is exact because O and l share it;
 //  * per K/V step the MMA warp issues P_A V_j, S_A(j+1), P_B V_j, S_B(j+1):
 //    one tile's softmax runs while the tensor pipe works for the other tile;
-//  * the query tiles of one head launch together (K/V reuse in L2), heaviest
-//    (latest, causal) first;
+//    its one issuing lane shares an SM sub-partition with two softmax warps,
+//    so the shared-memory descriptors are built once and each MMA only adds
+//    a constant to one 32-bit half;
+//  * dense inputs run one persistent CTA per SM over equal-cost work items
+//    (causal: a heavy and a light tile pair of one head; otherwise one tile
+//    pair); packed sequences launch one CTA per tile pair, heaviest first;
+//    the tiles of one head are adjacent in the order, so K/V stay in L2;
 //  * with RoPE (template flag) each softmax thread rotates its own row of the
 //    job's Q tile in shared memory (rope.cuh) and the MMA warp waits for all
 //    of them; the keys arrive already rotated from a pass of their own

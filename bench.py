@@ -69,11 +69,20 @@ def peaks():
                 "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
+def code_digest(path: str) -> str:
+    """sha256 prefix of a kernel source with its // comments and all whitespace removed: a comment edit does
+    not make committed counters stale, a code edit does."""
+    import hashlib
+    import re
+
+    text = open(path, encoding="utf-8").read()
+    code = "".join(line.split("//", 1)[0] for line in text.splitlines())
+    return hashlib.sha256(re.sub(r"\s+", "", code).encode()).hexdigest()[:16]
+
+
 def read_traffic(kernel: str, workload: str):
     """Per-launch DRAM bytes of `kernel` on `workload` from the committed ncu summary, or None when there is
-    none or the kernel source changed since the counters were taken."""
-    import hashlib
-
+    none or the kernel code changed since the counters were taken."""
     path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}_traffic.txt")
     if not os.path.exists(path):
         return None
@@ -83,10 +92,7 @@ def read_traffic(kernel: str, workload: str):
             k, v = line.strip().split("=", 1)
             kv[k.strip()] = v.strip()
     src = os.path.join(ROOT, "attention_attn_fwd_06_gb300", "csrc", kv.get("source", ""))
-    if not os.path.exists(src):
-        return None
-    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-    if digest != kv.get("source_sha256_16"):
+    if not os.path.exists(src) or code_digest(src) != kv.get("code_sha256_16"):
         return None  # kernel changed since the counters were taken
     try:
         return float(kv["dram_bytes_per_launch"])

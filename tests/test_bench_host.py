@@ -1,6 +1,5 @@
 """Host-side logic of bench.py (no GPU): the rotating input copies that stand in for an L2 flush, the note that
 states what the timing saw, and the lookup of committed ncu traffic."""
-import hashlib
 import os
 
 import pytest
@@ -81,6 +80,17 @@ def test_traffic_lookup_follows_the_kernel_source():
     path = os.path.join(ROOT, "profiles", "decode_split_decode_gqa_traffic.txt")
     kv = dict(line.strip().split("=", 1) for line in open(path) if "=" in line and not line.startswith("#"))
     src = os.path.join(ROOT, "attention_attn_fwd_06_gb300", "csrc", kv["source"])
-    if hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] == kv["source_sha256_16"]:
+    if bench.code_digest(src) == kv["code_sha256_16"]:
         assert bench.read_traffic("decode_split", "decode_gqa") == float(kv["dram_bytes_per_launch"])
     assert bench.read_traffic("decode_split", "no_such_workload") is None
+
+
+def test_code_digest_ignores_comments_but_not_code(tmp_path):
+    a = tmp_path / "a.cu"
+    a.write_text("int f(int x) {  // doubles\n  return 2 * x;\n}\n")
+    b = tmp_path / "b.cu"
+    b.write_text("int f(int x) {\n    return 2*x;  // the same code, other comments and spacing\n}\n")
+    c = tmp_path / "c.cu"
+    c.write_text("int f(int x) {\n  return 3 * x;\n}\n")
+    assert bench.code_digest(str(a)) == bench.code_digest(str(b))
+    assert bench.code_digest(str(a)) != bench.code_digest(str(c))
