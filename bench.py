@@ -696,7 +696,8 @@ def run_ours(args):
                 v2 = c2.work / s_step / su
                 pkv = pk["hbm_gbs"] if c2.kind == "hbm" else pk["bf16_tflops"]
                 also[name] = {"value": v2, "unit": c2.unit, "ms_per_step": s_step * 1e3, "frac": v2 / pkv,
-                              "per_launch_flushed_ms": l_ms / n2, "config": workload_config(c2)}
+                              "per_launch_flushed_ms": l_ms / n2, "traffic": read_traffic(c2.kernel, name),
+                              "config": workload_config(c2)}
                 del c2
                 torch.cuda.empty_cache()
             except Exception as e:  # a workload whose kernel is not built yet is reported, not fatal
