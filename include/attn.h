@@ -20,8 +20,9 @@
  *    never frees or retains them.  Every pointer must be 16-byte aligned.
  *  - Element types: q, k, v, kcache, vcache are bf16 (raw 16-bit words, passed
  *    as void*).  out is bf16 unless an *_ex call asks for fp32.  lse is fp32.
- *  - Arithmetic: fp32 accumulation everywhere; P is rounded to bf16 before the
- *    P V product (tensor-core prefill path).
+ *  - Arithmetic: fp32 accumulation everywhere; on the tensor-core paths
+ *    (prefill, multi-token decode) P is rounded to bf16 before the P V
+ *    product, single-token decode keeps P in fp32.
  *  - Causal masking is aligned to the bottom-right corner: key j is visible to
  *    query i iff j <= i + (Lkv - Lq).  For Lq == Lkv this is the lower
  *    triangle.  A query row that sees no key gets O = 0 and lse = -inf.
