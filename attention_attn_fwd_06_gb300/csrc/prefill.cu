@@ -9,7 +9,8 @@
 // scaled by `scale` and causally masked (bottom-right aligned) as in the
 // standard chain of the same section; the per-row log-sum-exp is written too.
 //
-// GB300 design (two 128-row query tiles per CTA, 10 warps):
+// GB300 design (two 128-row query tiles per CTA; 10 warps at D = 64, 12 at D = 128 where warpgroup 0 -- TMA,
+// MMA and two idle warps -- hands registers to the two softmax warpgroups with setmaxnreg):
 //  * warp 0 (one lane) issues TMA tile loads: both Q tiles once, then K_j and
 //    V_j into two shared-memory rings (128-byte swizzled boxes of 64 columns x
 //    128 rows); a K slot is refilled once the S MMAs reading it are done, a V
