@@ -47,9 +47,10 @@ float* g_noalloc_ptr[kMaxDevices] = {};
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// ATTN_FAULT_INJECT=skip_arrive (read at each decode call): the decode kernel's CTA 0 withholds one pipeline-slot
-// release, so its producer's bounded wait runs out and ATTN_ERR_DEVICE_TIMEOUT is recorded -- a test of the
-// failure path on a real kernel that neither faults nor hangs the GPU.
+// ATTN_FAULT_INJECT=skip_arrive (read at each decode and prefill call): CTA 0 of the kernel withholds one
+// arrival -- decode a pipeline-slot release, prefill a P-ready signal -- so a bounded wait runs out and
+// ATTN_ERR_DEVICE_TIMEOUT is recorded: a test of the failure path on a real kernel that neither faults nor hangs
+// the GPU.
 int fault_skip_arrive() {
   const char* v = std::getenv("ATTN_FAULT_INJECT");
   return (v != nullptr && std::strcmp(v, "skip_arrive") == 0) ? 1 : 0;
@@ -587,6 +588,7 @@ int attn_fwd_ex(const attn_fwd_params* p) {
   L.num_sms = s->num_sms;
   L.status = s->status;
   L.rope = rope_args(p->rope);
+  L.fault_skip_arrive = fault_skip_arrive();
   L.stream = stream;
   return map_cuda(attn::launch_prefill(L));
 }

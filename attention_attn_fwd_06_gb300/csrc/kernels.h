@@ -90,6 +90,7 @@ struct PrefillLaunch {
   int num_sms;      // persistent grid size
   unsigned* status;
   RopeArgs rope;    // rotates q (query i to Lkv - Lq + i) and k (key j to j) when style != 0
+  int fault_skip_arrive;  // test hook: CTA 0 withholds one P-ready arrival (its MMA warp's wait runs out)
   cudaStream_t stream;
 };
 

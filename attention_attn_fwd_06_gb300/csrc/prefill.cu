@@ -126,6 +126,7 @@ struct PrefillArgs {
   int total_q, total_k;  // packed layout: rows of q/out and of k/v
   unsigned* status;
   RopeArgs rope;         // style != 0: the softmax groups rotate their q rows (k arrives rotated)
+  int fault_skip_arrive; // test hook (see launch_prefill's caller): CTA 0 withholds one P-ready arrival
 };
 
 // One job = one pair of 128-row query tiles of one (sequence, head).
@@ -535,7 +536,9 @@ __global__ void __launch_bounds__(Cfg<D, ROPE>::THREADS, 1)
           }
           tc::tmem_st_wait();
           tc::fence_before_sync();
-          mbar_arrive(&p_full[t]);
+          // (the test hook: one thread of CTA 0 withholds its arrival for tile 0's second P, so the MMA warp's
+          // bounded wait for it runs out and the CTA winds down -- no fault, no hang)
+          if (!(a.fault_skip_arrive && blockIdx.x == 0 && t == 0 && j == 1 && row == 0)) mbar_arrive(&p_full[t]);
         }
         if (!ok) break;
 
@@ -683,6 +686,7 @@ cudaError_t launch_d(const PrefillLaunch& p) {
   a.total_k = p.total_k;
   a.status = p.status;
   a.rope = p.rope;
+  a.fault_skip_arrive = p.fault_skip_arrive;
   const long long items = (long long)p.B * p.Hq * a.ns;
   if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
   a.total_items = (int)items;

@@ -179,3 +179,21 @@ def test_prefill_persistent_many_items(D, causal):
             rows = np.array(sorted(set(rng.choice(L, 6, replace=False).tolist()) | {0, L - 1}))
             O_ref, lse_ref = oracle.attention_rows(q, k, v, D ** -0.5, causal, b, h, rows)
             assert_attn_close(O[b, h, rows], lse[b, h, rows], O_ref, lse_ref, f"b={b} h={h}")
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_prefill_fault_injection_times_out_and_recovers(monkeypatch, D):
+    # ATTN_FAULT_INJECT=skip_arrive: one softmax thread of CTA 0 withholds its P-ready arrival for the second K
+    # step of its first tile; the MMA warp's bounded wait runs out (about a second), every role of that CTA winds
+    # down (in-flight copies and MMAs drained, TMEM freed), the status word reports the timeout, and the next
+    # clean call is correct.  Both warp layouts: D = 64 (10 warps) and D = 128 (12 warps, register split).
+    q, k, v = make_prefill(1, 2, 2, 512, 512, D, seed=77 + D)  # CTA 0's first tile pair has 4 K steps
+    AB.attn_get_device_status()
+    monkeypatch.setenv("ATTN_FAULT_INJECT", "skip_arrive")
+    run(q, k, v, False)
+    assert AB.attn_get_device_status() == AB.ATTN_ERR_DEVICE_TIMEOUT
+    monkeypatch.delenv("ATTN_FAULT_INJECT")
+    O, lse = run(q, k, v, False)
+    assert AB.attn_get_device_status() == AB.ATTN_OK
+    O_ref, lse_ref = oracle.attention(q, k, v, D ** -0.5, False)
+    assert_attn_close(O, lse, O_ref, lse_ref)
