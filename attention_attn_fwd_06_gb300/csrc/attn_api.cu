@@ -48,9 +48,9 @@ float* g_noalloc_ptr[kMaxDevices] = {};
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // ATTN_FAULT_INJECT=skip_arrive (read at each decode and prefill call): CTA 0 of the kernel withholds one
-// arrival -- decode a pipeline-slot release, prefill a P-ready signal -- so a bounded wait runs out and
-// ATTN_ERR_DEVICE_TIMEOUT is recorded: a test of the failure path on a real kernel that neither faults nor hangs
-// the GPU.
+// arrival -- decode a pipeline-slot release, prefill and multi-token decode a P-ready signal -- so a bounded
+// wait runs out and ATTN_ERR_DEVICE_TIMEOUT is recorded: a test of the failure path on a real kernel that
+// neither faults nor hangs the GPU.
 int fault_skip_arrive() {
   const char* v = std::getenv("ATTN_FAULT_INJECT");
   return (v != nullptr && std::strcmp(v, "skip_arrive") == 0) ? 1 : 0;
@@ -496,6 +496,7 @@ int attn_decode_multi(const attn_decode_multi_params* p) {
   L.num_sms = s->num_sms;
   L.status = s->status;
   L.rope = rope_args(p->rope);
+  L.fault_skip_arrive = fault_skip_arrive();
   L.stream = stream;
   return map_cuda(attn::launch_decode_multi(L));
 }

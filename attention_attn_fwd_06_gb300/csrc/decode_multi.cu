@@ -107,6 +107,7 @@ struct MultiArgs {
   int out_f32;
   unsigned* status;
   RopeArgs rope;       // style != 0: the softmax threads rotate the Q tile's rows before the S MMAs
+  int fault_skip_arrive;  // test hook: CTA 0 withholds one P-ready arrival (its MMA warp's wait runs out)
 };
 
 __device__ __forceinline__ int clamp_len(int len, int Lmax) { return len < 0 ? 0 : (len > Lmax ? Lmax : len); }
@@ -588,7 +589,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc::tmem_st_wait();
         tc::fence_before_sync();
-        mbar_arrive(&p_full[buf]);
+        // (the test hook: one thread of CTA 0 withholds its arrival for the CTA's second tile, so the MMA warp's
+        // bounded wait for it runs out and the CTA winds down -- no fault, no hang)
+        if (!(a.fault_skip_arrive && blockIdx.x == 0 && gi == 1 && row == 0)) mbar_arrive(&p_full[buf]);
       }
       g += nt;
       if (ok) {
@@ -807,6 +810,7 @@ cudaError_t launch_d(const DecodeMultiLaunch& p) {
   a.out_f32 = p.out_f32;
   a.status = p.status;
   a.rope = p.rope;
+  a.fault_skip_arrive = p.fault_skip_arrive;
   decode_multi_kernel<D><<<decode_multi_grid(p.num_sms), kThreads, C::SMEM_ALLOC, p.stream>>>(tmq, tmk, tmv, a);
   return cudaGetLastError();
 }

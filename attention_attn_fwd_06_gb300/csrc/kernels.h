@@ -66,6 +66,7 @@ struct DecodeMultiLaunch {
   int num_sms;
   unsigned* status;
   RopeArgs rope;        // rotates q (token t to kv_len - Lq + t) when style != 0
+  int fault_skip_arrive;  // test hook: CTA 0 withholds one P-ready arrival (its MMA warp's wait runs out)
   cudaStream_t stream;
 };
 

@@ -156,3 +156,22 @@ def test_decode_multi_long_workload_sampled():
     idx_b = [b for b, _ in heads]
     idx_h = [h for _, h in heads]
     assert_attn_close(O[idx_b, idx_h], lse[idx_b, idx_h], O_ref[idx_b, idx_h], lse_ref[idx_b, idx_h])
+
+
+def test_decode_multi_fault_injection_times_out_and_recovers(monkeypatch):
+    # ATTN_FAULT_INJECT=skip_arrive: one softmax thread of CTA 0 withholds its P-ready arrival for the CTA's second
+    # tile; the MMA warp's bounded wait runs out (about a second), the CTA winds down (copies and MMAs drained,
+    # TMEM freed, its partials never published), the status word reports the timeout -- reading it re-zeroes the
+    # row counters that the unpublished partials left behind -- and the next clean call is correct.
+    B, Hq, Hkv, Lq, L = 4, 32, 8, 8, 8192  # ~14 tiles per CTA, so CTA 0 has a second tile
+    q, kc, vc, _ = make_decode_multi(B, Hq, Hkv, Lq, L, 128, seed=1701)
+    lens = torch.tensor([L, L - 300, 5000, 777], dtype=torch.int32)
+    AB.attn_get_device_status()
+    monkeypatch.setenv("ATTN_FAULT_INJECT", "skip_arrive")
+    run(q, kc, vc, lens)
+    assert AB.attn_get_device_status() == AB.ATTN_ERR_DEVICE_TIMEOUT
+    monkeypatch.delenv("ATTN_FAULT_INJECT")
+    O, lse = run(q, kc, vc, lens)
+    assert AB.attn_get_device_status() == AB.ATTN_OK
+    O_ref, lse_ref = oracle.decode_multi(q, kc, vc, lens.tolist(), 128 ** -0.5)
+    assert_attn_close(O, lse, O_ref, lse_ref)
