@@ -7,6 +7,7 @@
 
 #include <cstdint>
 #include <cstdlib>
+#include <cmath>
 #include <cstring>
 #include <mutex>
 
@@ -156,7 +157,7 @@ int validate_decode(const attn_decode_params* p) {
   if (p->D != 64 && p->D != 128) return ATTN_ERR_UNSUPPORTED;
   if (p->out_dtype != ATTN_DTYPE_BF16 && p->out_dtype != ATTN_DTYPE_F32) return ATTN_ERR_INVALID_ARG;
   if (p->chunk < 0 || p->chunk > (1 << 20)) return ATTN_ERR_INVALID_ARG;
-  if (!(p->scale == p->scale)) return ATTN_ERR_INVALID_ARG;  // NaN scale
+  if (!std::isfinite(p->scale)) return ATTN_ERR_INVALID_ARG;  // NaN or infinite scale
   if (p->B == 0) return ATTN_OK;
   if (p->q == nullptr || p->kcache == nullptr || p->vcache == nullptr || p->kv_lens == nullptr ||
       p->out == nullptr)
@@ -176,7 +177,7 @@ int validate_fwd(const attn_fwd_params* p) {
   if (p->D != 64 && p->D != 128) return ATTN_ERR_UNSUPPORTED;
   if (p->causal != 0 && p->causal != 1) return ATTN_ERR_INVALID_ARG;
   if (p->out_dtype != ATTN_DTYPE_BF16 && p->out_dtype != ATTN_DTYPE_F32) return ATTN_ERR_INVALID_ARG;
-  if (!(p->scale == p->scale)) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(p->scale)) return ATTN_ERR_INVALID_ARG;  // NaN or infinite scale
   const bool varlen = p->cu_seqlens_q != nullptr || p->cu_seqlens_k != nullptr;
   if (varlen) {
     if (p->cu_seqlens_q == nullptr || p->cu_seqlens_k == nullptr) return ATTN_ERR_INVALID_ARG;

@@ -108,7 +108,8 @@ typedef struct attn_rope {
  *   v    bf16 [B, Hkv, Lkv, D]  contiguous
  *   out  bf16 [B, Hq,  Lq,  D]  written
  *   lse  fp32 [B, Hq,  Lq]      written; may be NULL (then not written)
- *   scale   multiplies the logits (pass 1/sqrt(D) for the standard chain)
+ *   scale   multiplies the logits (pass 1/sqrt(D) for the standard chain); must be
+ *           finite (NaN or +-inf: ATTN_ERR_INVALID_ARG)
  *   causal  0 = no mask, 1 = bottom-right-aligned causal mask
  *
  * Runs on the tensor cores (tcgen05 MMAs with TMEM accumulators, TMA-fed

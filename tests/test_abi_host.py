@@ -78,6 +78,8 @@ def dec(lib, **kw):
     (dict(D=256), B.ATTN_ERR_UNSUPPORTED),
     (dict(causal=2), B.ATTN_ERR_INVALID_ARG),
     (dict(scale=float("nan")), B.ATTN_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), B.ATTN_ERR_INVALID_ARG),
+    (dict(scale=float("-inf")), B.ATTN_ERR_INVALID_ARG),
     (dict(q=FAKE + 8), B.ATTN_ERR_ALIGNMENT),
     (dict(out=FAKE + 2), B.ATTN_ERR_ALIGNMENT),
     (dict(lse=FAKE + 2), B.ATTN_ERR_ALIGNMENT),
@@ -138,6 +140,8 @@ def multi(lib, **kw):
     (dict(Lq=-3), B.ATTN_ERR_INVALID_ARG),
     (dict(Hq=6, Hkv=4), B.ATTN_ERR_INVALID_ARG),
     (dict(scale=float("nan")), B.ATTN_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), B.ATTN_ERR_INVALID_ARG),
+    (dict(scale=float("-inf")), B.ATTN_ERR_INVALID_ARG),
     (dict(out_dtype=5), B.ATTN_ERR_INVALID_ARG),
     (dict(D=96), B.ATTN_ERR_UNSUPPORTED),
     (dict(Lq=33), B.ATTN_ERR_UNSUPPORTED),           # 4 heads x 33 tokens > one 128-row tile
