@@ -24,10 +24,15 @@ it (it includes the per-launch event and launch floor).
 ``e2e`` repeats the measurement through the same call with the inputs copied
 from pinned host memory and the outputs copied back inside the timed region
 (one call at a time, L2 flushed before each).
-``cpu_baseline`` times the fp64 oracle on a bounded sample on the host cores.
+``cpu_baseline`` times the fp64 oracle on a bounded sample on the host cores
+(one spawn-started worker per core; each worker rebuilds the workload's
+inputs from the seeded generators once, so a unit of work ships only its
+indices).
 
 ``--impl reference`` times that oracle alone (the only reference this
-library has) and prints the same JSON line with ``"impl": "reference"``.
+library has) and prints the same JSON line with ``"impl": "reference"``;
+each step is one bounded sample and the whole run, warm-up included, takes
+about ``--ref-total`` seconds of host work (default 120).
 
 With ``--gpus N > 1`` (launched by torch.distributed.run) every rank runs an
 independent replica of the workload; nothing is exchanged ("scaling": "weak").
@@ -211,12 +216,11 @@ class _RopeMixin:
     def _rope_setup(self, w, max_pos, device):
         """RoPE tables (model constants: resident on the device, not copied per step) when the workload asks."""
         self.rope_style = w.extra.get("rope")
-        self.rope_dev = self.rope_host = None
+        self.rope_dev = None
         if self.rope_style:
             from attention_attn_fwd_06_gb300.inputs import rope_tables
 
             cos, sin = rope_tables(max_pos, w.D)
-            self.rope_host = (cos.numpy(), sin.numpy(), self.rope_style)
             self.rope_dev = (cos.to(device), sin.to(device), self.rope_style)
 
 
@@ -236,7 +240,6 @@ class DecodeCase(_Rotation, _RopeMixin):
             q, kc, vc, lens = make_decode(w.B, w.Hq, w.Hkv, w.L, w.D, w.seed,
                                           kv_lens=w.kv_lens or None, kv_range=w.kv_range or None)
         self.page_size = w.extra.get("page_size")
-        self.oracle_host = (q, kc, vc)
         self._rope_setup(w, w.L, device)
         if self.page_size:
             from attention_attn_fwd_06_gb300.inputs import make_pages
@@ -347,103 +350,146 @@ class PrefillCase(_Rotation, _RopeMixin):
 
 # ----------------------------------------------------------------------------- oracle (CPU) leg
 
-def _oracle_task(args):
-    os.environ.setdefault("OMP_NUM_THREADS", "1")
-    import numpy as np
+_ORACLE_DATA = None  # per worker process: the workload's inputs as the oracle takes them
 
+
+def _oracle_inputs(name):
+    """(workload, q, k, v, lengths or cu_seqlens, rope) of a workload, rebuilt from its seeded generators: the
+    same bf16 values the kernels get, as fp32 arrays (exact), which the oracle lifts to fp64."""
+    from attention_attn_fwd_06_gb300.inputs import (WORKLOADS, make_decode, make_decode_multi, make_prefill,
+                                                    make_varlen, rope_tables)
+
+    w = WORKLOADS[name]
+    lens = None
+    if w.kind == "decode_multi":
+        q, k, v, n = make_decode_multi(w.B, w.Hq, w.Hkv, w.Lq, w.L, w.D, w.seed,
+                                       kv_lens=w.kv_lens or None, kv_range=w.kv_range or None)
+        lens, max_pos = [int(x) for x in n.tolist()], w.L
+    elif w.kind == "decode":
+        q, k, v, n = make_decode(w.B, w.Hq, w.Hkv, w.L, w.D, w.seed,
+                                 kv_lens=w.kv_lens or None, kv_range=w.kv_range or None)
+        lens, max_pos = [int(x) for x in n.tolist()], w.L
+    elif w.kind == "varlen":
+        q, k, v, cu = make_varlen(w.B, w.Hq, w.Hkv, w.D, w.seed, seq_range=w.seq_range)
+        lens, max_pos = [int(x) for x in cu.tolist()], w.seq_range[1]
+    else:
+        q, k, v = make_prefill(w.B, w.Hq, w.Hkv, w.L, w.L, w.D, w.seed)
+        max_pos = w.L
+    rope = None
+    if w.extra.get("rope"):
+        cos, sin = rope_tables(max_pos, w.D)
+        rope = (cos.numpy(), sin.numpy(), w.extra["rope"])
+    return w, q.float().numpy(), k.float().numpy(), v.float().numpy(), lens, rope
+
+
+def _oracle_init(name):
+    global _ORACLE_DATA
+    os.environ["OMP_NUM_THREADS"] = "1"
+    os.environ["OPENBLAS_NUM_THREADS"] = "1"
+    _ORACLE_DATA = _oracle_inputs(name)
+
+
+def _oracle_task(unit):
+    """One unit of the workload through the oracle's own entry points; returns its seconds."""
     import oracle
 
-    kind, payload, rope = args
+    w, q, k, v, lens, rope = _ORACLE_DATA
+    a, h = unit
+    hk = h // (w.Hq // w.Hkv)
     t0 = time.perf_counter()
-    # one (sequence, head) problem through the oracle's own entry points
-    if kind == "decode":
-        q, kc, vc, n, scale = payload
-        oracle.decode(q[None, None], kc[None, None, :n], vc[None, None, :n], [n], scale, rope=rope)
-    elif kind == "decode_multi":
-        q, kc, vc, n, scale = payload  # q [Lq, D]: bottom-right causal over the sequence's n keys
-        oracle.decode_multi(q[None, None], kc[None, None, :n], vc[None, None, :n], [n], scale, rope=rope)
+    if w.kind in ("decode", "decode_multi"):
+        n = lens[a]
+        args = (q[a, h][None, None], k[a, hk][None, None, :n], v[a, hk][None, None, :n], [n], w.scale)
+        if w.kind == "decode":  # q [D]
+            oracle.decode(*args, rope=rope)
+        else:  # q [Lq, D]: bottom-right causal over the sequence's n keys
+            oracle.decode_multi(*args, rope=rope)
+    elif w.kind == "varlen":
+        s0, s1 = lens[a], lens[a + 1]
+        oracle.attention(q[s0:s1, h][None, None], k[s0:s1, hk][None, None], v[s0:s1, hk][None, None], w.scale,
+                         w.causal, rope=rope)
     else:
-        q, k, v, scale, causal = payload
-        oracle.attention(q[None, None], k[None, None], v[None, None], scale, causal, rope=rope)
+        oracle.attention(q[a, h][None, None], k[a, hk][None, None], v[a, hk][None, None], w.scale, w.causal,
+                         rope=rope)
     return time.perf_counter() - t0
 
 
-def run_oracle_pool(case, budget_s):
-    """Time the fp64 oracle on a bounded, seeded sample of the case's rows, on all host cores.
+class OraclePool:
+    """The fp64 oracle timed on bounded, seeded samples of a case's rows, on all host cores.
 
     Work units are dealt to a spawn-started process pool (one BLAS thread per
-    process) in rounds of one unit per core until ``budget_s`` seconds have
-    passed; the value counts the algorithmic work of the units finished.
-    Decode units are (b, hq) rows, each worth its share of its kv head's
-    K/V bytes plus its q, O and lse; prefill units are (sequence, head)
-    problems worth 4*D FLOPs per visible pair.
+    process; started once, outside every timed sample) in rounds of one unit
+    per core until a sample's budget has passed; a sample's work counts the
+    algorithmic work of the units finished.  Decode units are (b, hq) rows,
+    each worth its share of its kv head's K/V bytes plus its q, O and lse;
+    prefill units are (sequence, head) problems worth 4*D FLOPs per visible
+    pair.  Samples continue through the seeded unit order where the last one
+    stopped.
     """
-    import multiprocessing as mp
 
-    import numpy as np
+    def __init__(self, case):
+        import multiprocessing as mp
 
-    w = case.w
-    rng = np.random.default_rng(12345)
-    cores = os.cpu_count() or 1
-    units = []
-    if isinstance(case, DecodeCase):
-        q, kc, vc = (t.float().numpy() for t in case.oracle_host)
+        import numpy as np
+
+        w = case.w
+        rng = np.random.default_rng(12345)
+        self.cores = os.cpu_count() or 1
+        units = []  # ((sequence, q head), algorithmic work)
         g = w.Hq // w.Hkv
-        Lq = case.Lq
-        for b in range(w.B):
-            for h in range(w.Hq):
-                n = case.lens[b]
-                hk = h // g
-                bytes_ = n * w.D * 2 * 2 / g + Lq * (w.D * 2 * 2 + 4)
-                units.append(((case.w.kind, (q[b, h], kc[b, hk], vc[b, hk], n, w.scale), case.rope_host), bytes_))
-        what = "(b, hq) decode rows" if Lq == 1 else f"(b, hq) decode rows of {Lq} tokens"
-    else:
-        hosts = [t.float().numpy() for t in case.host[:3]]
-        cu = case.host[3].numpy() if w.kind == "varlen" else None
-        g = w.Hq // w.Hkv
-        for a in range(w.B):
-            for h in range(w.Hq):
-                hk = h // g
-                if cu is not None:
-                    s0, s1 = int(cu[a]), int(cu[a + 1])
-                    qh, kh, vh = hosts[0][s0:s1, h], hosts[1][s0:s1, hk], hosts[2][s0:s1, hk]
-                    L = s1 - s0
-                else:
-                    qh, kh, vh = hosts[0][a, h], hosts[1][a, hk], hosts[2][a, hk]
-                    L = w.L
+        if isinstance(case, DecodeCase):
+            Lq = case.Lq
+            for b in range(w.B):
+                for h in range(w.Hq):
+                    units.append(((b, h), case.lens[b] * w.D * 2 * 2 / g + Lq * (w.D * 2 * 2 + 4)))
+            self.what = "(b, hq) decode rows" if Lq == 1 else f"(b, hq) decode rows of {Lq} tokens"
+        else:
+            for a in range(w.B):
+                L = case.seqlens[a]
                 f = 4.0 * w.D * ((L * (L + 1)) // 2 if w.causal else L * L)
-                units.append((("prefill", (qh, kh, vh, w.scale, w.causal), case.rope_host), f))
-        what = "(sequence, head) prefill problems"
-    order = rng.permutation(len(units))
-    units = [units[i] for i in order]
-    ctx = mp.get_context("spawn")
-    saved = {k: os.environ.get(k) for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS")}
-    os.environ["OMP_NUM_THREADS"] = "1"
-    os.environ["OPENBLAS_NUM_THREADS"] = "1"
-    done, work, passes = 0, 0.0, 0
-    try:
-        with ctx.Pool(cores) as pool:
-            pool.map(_oracle_task, [units[0][0]] * cores)  # spawn + import cost stays outside the timing
-            t0 = time.perf_counter()
-            i = 0
-            while True:
-                batch = [units[(i + j) % len(units)] for j in range(cores)]
-                pool.map(_oracle_task, [u[0] for u in batch], chunksize=1)
-                i += cores
-                done += len(batch)
-                work += sum(u[1] for u in batch)
-                if time.perf_counter() - t0 >= budget_s or done >= 50 * len(units):
-                    break
-            dt = time.perf_counter() - t0
-    finally:
-        for k, v in saved.items():
-            if v is None:
-                os.environ.pop(k, None)
-            else:
-                os.environ[k] = v
-    desc = (f"{done} {what} (of {len(units)} in the workload; seeded order, repeating if all done), "
-            f"fp64 numpy oracle, {cores} spawn worker processes x 1 BLAS thread, {dt:.1f} s")
-    return work, dt, cores, desc
+                for h in range(w.Hq):
+                    units.append(((a, h), f))
+            self.what = "(sequence, head) prefill problems"
+        order = rng.permutation(len(units))
+        self.units = [units[i] for i in order]
+        self._i = 0
+        # every worker rebuilds the inputs from the seeded generators once (no arrays cross the pipe per unit);
+        # the start-up and a first unit per worker stay outside every timed sample
+        self.pool = mp.get_context("spawn").Pool(self.cores, initializer=_oracle_init, initargs=(w.name,))
+        self.pool.map(_oracle_task, [self.units[0][0]] * self.cores, chunksize=1)
+
+    def sample(self, budget_s):
+        """(work units done, seconds, cores, description) for rounds of units until ``budget_s`` has passed."""
+        done, work = 0, 0.0
+        t0 = time.perf_counter()
+        while True:
+            batch = [self.units[(self._i + j) % len(self.units)] for j in range(self.cores)]
+            self.pool.map(_oracle_task, [u[0] for u in batch], chunksize=1)
+            self._i += self.cores
+            done += len(batch)
+            work += sum(u[1] for u in batch)
+            if time.perf_counter() - t0 >= budget_s or done >= 50 * len(self.units):
+                break
+        dt = time.perf_counter() - t0
+        desc = (f"{done} {self.what} (of {len(self.units)} in the workload; seeded order, repeating if all done), "
+                f"fp64 numpy oracle, {self.cores} spawn worker processes x 1 BLAS thread, {dt:.1f} s")
+        return work, dt, self.cores, desc
+
+    def close(self):
+        self.pool.terminate()
+        self.pool.join()
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+
+def run_oracle_pool(case, budget_s):
+    """One bounded sample of the fp64 oracle on all host cores (see ``OraclePool``)."""
+    with OraclePool(case) as pool:
+        return pool.sample(budget_s)
 
 
 # ----------------------------------------------------------------------------- main
@@ -717,15 +763,19 @@ def run_reference(args):
     import torch  # noqa: F401
 
     case = make_case(args.workload, "cpu")
-    per_step = []
-    desc, cores, work = "", 0, 0.0
-    for i in range(args.warmup + args.steps):
-        work, dt, cores, desc = case.oracle_sample(args.ref_budget)
-        if i >= args.warmup:
-            per_step.append(dt)
+    # each step is one bounded sample; the whole run (warm-up included) stays within about --ref-total seconds
+    budget = min(args.ref_budget, args.ref_total / max(1, args.steps + args.warmup))
+    per_step, work_sum = [], 0.0
+    desc, cores = "", 0
+    with OraclePool(case) as pool:
+        for i in range(args.warmup + args.steps):
+            work, dt, cores, desc = pool.sample(budget)
+            if i >= args.warmup:
+                per_step.append(dt)
+                work_sum += work
     scale_unit = 1e9 if case.unit == "GB/s" else 1e12
     sec = sum(per_step) / len(per_step)
-    value = work / sec / scale_unit
+    value = work_sum / sum(per_step) / scale_unit
     line = {
         "impl": "reference",
         "metric": METRIC,
@@ -758,7 +808,10 @@ def main():
                                       "prefill_causal,prefill_causal_rope,prefill_ragged_gqa,prefill_noncausal_d64",
                     help="comma-separated extra workloads measured in the same run (rank 0, N=1 style)")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of host work for cpu_baseline")
-    ap.add_argument("--ref-budget", type=float, default=5.0, help="seconds of host work per reference step")
+    ap.add_argument("--ref-budget", type=float, default=5.0, help="at most this many seconds of host work per "
+                                                                  "reference step")
+    ap.add_argument("--ref-total", type=float, default=120.0,
+                    help="seconds of host work for the whole reference run (warm-up steps included)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":

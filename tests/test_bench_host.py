@@ -1,6 +1,10 @@
 """Host-side logic of bench.py (no GPU): the rotating input copies that stand in for an L2 flush, the note that
-states what the timing saw, and the lookup of committed ncu traffic."""
+states what the timing saw, the lookup of committed ncu traffic, and the reference arm (the oracle on the host
+cores), which needs no GPU at all."""
+import json
 import os
+import subprocess
+import sys
 
 import pytest
 import torch
@@ -94,3 +98,32 @@ def test_code_digest_ignores_comments_but_not_code(tmp_path):
     c.write_text("int f(int x) {\n  return 3 * x;\n}\n")
     assert bench.code_digest(str(a)) == bench.code_digest(str(b))
     assert bench.code_digest(str(a)) != bench.code_digest(str(c))
+
+
+def _reference_run(extra_env=None, *args):
+    env = dict(os.environ, **(extra_env or {}))
+    cmd = [sys.executable, "bench.py", "--impl", "reference", "--workload", "tiny_causal", "--steps", "2",
+           "--warmup", "1", "--ref-total", "2"] + list(args)
+    return subprocess.run(cmd, cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+
+
+def test_reference_arm_prints_one_oracle_line():
+    r = _reference_run()
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC
+    assert line["value"] > 0 and line["unit"] == "TFLOP/s" and line["higher_is_better"] is True
+    assert (line["steps"], line["warmup"], line["n_gpus"]) == (2, 1, 1)
+    assert line["config"]["workload"] == "tiny_causal"
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == line["value"] and cb["sample"]
+    assert line["e2e"] == {"value": line["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
+
+
+def test_reference_arm_other_ranks_exit_without_work():
+    r = _reference_run({"RANK": "1", "WORLD_SIZE": "2"})
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert r.stdout.strip() == ""
