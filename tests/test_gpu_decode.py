@@ -6,7 +6,8 @@ that needs several head groups), both head dims, ragged and degenerate
 lengths (0, 1, not a multiple of the stage or the chunk, == Lmax) and several
 minimum slice sizes (down to one key per CTA, which splits rows into many
 partials); the two decode workloads run at full size (all rows for the 8 x
-4096 cache, a sample of rows for the 131072-key cache).
+4096 cache, a sample of rows for the 131072-key cache), and so does a 2^20-key
+cache (sampled heads).
 """
 import numpy as np
 import pytest
@@ -164,6 +165,22 @@ def test_decode_workload_long_sampled():
                       O_ref[bi, hi], lse_ref[bi, hi], "decode_long")
     assert torch.isfinite(O).all() and torch.isfinite(lse).all()
     assert AB.attn_get_device_status() == AB.ATTN_OK
+
+
+def test_decode_million_key_cache_sampled():
+    """A 2^20-key cache (8x the longest workload): one sequence filling it, one of 777,777 keys; sampled heads of
+    both against the oracle."""
+    B, Hq, Hkv, Lmax, D = 2, 8, 2, 1 << 20, 128
+    q, kc, vc, lens = make_decode(B, Hq, Hkv, Lmax, D, seed=1 << 20, kv_lens=[Lmax, 777_777])
+    O, lse = run(q, kc, vc, lens, D ** -0.5)
+    assert torch.isfinite(O).all() and torch.isfinite(lse).all()
+    assert AB.attn_get_device_status() == AB.ATTN_OK
+    heads = [(0, 0), (0, 5), (1, 3), (1, 7)]
+    O_ref, lse_ref = oracle.decode(q, kc, vc, lens.tolist(), D ** -0.5, heads=heads)
+    bi = np.array([b for b, _ in heads])
+    hi = np.array([h for _, h in heads])
+    assert_attn_close(O[torch.as_tensor(bi), torch.as_tensor(hi)], lse[torch.as_tensor(bi), torch.as_tensor(hi)],
+                      O_ref[bi, hi], lse_ref[bi, hi], "2^20-key decode")
 
 
 @pytest.mark.parametrize("B,Hq,Hkv,Lmax,D,page_size", [

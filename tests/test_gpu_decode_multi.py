@@ -7,8 +7,8 @@ exact tile multiples, one past them, shorter than a tile, shorter than Lq
 (tokens that see no key) and zero, one long sequence split over every CTA
 (many partials per item, merged in the kernel), fp32 output, logits peaked
 enough to force the O rescale, determinism, Lq = 1 against the single-token
-decode, and both multi-token workloads (8 x 4096 and 131k keys) at full size on
-sampled heads.
+decode, and both multi-token workloads (8 x 4096 and 131k keys) and a 2^20-key
+cache at full size on sampled heads.
 """
 import numpy as np
 import pytest
@@ -153,6 +153,19 @@ def test_decode_multi_long_workload_sampled():
     assert torch.isfinite(O.float()).all() and torch.isfinite(lse).all()
     heads = [(b, h) for b in range(w.B) for h in (0, 13, 31)]
     O_ref, lse_ref = oracle.decode_multi(q, kc, vc, lens.tolist(), w.scale, heads=heads)
+    idx_b = [b for b, _ in heads]
+    idx_h = [h for _, h in heads]
+    assert_attn_close(O[idx_b, idx_h], lse[idx_b, idx_h], O_ref[idx_b, idx_h], lse_ref[idx_b, idx_h])
+
+
+def test_decode_multi_million_key_cache_sampled():
+    """4 new tokens over a 2^20-key cache (8x the longest workload) and one of 777,777 keys, sampled heads."""
+    B, Hq, Hkv, Lq, Lmax, D = 2, 8, 2, 4, 1 << 20, 128
+    q, kc, vc, lens = make_decode_multi(B, Hq, Hkv, Lq, Lmax, D, seed=(1 << 20) + 1, kv_lens=[Lmax, 777_777])
+    O, lse = run(q, kc, vc, lens.tolist())
+    assert torch.isfinite(O.float()).all() and torch.isfinite(lse).all()
+    heads = [(0, 1), (0, 6), (1, 0), (1, 7)]
+    O_ref, lse_ref = oracle.decode_multi(q, kc, vc, lens.tolist(), D ** -0.5, heads=heads)
     idx_b = [b for b, _ in heads]
     idx_h = [h for _, h in heads]
     assert_attn_close(O[idx_b, idx_h], lse[idx_b, idx_h], O_ref[idx_b, idx_h], lse_ref[idx_b, idx_h])

@@ -7,7 +7,8 @@ single query, a single key, no keys at all, fp32 output and logits large
 enough to trigger the O rescale.  The prefill workloads run at full size in
 the bench's launch configuration and are checked on sampled rows that the
 oracle computes one by one, as is a shape with more work items than SMs (every
-persistent CTA walks several jobs).
+persistent CTA walks several jobs) and one 65,536-token sequence at each head
+dim.
 """
 import numpy as np
 import pytest
@@ -144,6 +145,22 @@ def test_prefill_workload_sampled(name):
             rows = _sample_rows(rng, w.L, 48)
             O_ref, lse_ref = oracle.attention_rows(q, k, v, w.scale, w.causal, b, int(h), rows)
             assert_attn_close(O[b, h, rows], lse[b, h, rows], O_ref, lse_ref, f"{name} b={b} h={h}")
+
+
+@pytest.mark.parametrize("D,causal", [(128, True), (64, False)])
+def test_prefill_64k_sequence_sampled(D, causal):
+    """One 65,536-token sequence (8x the longest workload), grouped heads: sampled rows across the whole range,
+    the last rows included, against the oracle row by row."""
+    B, Hq, Hkv, L = 1, 2, 1, 65536
+    q, k, v = make_prefill(B, Hq, Hkv, L, L, D, seed=65536 + D)
+    O, lse = run(q, k, v, causal)
+    assert torch.isfinite(O.float()).all() and torch.isfinite(lse).all()
+    rng = np.random.default_rng(13)
+    for h in range(Hq):
+        rows = _sample_rows(rng, L, 24)
+        rows = np.union1d(rows, [L - 129, L - 128, L - 2])
+        O_ref, lse_ref = oracle.attention_rows(q, k, v, D ** -0.5, causal, 0, h, rows)
+        assert_attn_close(O[0, h, rows], lse[0, h, rows], O_ref, lse_ref, f"L={L} D={D} h={h}")
 
 
 def test_prefill_ragged_workload_sampled():
