@@ -543,33 +543,51 @@ int attn_fwd_ex(const attn_fwd_params* p) {
   const void* kk = p->k;
   const bool varlen = p->cu_seqlens_q != nullptr;
   const long long krows = varlen ? (long long)p->total_k * p->Hkv : (long long)p->B * p->Hkv * p->Lkv;
+  const void* qq = p->q;
+  const long long qrows = varlen ? (long long)p->total_q * p->Hq : (long long)p->B * p->Hq * p->Lq;
   if (rope_on && krows > 0) {
-    // rotate the keys once (into k_out or the workspace), then attend over the rotated copy
+    // rotate the keys once (into k_out or the workspace) and the queries (into the workspace), then attend over
+    // the rotated copies
     void* kdst = p->rope.k_out;
-    if (kdst == nullptr) {
+    void* qdst = nullptr;
+    {
+      const size_t kbytes = kdst == nullptr ? (size_t)krows * p->D * 2 : 0;
       std::lock_guard<std::mutex> lock(g_mu);
-      st = ensure_workspace_locked(*s, kCounterBytes + (size_t)krows * p->D * 2, stream);
+      st = ensure_workspace_locked(*s, kCounterBytes + kbytes + (size_t)qrows * p->D * 2, stream);
       if (st != ATTN_OK) return st;
-      kdst = static_cast<char*>(s->ws) + kCounterBytes;
+      if (kdst == nullptr) kdst = static_cast<char*>(s->ws) + kCounterBytes;
+      qdst = static_cast<char*>(s->ws) + kCounterBytes + kbytes;
     }
-    attn::RopeKLaunch R{};
-    R.k = p->k;
-    R.k_out = kdst;
-    R.cu_k = varlen ? p->cu_seqlens_k : nullptr;
+    attn::RopeRowsLaunch R{};
+    R.src = p->k;
+    R.dst = kdst;
+    R.cu = varlen ? p->cu_seqlens_k : nullptr;
     R.B = p->B;
-    R.Hkv = p->Hkv;
+    R.H = p->Hkv;
     R.L = p->Lkv;
     R.D = p->D;
-    R.total_k = p->total_k;
+    R.total = p->total_k;
     R.rope = rope_args(p->rope);
     R.status = s->status;
     R.stream = stream;
-    st = map_cuda(attn::launch_rope_k(R));
+    st = map_cuda(attn::launch_rope_rows(R));
     if (st != ATTN_OK) return st;
     kk = kdst;
+    attn::RopeRowsLaunch Rq = R;  // query i of a sequence sits at i + Lkv - Lq
+    Rq.src = p->q;
+    Rq.dst = qdst;
+    Rq.cu = varlen ? p->cu_seqlens_q : nullptr;
+    Rq.cu_kv = varlen ? p->cu_seqlens_k : nullptr;
+    Rq.H = p->Hq;
+    Rq.L = p->Lq;
+    Rq.total = p->total_q;
+    Rq.pos_off = varlen ? 0 : p->Lkv - p->Lq;
+    st = map_cuda(attn::launch_rope_rows(Rq));
+    if (st != ATTN_OK) return st;
+    qq = qdst;
   }
   attn::PrefillLaunch L{};
-  L.q = p->q;
+  L.q = qq;
   L.k = kk;
   L.v = p->v;
   L.out = p->out;
@@ -589,7 +607,6 @@ int attn_fwd_ex(const attn_fwd_params* p) {
   L.total_k = p->total_k;
   L.num_sms = s->num_sms;
   L.status = s->status;
-  L.rope = rope_args(p->rope);
   L.fault_skip_arrive = fault_skip_arrive();
   L.stream = stream;
   return map_cuda(attn::launch_prefill(L));

@@ -90,26 +90,27 @@ struct PrefillLaunch {
   int total_q, total_k;
   int num_sms;      // persistent grid size
   unsigned* status;
-  RopeArgs rope;    // rotates q (query i to Lkv - Lq + i) and k (key j to j) when style != 0
   int fault_skip_arrive;  // test hook: CTA 0 withholds one P-ready arrival (its MMA warp's wait runs out)
   cudaStream_t stream;
 };
 
 cudaError_t launch_prefill(const PrefillLaunch& p);
 
-// Rotary embedding of a prefill call's keys into k_out (same layout as k), once per call.
-struct RopeKLaunch {
-  const void* k;       // bf16 [B, Hkv, L, D] (dense) or [total_k, Hkv, D] (packed)
-  void* k_out;         // bf16, same layout
-  const int* cu_k;     // null for the dense layout; else int32 [B + 1]
-  int B, Hkv, L, D;    // L: keys per sequence (dense)
-  int total_k;         // packed: rows
+// Rotary embedding of the keys or the queries of a prefill call into dst (same layout as src), once per call.
+struct RopeRowsLaunch {
+  const void* src;     // bf16 [B, H, L, D] (dense) or [total, H, D] (packed)
+  void* dst;           // bf16, same layout
+  const int* cu;       // null for the dense layout; else int32 [B + 1]
+  int B, H, L, D;      // L: rows per sequence (dense)
+  int total;           // packed: tokens
+  int pos_off;         // dense: added to every row's position (queries: Lkv - Lq)
+  const int* cu_kv;    // packed queries: the keys' offsets; a sequence's rows are shifted by its Lkv - Lq
   RopeArgs rope;
   unsigned* status;
   cudaStream_t stream;
 };
 
-cudaError_t launch_rope_k(const RopeKLaunch& p);
+cudaError_t launch_rope_rows(const RopeRowsLaunch& p);
 
 // One thread waits on a barrier nothing arrives on, with the kernels' bounded wait and a limit of limit_ns.
 cudaError_t launch_selftest_timeout(unsigned long long limit_ns, unsigned* status, cudaStream_t stream);

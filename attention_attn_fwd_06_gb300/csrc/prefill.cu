@@ -33,11 +33,10 @@
 //    (causal: a heavy and a light tile pair of one head; otherwise one tile
 //    pair); packed sequences launch one CTA per tile pair, heaviest first;
 //    the tiles of one head are adjacent in the order, so K/V stay in L2;
-//  * with RoPE (template flag) each softmax thread rotates its own row of the
-//    job's Q tile in shared memory (rope.cuh) and the MMA warp waits for all
-//    of them; the keys arrive already rotated from a pass of their own
-//    (rope_k.cu), since rotating every K tile at every visit would repeat the
-//    work and its table reads for every query tile of the head.
+//  * with RoPE the queries and keys arrive already rotated from a pass of
+//    their own (rope_rows.cu): rotating K tiles where they land would repeat the
+//    work for every query tile of the head, and rotating each Q tile where it
+//    lands put the rotation on the MMA warp's path at every job start.
 //
 // Every wait is bounded (common.cuh); on a timeout the CTA records the status,
 // drains its in-flight copies and MMAs, frees TMEM and exits.
@@ -45,7 +44,6 @@
 
 #include "common.cuh"
 #include "kernels.h"
-#include "rope.cuh"
 #include "tcgen05.cuh"
 #include "tmap.h"
 
@@ -62,7 +60,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: p <= 2^8 between rescales
 
-template <int D, bool ROPE>
+template <int D>
 struct Cfg {
   // Warp roles.  D = 64: 10 warps -- TMA, MMA, then a 4-warp softmax group per query tile (warps 2-5, 6-9).
   // D = 128: 12 warps with a register split -- warpgroup 0 holds the TMA and MMA warps (warps 2-3 idle) and
@@ -91,8 +89,8 @@ struct Cfg {
   static constexpr int OFF_V = OFF_K + NSK * TILE_BYTES;
   static constexpr int OFF_BAR = OFF_V + NSV * TILE_BYTES;
   // barriers: q_full, q_empty, k_full[NSK], v_full[NSV], k_empty[NSK], v_empty[NSV], s_full[NQ], p_full[NQ],
-  // o_done[NQ], drain, q_ready
-  static constexpr int NBAR = 2 + 2 * NSK + 2 * NSV + 3 * NQ + 2;
+  // o_done[NQ], drain
+  static constexpr int NBAR = 2 + 2 * NSK + 2 * NSV + 3 * NQ + 1;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // tmem address, abort flag
   static constexpr int SMEM_USED = OFF_MISC + 16;
   static constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // slack to align the base to 1024
@@ -125,7 +123,6 @@ struct PrefillArgs {
   int total_items;   // B * Hq * ns
   int total_q, total_k;  // packed layout: rows of q/out and of k/v
   unsigned* status;
-  RopeArgs rope;         // style != 0: the softmax groups rotate their q rows (k arrives rotated)
   int fault_skip_arrive; // test hook (see launch_prefill's caller): CTA 0 withholds one P-ready arrival
 };
 
@@ -197,11 +194,11 @@ __device__ __forceinline__ bool make_job(const PrefillArgs& a, int item, int hal
   return true;
 }
 
-template <int D, bool ROPE>
-__global__ void __launch_bounds__(Cfg<D, ROPE>::THREADS, 1)
+template <int D>
+__global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     prefill_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                        const __grid_constant__ CUtensorMap tmv, const PrefillArgs a) {
-  using C = Cfg<D, ROPE>;
+  using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* Qs = smem + C::OFF_Q;
@@ -218,18 +215,16 @@ __global__ void __launch_bounds__(Cfg<D, ROPE>::THREADS, 1)
   uint64_t* p_full = s_full + NQ;
   uint64_t* o_done = p_full + NQ;
   uint64_t* drain = o_done + NQ;
-  uint64_t* q_ready = drain + 1;    // with RoPE: both Q tiles of the job rotated (one arrival per softmax thread)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  constexpr bool rope = ROPE;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::NBAR; ++i) {
       const bool is_p = (&bars[i] >= p_full) && (&bars[i] < p_full + NQ);
-      mbar_init(&bars[i], is_p ? 128 : (&bars[i] == q_ready ? 128 * NQ : 1));
+      mbar_init(&bars[i], is_p ? 128 : 1);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -353,8 +348,7 @@ __global__ void __launch_bounds__(Cfg<D, ROPE>::THREADS, 1)
           Job jb;
           if (!make_job(a, item, half, jb) || jb.n == 0) continue;
           const int g0 = kv;
-          // with RoPE, wait for the rotated Q tiles and K slots instead of the raw ones
-          if (!mbar_wait(rope ? q_ready : q_full, qjobs & 1, a.status, abort_flag) ||
+          if (!mbar_wait(q_full, qjobs & 1, a.status, abort_flag) ||
               !mbar_wait(&k_full[g0 % C::NSK], (g0 / C::NSK) & 1, a.status,
                          abort_flag)) {
             ok = false;
@@ -424,7 +418,6 @@ __global__ void __launch_bounds__(Cfg<D, ROPE>::THREADS, 1)
     const uint32_t s_addr = tbase + lane_addr + C::tm_s(t);
     const uint32_t o_addr = tbase + lane_addr + C::tm_o(t);
     int ss = 0;  // S steps of this tile consumed so far (s_full / o_done phases)
-    int qj = 0;  // jobs with work seen (q_full / q_ready phases)
     bool ok = true;
 
     for (int item = blockIdx.x; ok && item < a.total_items; item += gridDim.x) {
@@ -432,28 +425,6 @@ __global__ void __launch_bounds__(Cfg<D, ROPE>::THREADS, 1)
         Job jb;
         if (!make_job(a, item, half, jb)) continue;
         const int q0 = jb.q00 + t * BM;
-        if (rope && jb.n > 0) {
-          // Rotate this thread's query row of tile t to position qi + (Lkv - Lq), then hand the tiles to the
-          // MMA warp (every softmax thread arrives, also for a tile past the sequence end).
-          if (!mbar_wait(q_full, qj & 1, a.status, abort_flag)) {
-            ok = false;
-            break;
-          }
-          const int qi_r = q0 + row;
-          if (jb.nt[t] > 0 && qi_r < jb.Lq_s) {
-            const int pos = qi_r + jb.off;
-            if (pos < 0) {
-              record_status(a.status, ATTN_ERR_DEVICE_BOUNDS);  // a packed sequence with more queries than keys
-            } else {
-              const size_t off = (size_t)pos * (D / 2);
-              rope_rotate_row_sw128<D>(Qs + t * C::TILE_BYTES, C::BLOCK_BYTES, row, a.rope.cos + off,
-                                       a.rope.sin + off, a.rope.style);
-            }
-          }
-          fence_proxy_async_smem();
-          mbar_arrive(q_ready);
-        }
-        if (jb.n > 0) ++qj;
         if (q0 >= jb.Lq_s) continue;                    // this tile lies past the sequence end
         const int qi = q0 + row;                         // query index within its sequence
         const int horizon = qi + jb.off;                 // last visible key under the causal mask
@@ -615,23 +586,23 @@ __global__ void __launch_bounds__(Cfg<D, ROPE>::THREADS, 1)
   }
 }
 
-template <int D, bool ROPE>
+template <int D>
 cudaError_t launch_d(const PrefillLaunch& p) {
-  using C = Cfg<D, ROPE>;
+  using C = Cfg<D>;
   static bool attr_set[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!attr_set[dev]) {
-    e = cudaFuncSetAttribute(prefill_fwd_kernel<D, ROPE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(prefill_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
     if (C::SPLIT) {
       // the kernel's register split assumes this many registers per thread at launch: refuse to launch a
       // build that compiled to another count rather than let an increase wait for registers that never come
       cudaFuncAttributes fa;
-      e = cudaFuncGetAttributes(&fa, prefill_fwd_kernel<D, ROPE>);
+      e = cudaFuncGetAttributes(&fa, prefill_fwd_kernel<D>);
       if (e != cudaSuccess) return e;
       if (fa.numRegs != C::LAUNCH_REGS) return cudaErrorInvalidKernelImage;
     }
@@ -685,7 +656,6 @@ cudaError_t launch_d(const PrefillLaunch& p) {
   a.total_q = p.total_q;
   a.total_k = p.total_k;
   a.status = p.status;
-  a.rope = p.rope;
   a.fault_skip_arrive = p.fault_skip_arrive;
   const long long items = (long long)p.B * p.Hq * a.ns;
   if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
@@ -694,16 +664,15 @@ cudaError_t launch_d(const PrefillLaunch& p) {
   int grid = persistent ? (p.num_sms > 0 ? p.num_sms : 148) : a.total_items;
   if (grid > a.total_items) grid = a.total_items;
   if (grid < 1) grid = 1;
-  prefill_fwd_kernel<D, ROPE><<<grid, C::THREADS, C::SMEM_ALLOC, p.stream>>>(tmq, tmk, tmv, a);
+  prefill_fwd_kernel<D><<<grid, C::THREADS, C::SMEM_ALLOC, p.stream>>>(tmq, tmk, tmv, a);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_prefill(const PrefillLaunch& p) {
-  const bool rope = p.rope.style != 0;
-  if (p.D == 64) return rope ? launch_d<64, true>(p) : launch_d<64, false>(p);
-  if (p.D == 128) return rope ? launch_d<128, true>(p) : launch_d<128, false>(p);
+  if (p.D == 64) return launch_d<64>(p);
+  if (p.D == 128) return launch_d<128>(p);
   return cudaErrorNotSupported;
 }
 

@@ -1,24 +1,29 @@
-// rope_k.cu -- rotary position embedding of the keys of a prefill call, once
-// per call, before the attention kernel reads them.
+// rope_rows.cu -- rotary position embedding of the keys and of the queries of
+// a prefill call, one pass each per call, before the attention kernel reads
+// them.
 //
 // The rotation is the one of rope.cuh (pair i of a row at position p, (a, b),
 // becomes (a cos - b sin, b cos + a sin) with cos, sin from row p of the
 // caller's fp32 tables; pairs (i, i + D/2) or (2i, 2i + 1); fp32 arithmetic,
-// bf16 result).  Key j of a sequence sits at position j.
+// bf16 result).  Key j of a sequence sits at position j, query i at
+// i + Lkv - Lq (the causal alignment).
 //
-// Why a pass of its own: in a causal prefill every K tile of a head is read by
-// every query-tile job of that head; rotating it where it lands in shared
+// Why passes of their own: in a causal prefill every K tile of a head is read
+// by every query-tile job of that head; rotating it where it lands in shared
 // memory repeats the rotation (and the cos/sin reads, 2x the tile's bytes) for
 // every visit and made the attention kernel L2-bound (measured 2.3x slower).
-// One pass reads K and the tables once and writes the rotated keys -- which a
-// serving engine wants anyway for its KV cache -- and the attention kernel
-// then streams them like unrotated keys.  Queries are still rotated on load
-// (each Q tile is loaded once per job).
+// A Q tile is loaded once per job, but rotating it where it lands put the
+// rotation on the MMA warp's path at every job start (the causal 4k call took
+// 570 us that way, 526 us with this pass).  Each pass reads its tensor and
+// the tables once and writes the rotated rows -- the keys a serving engine
+// wants anyway for its KV cache -- and the attention kernel then streams them
+// like unrotated ones.
 //
-// Layout: dense k [B, Hkv, L, D] (row r of head (b, h) at position r), or
-// packed k [total, Hkv, D] with cu_seqlens (token t of sequence s at position
-// t - cu[s]).  Each thread rotates eight pairs of one row with 16-byte loads
-// and stores; a warp covers whole rows, so global accesses are coalesced.
+// Layout: dense [B, H, L, D] (row r of head (b, h) at position r + pos_off),
+// or packed [total, H, D] with cu_seqlens (token t of sequence s at position
+// t - cu[s], plus that sequence's Lkv - Lq for queries).  Each thread rotates
+// eight pairs of one row with 16-byte loads and stores; a warp covers whole
+// rows, so global accesses are coalesced.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -45,7 +50,7 @@ __device__ __forceinline__ uint4 pack8f(const float (&f)[8]) {
 
 // One thread = one group of eight pairs of one row: TPR threads per row.
 template <int D>
-__global__ void __launch_bounds__(256) rope_k_kernel(const RopeKLaunch p, long long nrows) {
+__global__ void __launch_bounds__(256) rope_rows_kernel(const RopeRowsLaunch p, long long nrows) {
   constexpr int NP = D / 2;
   constexpr int TPR = NP / 8;  // threads per row
   const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -54,23 +59,24 @@ __global__ void __launch_bounds__(256) rope_k_kernel(const RopeKLaunch p, long l
   if (row >= nrows) return;
   // position of the row within its sequence
   long long pos;
-  if (p.cu_k == nullptr) {
-    pos = row % p.L;  // [B, Hkv, L, D]
+  if (p.cu == nullptr) {
+    pos = row % p.L + p.pos_off;  // [B, H, L, D]
   } else {
-    const long long tok = row / p.Hkv;  // [total, Hkv, D]
-    int lo = 0, hi = p.B;               // the sequence s with cu[s] <= tok < cu[s + 1]
+    const long long tok = row / p.H;  // [total, H, D]
+    int lo = 0, hi = p.B;             // the sequence s with cu[s] <= tok < cu[s + 1]
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
-      if (p.cu_k[mid] <= tok) lo = mid; else hi = mid;
+      if (p.cu[mid] <= tok) lo = mid; else hi = mid;
     }
-    pos = tok - p.cu_k[lo];
+    pos = tok - p.cu[lo];
+    if (p.cu_kv != nullptr) pos += (long long)(p.cu_kv[lo + 1] - p.cu_kv[lo]) - (p.cu[lo + 1] - p.cu[lo]);
   }
   if (pos < 0 || pos >= p.rope.max_pos) {
     record_status(p.status, ATTN_ERR_DEVICE_BOUNDS);
     pos = pos < 0 ? 0 : p.rope.max_pos - 1;
   }
-  const __nv_bfloat16* src = reinterpret_cast<const __nv_bfloat16*>(p.k) + row * D;
-  __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.k_out) + row * D;
+  const __nv_bfloat16* src = reinterpret_cast<const __nv_bfloat16*>(p.src) + row * D;
+  __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.dst) + row * D;
   const float* crow = p.rope.cos + pos * NP;
   const float* srow = p.rope.sin + pos * NP;
   if (p.rope.style == 1) {
@@ -112,17 +118,17 @@ __global__ void __launch_bounds__(256) rope_k_kernel(const RopeKLaunch p, long l
 
 }  // namespace
 
-cudaError_t launch_rope_k(const RopeKLaunch& p) {
-  const long long nrows = p.cu_k == nullptr ? (long long)p.B * p.Hkv * p.L : (long long)p.total_k * p.Hkv;
+cudaError_t launch_rope_rows(const RopeRowsLaunch& p) {
+  const long long nrows = p.cu == nullptr ? (long long)p.B * p.H * p.L : (long long)p.total * p.H;
   if (nrows <= 0) return cudaSuccess;
   const int tpr = p.D / 16;
   const long long threads = nrows * tpr;
   const long long blocks = (threads + 255) / 256;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
   if (p.D == 64)
-    rope_k_kernel<64><<<(unsigned)blocks, 256, 0, p.stream>>>(p, nrows);
+    rope_rows_kernel<64><<<(unsigned)blocks, 256, 0, p.stream>>>(p, nrows);
   else if (p.D == 128)
-    rope_k_kernel<128><<<(unsigned)blocks, 256, 0, p.stream>>>(p, nrows);
+    rope_rows_kernel<128><<<(unsigned)blocks, 256, 0, p.stream>>>(p, nrows);
   else
     return cudaErrorNotSupported;
   return cudaGetLastError();

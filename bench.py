@@ -321,8 +321,8 @@ class PrefillCase(_Rotation, _RopeMixin):
         self.unit, self.kind = "TFLOP/s", "tensor"
         self.kernel = "prefill_fwd"
         self.kernel_desc = "prefill_fwd_kernel (one attn_fwd call, event-timed)"
-        # with RoPE a call launches the key-rotation pass, then the attention kernel
-        self.launches_per_step = 2 if self.rope_style else 1
+        # with RoPE a call launches the key- and query-rotation passes, then the attention kernel
+        self.launches_per_step = 3 if self.rope_style else 1
         self.h2d = sum(t.numel() * t.element_size() for t in self.host)
         self.d2h = self.out.numel() * self.out.element_size() + self.lse.numel() * 4
         self.touch_bytes = self.h2d + self.d2h  # q, k, v read and O, lse written once per step (at least)

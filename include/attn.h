@@ -80,8 +80,8 @@ typedef enum attn_dtype { ATTN_DTYPE_BF16 = 0, ATTN_DTYPE_F32 = 1 } attn_dtype;
  * ATTN_ERR_INVALID_ARG; a packed sequence with more queries than keys is
  * flagged ATTN_ERR_DEVICE_BOUNDS).  The keys are rotated once per call by a
  * pass of their own into k_out (or the library workspace, grown like the
- * decode workspace and shared with it), then the attention kernel streams
- * them; each query tile is rotated where it lands in shared memory.  Decode:
+ * decode workspace and shared with it), the queries by a second pass into the
+ * workspace, then the attention kernel streams the rotated copies.  Decode:
  * only the query is rotated, to kv_len - 1 (token t of attn_decode_multi to
  * kv_len - Lq + t); cached keys must be stored already rotated.  Every
  * position must be below max_pos: calls whose Lkv (prefill) or Lmax (decode)
