@@ -219,7 +219,7 @@ def attn_fwd(q, k, v, out=None, lse=None, causal=True, scale=None, out_dtype=tor
              want_lse=True, stream=None, rope=None):
     """Dense prefill: q [B,Hq,Lq,D], k/v [B,Hkv,Lkv,D] bf16 -> (out [B,Hq,Lq,D], lse [B,Hq,Lq] fp32).
 
-    ``rope = (cos, sin, style)`` rotates q and k in the kernel (fp32 device tables [max_pos, D/2];
+    ``rope = (cos, sin, style)`` rotates q and k inside the call (fp32 device tables [max_pos, D/2];
     style "half" or "interleaved"); every call of this module takes the same argument."""
     _need(q, "q", torch.bfloat16, 4)
     _need(k, "k", torch.bfloat16, 4)

@@ -1,8 +1,8 @@
 """GPU parity of the fused rotary position embedding against the fp64 oracle.
 
-Prefill rotates each q tile where it lands (the softmax warps) and the keys
-once per call in a pass of their own (optionally into a caller buffer, which
-is checked too); the decode kernels rotate only the query (the cache holds
+Prefill rotates the keys (optionally into a caller buffer, which is checked
+too) and the queries once per call, in a pass each, before the attention
+kernel; the decode kernels rotate only the query (the cache holds
 keys already rotated, so any cache contents serve).  Both pair layouts, both
 head dims, Lq < Lkv (queries placed at Lkv - Lq + i), packed sequences, paged
 caches, multi-token decode and the causal prefill workload at full size
