@@ -65,6 +65,42 @@ def test_prefill_rope_varlen(style):
     assert_attn_close(out.cpu(), lse.cpu(), O_ref, lse_ref)
 
 
+@pytest.mark.parametrize("style", ["half", "interleaved"])
+def test_prefill_rope_varlen_fewer_queries_than_keys(style):
+    # each packed sequence places its queries at Lkv_s - Lq_s + i: the query pass shifts every sequence by its own
+    # offset (0, 66, 6 and 160 here)
+    q_lens, k_lens = [5, 64, 1, 100], [5, 130, 7, 260]
+    q, _, _, cu_q = make_varlen(4, 8, 2, 128, seed=71, seqlens=q_lens)
+    _, k, v, cu_k = make_varlen(4, 8, 2, 128, seed=72, seqlens=k_lens)
+    cos, sin, cos_d, sin_d = tables(300, 128)
+    AB.attn_get_device_status()
+    out, lse = AB.attn_fwd_varlen(q.to(DEV), k.to(DEV), v.to(DEV), cu_q.to(DEV), cu_k.to(DEV), max(q_lens),
+                                  max(k_lens), causal=True, rope=(cos_d, sin_d, style))
+    torch.cuda.synchronize()
+    assert AB.attn_get_device_status() == AB.ATTN_OK
+    O_ref, lse_ref = oracle.attention_varlen(q, k, v, cu_q.tolist(), cu_k.tolist(), 128 ** -0.5, True,
+                                             rope=(cos, sin, style))
+    assert_attn_close(out.cpu(), lse.cpu(), O_ref, lse_ref)
+
+
+def test_prefill_rope_varlen_more_queries_than_keys_is_flagged():
+    # a packed sequence with more queries than keys would place its first queries before position 0: the call
+    # reports ATTN_ERR_DEVICE_BOUNDS (its rows are then not meaningful) and the other sequences are unaffected
+    q_lens, k_lens = [40, 64], [64, 20]
+    q, _, _, cu_q = make_varlen(2, 4, 2, 128, seed=73, seqlens=q_lens)
+    _, k, v, cu_k = make_varlen(2, 4, 2, 128, seed=74, seqlens=k_lens)
+    cos, sin, cos_d, sin_d = tables(100, 128)
+    AB.attn_get_device_status()
+    out, lse = AB.attn_fwd_varlen(q.to(DEV), k.to(DEV), v.to(DEV), cu_q.to(DEV), cu_k.to(DEV), 64, 64,
+                                  causal=True, rope=(cos_d, sin_d, "half"))
+    torch.cuda.synchronize()
+    assert AB.attn_get_device_status() == AB.ATTN_ERR_DEVICE_BOUNDS
+    O_ref, lse_ref = oracle.attention_varlen(q[:40], k[:64], v[:64], [0, 40], [0, 64], 128 ** -0.5, True,
+                                             rope=(cos, sin, "half"))
+    assert_attn_close(out[:40].cpu(), lse[:40].cpu(), O_ref, lse_ref)
+    assert AB.attn_get_device_status() == AB.ATTN_OK
+
+
 def test_prefill_rope_writes_rotated_keys():
     # k_out receives the rotated keys (what a serving engine appends to its cache): the oracle's rotation held in
     # bf16, up to a last-bit difference where fp32 and fp64 arithmetic round to different neighbours
