@@ -54,7 +54,7 @@ __global__ void __launch_bounds__(256) rope_rows_kernel(const RopeRowsLaunch p, 
   constexpr int NP = D / 2;
   constexpr int TPR = NP / 8;  // threads per row
   const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  const long long row = tid / TPR;  // row of k in memory order
+  const long long row = tid / TPR;  // row in memory order
   const int grp = (int)(tid % TPR);
   if (row >= nrows) return;
   // position of the row within its sequence
