@@ -13,7 +13,12 @@ from tests.test_oracle_pins import PINS
 
 _orig = {name: getattr(OA, name) for name in
          ("scores", "visible_mask", "kv_head_of", "softmax_two_pass", "log_sum_exp", "attention_head",
-          "decode_multi", "rope_rotate", "_rope_q_k")}
+          "decode_multi", "rope_rotate", "_rope_q_k", "attention_varlen")}
+
+
+def _varlen_keys_at_query_offsets(q, k, v, cu_seqlens_q, cu_seqlens_k, scale, causal, rope=None):
+    # each packed sequence's keys sliced with the query offsets (right only while the two layouts coincide)
+    return _orig["attention_varlen"](q, k, v, cu_seqlens_q, cu_seqlens_q, scale, causal, rope=rope)
 
 
 def _rope_backwards(x, positions, cos, sin, style):
@@ -115,6 +120,7 @@ MUTATIONS = {
     "rope_query_from_zero": ("_rope_q_k", _rope_query_from_zero),
     "rope_keys_not_rotated": ("_rope_q_k", _rope_keys_not_rotated),
     "rope_unrounded": ("_rope_q_k", _rope_unrounded),
+    "varlen_keys_at_query_offsets": ("attention_varlen", _varlen_keys_at_query_offsets),
 }
 
 

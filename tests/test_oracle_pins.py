@@ -430,7 +430,8 @@ def pin_rope_multi_tokens_are_prefill_rows():
 
 
 def pin_rope_rows_and_varlen_agree_with_dense():
-    """The row-sampled and packed forms rotate with the same positions as dense prefill."""
+    """The row-sampled and packed forms rotate with the same positions as dense prefill, also when a packed
+    sequence has fewer queries than keys."""
     r = _rng(175)
     Hq, Hkv, D = 4, 2, 8
     cos, sin = _tables(32, D)
@@ -449,6 +450,21 @@ def pin_rope_rows_and_varlen_agree_with_dense():
         np.testing.assert_allclose(Orr, Od[0, 3, rows], atol=1e-13)
         Ovr, lvr = OA.attention_varlen_rows(q, k, v, cu, cu, 0.5, True, s, 3, rows, rope=rope)
         np.testing.assert_allclose(Ovr, Od[0, 3, rows], atol=1e-13)
+    # fewer queries than keys in each sequence: the packed forms place sequence s's queries at Lkv_s - Lq_s + i
+    # of that sequence alone, as dense prefill does for the same slices
+    q_lens, k_lens = [4, 11], [9, 14]
+    cq, ck = [0, 4, 15], [0, 9, 23]
+    q = r.standard_normal((15, Hq, D))
+    Ov, lv = OA.attention_varlen(q, k, v, cq, ck, 0.5, True, rope=rope)
+    for s in range(2):
+        qd = q[cq[s]:cq[s + 1]].transpose(1, 0, 2)[None]
+        kd, vd = (x[ck[s]:ck[s + 1]].transpose(1, 0, 2)[None] for x in (k, v))
+        Od, ld = OA.attention(qd, kd, vd, 0.5, True, rope=rope)
+        np.testing.assert_allclose(Ov[cq[s]:cq[s + 1]].transpose(1, 0, 2), Od[0], atol=1e-13)
+        np.testing.assert_allclose(lv[cq[s]:cq[s + 1]].T, ld[0], atol=1e-13)
+        rows = np.array([0, q_lens[s] - 1])
+        Ovr, lvr = OA.attention_varlen_rows(q, k, v, cq, ck, 0.5, True, s, 1, rows, rope=rope)
+        np.testing.assert_allclose(Ovr, Od[0, 1, rows], atol=1e-13)
 
 
 PINS = [
