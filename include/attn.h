@@ -81,7 +81,11 @@ typedef enum attn_dtype { ATTN_DTYPE_BF16 = 0, ATTN_DTYPE_F32 = 1 } attn_dtype;
  * flagged ATTN_ERR_DEVICE_BOUNDS).  The keys are rotated once per call by a
  * pass of their own into k_out (or the library workspace, grown like the
  * decode workspace and shared with it), the queries by a second pass into the
- * workspace, then the attention kernel streams the rotated copies.  Decode:
+ * workspace, then the attention kernel streams the rotated copies.  Such a
+ * call needs 256 KiB + (k_out ? 0 : rows of k * D * 2) + rows of q * D * 2
+ * bytes of workspace; during CUDA graph capture it is never grown (make one
+ * uncaptured call with the largest sizes first), and calls that can overlap
+ * on the GPU race on it, as decode calls do.  Decode:
  * only the query is rotated, to kv_len - 1 (token t of attn_decode_multi to
  * kv_len - Lq + t); cached keys must be stored already rotated.  Every
  * position must be below max_pos: calls whose Lkv (prefill) or Lmax (decode)
