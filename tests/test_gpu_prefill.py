@@ -49,6 +49,8 @@ def run(q, k, v, causal, scale=None, out_dtype=torch.bfloat16):
     (1, 2, 1, 1, 77, 128, True),       # a single query row
     (1, 2, 2, 64, 1, 128, False),      # a single key
     (2, 2, 2, 256, 640, 128, False),   # several K tiles, exact multiples
+    (1, 16, 1, 300, 300, 64, True),    # multi-query: 16 heads on one kv head
+    (2, 16, 2, 200, 450, 128, False),  # 8 heads per kv head, Lq < Lkv, non-causal
 ])
 def test_prefill_small(B, Hq, Hkv, Lq, Lkv, D, causal):
     q, k, v = make_prefill(B, Hq, Hkv, Lq, Lkv, D, seed=Lq * 7 + Lkv)
