@@ -4,13 +4,17 @@
  * It makes seeded inputs (a 32-bit linear congruential generator mapped to [-2, 2), rounded to bf16), allocates
  * its own device buffers with the CUDA runtime, and runs
  *   - one causal GQA prefill through attn_fwd (B=1, Hq=4, Hkv=2, L=200, D=128: a ragged second tile), and
- *   - one GQA decode through attn_decode (B=3, Hq=16, Hkv=4, Lmax=300, D=128, kv_lens 300, 77, 1),
+ *   - one GQA decode through attn_decode (B=3, Hq=16, Hkv=4, Lmax=300, D=128, kv_lens 300, 77, 1), and
+ *   - one packed causal prefill with rotary embedding through attn_fwd_ex and its parameter struct (two
+ *     sequences of 70 and 130 queries over 100 and 130 keys, Hq=4, Hkv=2, D=64, fp32 output, rotated keys
+ *     returned in a caller buffer; cos/sin tables of p * 10000^(-2i/D) computed here),
  * checks the status codes (and that a call with an unsupported head dim is refused before any launch), and
  * writes every input and output as a raw little-endian file into the directory given as argv[1]: the test that
  * builds and runs this program compares the outputs with the fp64 oracle.
  *
  * Exit status 0 on success; otherwise a message on stderr.
  */
+#include <math.h>
 #include <stdint.h>
 #include <stdio.h>
 #include <stdlib.h>
@@ -142,7 +146,87 @@ int main(int argc, char** argv) {
     cudaFree(dq); cudaFree(dk); cudaFree(dv); cudaFree(dout); cudaFree(dlse); cudaFree(dlens);
     free(hq); free(hk); free(hv); free(hout); free(hlse);
   }
+  /* ---- packed prefill with RoPE through attn_fwd_ex ---- */
+  {
+    const int Hq = 4, Hkv = 2, D = 64, maxpos = 160;
+    const int cu_q[3] = {0, 70, 200}, cu_k[3] = {0, 100, 230};
+    const int total_q = 200, total_k = 230;
+    const size_t nq = (size_t)total_q * Hq * D, nk = (size_t)total_k * Hkv * D, nl = (size_t)total_q * Hq;
+    const size_t nt = (size_t)maxpos * (D / 2);
+    uint16_t *hq, *hk, *hv;
+    void *dq, *dk, *dv, *dkout;
+    float *dout, *dlse, *dcos, *dsin;
+    int *dcuq, *dcuk;
+    float* hcos = (float*)malloc(nt * sizeof(float));
+    float* hsin = (float*)malloc(nt * sizeof(float));
+    if (hcos == NULL || hsin == NULL) return 1;
+    for (int p = 0; p < maxpos; ++p)
+      for (int i = 0; i < D / 2; ++i) {
+        const double a = (double)p * pow(10000.0, -2.0 * i / D);
+        hcos[(size_t)p * (D / 2) + i] = (float)cos(a);
+        hsin[(size_t)p * (D / 2) + i] = (float)sin(a);
+      }
+    if (!make_bf16(nq, &hq, &dq) || !make_bf16(nk, &hk, &dk) || !make_bf16(nk, &hv, &dv)) return 1;
+    if (!cuda_ok(cudaMalloc((void**)&dout, nq * sizeof(float)), "cudaMalloc") ||
+        !cuda_ok(cudaMalloc((void**)&dlse, nl * sizeof(float)), "cudaMalloc") ||
+        !cuda_ok(cudaMalloc(&dkout, nk * sizeof(uint16_t)), "cudaMalloc") ||
+        !cuda_ok(cudaMalloc((void**)&dcos, nt * sizeof(float)), "cudaMalloc") ||
+        !cuda_ok(cudaMalloc((void**)&dsin, nt * sizeof(float)), "cudaMalloc") ||
+        !cuda_ok(cudaMalloc((void**)&dcuq, sizeof cu_q), "cudaMalloc") ||
+        !cuda_ok(cudaMalloc((void**)&dcuk, sizeof cu_k), "cudaMalloc") ||
+        !cuda_ok(cudaMemcpy(dcos, hcos, nt * sizeof(float), cudaMemcpyHostToDevice), "cudaMemcpy") ||
+        !cuda_ok(cudaMemcpy(dsin, hsin, nt * sizeof(float), cudaMemcpyHostToDevice), "cudaMemcpy") ||
+        !cuda_ok(cudaMemcpy(dcuq, cu_q, sizeof cu_q, cudaMemcpyHostToDevice), "cudaMemcpy") ||
+        !cuda_ok(cudaMemcpy(dcuk, cu_k, sizeof cu_k, cudaMemcpyHostToDevice), "cudaMemcpy"))
+      return 1;
+    attn_fwd_params p;
+    memset(&p, 0, sizeof p);
+    p.q = dq;
+    p.k = dk;
+    p.v = dv;
+    p.out = dout;
+    p.lse = dlse;
+    p.B = 2;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.Lq = 130;
+    p.Lkv = 130;
+    p.D = D;
+    p.scale = 0.125f;
+    p.causal = 1;
+    p.out_dtype = ATTN_DTYPE_F32;
+    p.cu_seqlens_q = dcuq;
+    p.cu_seqlens_k = dcuk;
+    p.total_q = total_q;
+    p.total_k = total_k;
+    p.stream = NULL;
+    p.rope.cos = dcos;
+    p.rope.sin = dsin;
+    p.rope.max_pos = maxpos;
+    p.rope.style = ATTN_ROPE_HALF;
+    p.rope.k_out = dkout;
+    st = attn_fwd_ex(&p);
+    if (st != ATTN_OK) return fail("attn_fwd_ex (packed, RoPE)", st);
+    st = attn_get_device_status(NULL);
+    if (st != ATTN_OK) return fail("attn_get_device_status after attn_fwd_ex", st);
+    float* hout = (float*)malloc(nq * sizeof(float));
+    float* hlse = (float*)malloc(nl * sizeof(float));
+    uint16_t* hkout = (uint16_t*)malloc(nk * sizeof(uint16_t));
+    if (hout == NULL || hlse == NULL || hkout == NULL) return 1;
+    if (!cuda_ok(cudaMemcpy(hout, dout, nq * sizeof(float), cudaMemcpyDeviceToHost), "cudaMemcpy") ||
+        !cuda_ok(cudaMemcpy(hlse, dlse, nl * sizeof(float), cudaMemcpyDeviceToHost), "cudaMemcpy") ||
+        !cuda_ok(cudaMemcpy(hkout, dkout, nk * sizeof(uint16_t), cudaMemcpyDeviceToHost), "cudaMemcpy"))
+      return 1;
+    if (!write_file(dir, "rope_q.bf16", hq, nq * 2) || !write_file(dir, "rope_k.bf16", hk, nk * 2) ||
+        !write_file(dir, "rope_v.bf16", hv, nk * 2) || !write_file(dir, "rope_cos.f32", hcos, nt * 4) ||
+        !write_file(dir, "rope_sin.f32", hsin, nt * 4) || !write_file(dir, "rope_out.f32", hout, nq * 4) ||
+        !write_file(dir, "rope_lse.f32", hlse, nl * 4) || !write_file(dir, "rope_kout.bf16", hkout, nk * 2))
+      return 1;
+    cudaFree(dq); cudaFree(dk); cudaFree(dv); cudaFree(dout); cudaFree(dlse); cudaFree(dkout);
+    cudaFree(dcos); cudaFree(dsin); cudaFree(dcuq); cudaFree(dcuk);
+    free(hq); free(hk); free(hv); free(hout); free(hlse); free(hkout); free(hcos); free(hsin);
+  }
   attn_release_workspace();
-  printf("c_abi_client: prefill and decode ran through the C ABI\n");
+  printf("c_abi_client: prefill, decode and packed RoPE prefill ran through the C ABI\n");
   return 0;
 }

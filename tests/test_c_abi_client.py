@@ -28,8 +28,8 @@ def compile_client(out_dir):
     cmd = [gcc, "-std=c11", "-Wall", "-Wextra", "-Werror", "-pedantic", "-O2",
            os.path.join(ROOT, "tests", "c_abi_client.c"), "-I", os.path.join(ROOT, "include"),
            "-I", os.path.join(CUDA, "include"), "-L", libdir, "-l:" + os.path.basename(LIB),
-           "-L", os.path.join(CUDA, "lib64"), "-lcudart", f"-Wl,-rpath,{libdir}:{os.path.join(CUDA, 'lib64')}",
-           "-o", exe]
+           "-L", os.path.join(CUDA, "lib64"), "-lcudart", "-lm",
+           f"-Wl,-rpath,{libdir}:{os.path.join(CUDA, 'lib64')}", "-o", exe]
     r = subprocess.run(cmd, capture_output=True, text=True)
     assert r.returncode == 0, r.stdout + r.stderr
     return exe
@@ -70,3 +70,22 @@ def test_c_client_matches_oracle(tmp_path):
     out, lse = _bf16(f("decode_out.bf16"), (3, 16, 128)), _f32(f("decode_lse.f32"), (3, 16))
     O_ref, lse_ref = oracle.decode(q, kc, vc, lens, 128 ** -0.5)
     assert_attn_close(out, lse, O_ref, lse_ref, "C client decode")
+    # packed causal prefill with RoPE through attn_fwd_ex: sequences of 70 / 130 queries over 100 / 130 keys,
+    # Hq=4, Hkv=2, D=64, fp32 output, scale 0.125, rotated keys returned in k_out
+    cu_q, cu_k = [0, 70, 200], [0, 100, 230]
+    q, k, v = _bf16(f("rope_q.bf16"), (200, 4, 64)), _bf16(f("rope_k.bf16"), (230, 2, 64)), \
+        _bf16(f("rope_v.bf16"), (230, 2, 64))
+    cos, sin = _f32(f("rope_cos.f32"), (160, 32)), _f32(f("rope_sin.f32"), (160, 32))
+    out, lse = _f32(f("rope_out.f32"), (200, 4, 64)), _f32(f("rope_lse.f32"), (200, 4))
+    O_ref, lse_ref = oracle.attention_varlen(q, k, v, cu_q, cu_k, 0.125, True, rope=(cos, sin, "half"))
+    assert_attn_close(out, lse, O_ref, lse_ref, "C client packed RoPE prefill")
+    # the rotated keys: each sequence's key j at position j, held in bf16 (one bf16 step of slack where fp32
+    # and fp64 arithmetic round to different neighbours)
+    kout = _bf16(f("rope_kout.bf16"), (230, 2, 64)).double().numpy()
+    kd = k.double().numpy()
+    for s in range(2):
+        a, e = cu_k[s], cu_k[s + 1]
+        want = oracle.round_bf16(oracle.rope_rotate(kd[a:e].transpose(1, 0, 2), np.arange(e - a), cos, sin, "half"))
+        got = kout[a:e].transpose(1, 0, 2)
+        assert np.all(np.abs(got - want) <= np.abs(want) * 2.0 ** -7 + 1e-30)
+        assert np.mean(got != want) < 1e-2
