@@ -205,7 +205,9 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS, DecodeCfg<D, GP>::M
       win_base = first_page;
       const int pg = first_page + lane;
       my_page = 0;
-      if (pg < p.max_pages) {
+      // only pages that hold keys of the sequence are read (and checked): entries past its last page may hold
+      // anything, e.g. the -1 a serving engine pads its block table with
+      if (pg < p.max_pages && (long long)pg * p.page_size < seq_len(b)) {
         const int id = p.block_table[(size_t)b * p.max_pages + pg];
         if (id < 0 || id >= p.num_pages) {
           record_status(p.status, ATTN_ERR_DEVICE_BOUNDS);  // out-of-pool page id: read page 0 instead

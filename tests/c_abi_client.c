@@ -8,6 +8,9 @@
  *   - one packed causal prefill with rotary embedding through attn_fwd_ex and its parameter struct (two
  *     sequences of 70 and 130 queries over 100 and 130 keys, Hq=4, Hkv=2, D=64, fp32 output, rotated keys
  *     returned in a caller buffer; cos/sin tables of p * 10000^(-2i/D) computed here),
+ *   - one multi-token decode through attn_decode_multi (B=2, Hq=8, Hkv=2, Lq=4, Lmax=200, D=128, kv_lens 200, 9),
+ *   - one paged decode through attn_decode_paged (B=2, Hq=8, Hkv=2, D=64, 16-key pages in a pool of 12, a
+ *     shuffled block table, kv_lens 100, 37),
  * checks the status codes (and that a call with an unsupported head dim is refused before any launch), and
  * writes every input and output as a raw little-endian file into the directory given as argv[1]: the test that
  * builds and runs this program compares the outputs with the fp64 oracle.
@@ -226,7 +229,111 @@ int main(int argc, char** argv) {
     cudaFree(dcos); cudaFree(dsin); cudaFree(dcuq); cudaFree(dcuk);
     free(hq); free(hk); free(hv); free(hout); free(hlse); free(hkout); free(hcos); free(hsin);
   }
+  /* ---- multi-token decode through attn_decode_multi ---- */
+  {
+    const int B = 2, Hq = 8, Hkv = 2, Lq = 4, Lmax = 200, D = 128;
+    const int lens[2] = {200, 9};
+    const size_t nq = (size_t)B * Hq * Lq * D, nc = (size_t)B * Hkv * Lmax * D, nl = (size_t)B * Hq * Lq;
+    uint16_t *hq, *hk, *hv;
+    void *dq, *dk, *dv, *dout;
+    int* dlens;
+    float* dlse;
+    if (!make_bf16(nq, &hq, &dq) || !make_bf16(nc, &hk, &dk) || !make_bf16(nc, &hv, &dv)) return 1;
+    if (!cuda_ok(cudaMalloc(&dout, nq * sizeof(uint16_t)), "cudaMalloc") ||
+        !cuda_ok(cudaMalloc((void**)&dlse, nl * sizeof(float)), "cudaMalloc") ||
+        !cuda_ok(cudaMalloc((void**)&dlens, sizeof lens), "cudaMalloc") ||
+        !cuda_ok(cudaMemcpy(dlens, lens, sizeof lens, cudaMemcpyHostToDevice), "cudaMemcpy"))
+      return 1;
+    attn_decode_multi_params p;
+    memset(&p, 0, sizeof p);
+    p.q = dq;
+    p.kcache = dk;
+    p.vcache = dv;
+    p.kv_lens = dlens;
+    p.out = dout;
+    p.lse = dlse;
+    p.B = B;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.Lq = Lq;
+    p.Lmax = Lmax;
+    p.D = D;
+    p.scale = 0.08838834764831845f;
+    p.out_dtype = ATTN_DTYPE_BF16;
+    st = attn_decode_multi(&p);
+    if (st != ATTN_OK) return fail("attn_decode_multi", st);
+    st = attn_get_device_status(NULL);
+    if (st != ATTN_OK) return fail("attn_get_device_status after attn_decode_multi", st);
+    uint16_t* hout = (uint16_t*)malloc(nq * sizeof(uint16_t));
+    float* hlse = (float*)malloc(nl * sizeof(float));
+    if (hout == NULL || hlse == NULL) return 1;
+    if (!cuda_ok(cudaMemcpy(hout, dout, nq * sizeof(uint16_t), cudaMemcpyDeviceToHost), "cudaMemcpy") ||
+        !cuda_ok(cudaMemcpy(hlse, dlse, nl * sizeof(float), cudaMemcpyDeviceToHost), "cudaMemcpy"))
+      return 1;
+    if (!write_file(dir, "multi_q.bf16", hq, nq * 2) || !write_file(dir, "multi_kc.bf16", hk, nc * 2) ||
+        !write_file(dir, "multi_vc.bf16", hv, nc * 2) || !write_file(dir, "multi_out.bf16", hout, nq * 2) ||
+        !write_file(dir, "multi_lse.f32", hlse, nl * 4))
+      return 1;
+    cudaFree(dq); cudaFree(dk); cudaFree(dv); cudaFree(dout); cudaFree(dlse); cudaFree(dlens);
+    free(hq); free(hk); free(hv); free(hout); free(hlse);
+  }
+
+  /* ---- paged decode through attn_decode_paged ---- */
+  {
+    const int B = 2, Hq = 8, Hkv = 2, D = 64, ps = 16, max_pages = 8, num_pages = 12;
+    const int lens[2] = {100, 37};
+    /* sequence 0 uses 7 pages, sequence 1 uses 3; unused entries hold -1 and are never read */
+    const int table[16] = {11, 3, 7, 0, 9, 5, 1, -1,
+                           6, 10, 2, -1, -1, -1, -1, -1};
+    const size_t nq = (size_t)B * Hq * D, npool = (size_t)num_pages * Hkv * ps * D, nl = (size_t)B * Hq;
+    uint16_t *hq, *hk, *hv;
+    void *dq, *dk, *dv, *dout;
+    int *dlens, *dtable;
+    float* dlse;
+    if (!make_bf16(nq, &hq, &dq) || !make_bf16(npool, &hk, &dk) || !make_bf16(npool, &hv, &dv)) return 1;
+    if (!cuda_ok(cudaMalloc(&dout, nq * sizeof(uint16_t)), "cudaMalloc") ||
+        !cuda_ok(cudaMalloc((void**)&dlse, nl * sizeof(float)), "cudaMalloc") ||
+        !cuda_ok(cudaMalloc((void**)&dlens, sizeof lens), "cudaMalloc") ||
+        !cuda_ok(cudaMalloc((void**)&dtable, sizeof table), "cudaMalloc") ||
+        !cuda_ok(cudaMemcpy(dlens, lens, sizeof lens, cudaMemcpyHostToDevice), "cudaMemcpy") ||
+        !cuda_ok(cudaMemcpy(dtable, table, sizeof table, cudaMemcpyHostToDevice), "cudaMemcpy"))
+      return 1;
+    attn_decode_paged_params p;
+    memset(&p, 0, sizeof p);
+    p.q = dq;
+    p.kpages = dk;
+    p.vpages = dv;
+    p.block_table = dtable;
+    p.kv_lens = dlens;
+    p.out = dout;
+    p.lse = dlse;
+    p.B = B;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.D = D;
+    p.page_size = ps;
+    p.max_pages = max_pages;
+    p.num_pages = num_pages;
+    p.scale = 0.125f;
+    p.out_dtype = ATTN_DTYPE_BF16;
+    st = attn_decode_paged(&p);
+    if (st != ATTN_OK) return fail("attn_decode_paged", st);
+    st = attn_get_device_status(NULL);
+    if (st != ATTN_OK) return fail("attn_get_device_status after attn_decode_paged", st);
+    uint16_t* hout = (uint16_t*)malloc(nq * sizeof(uint16_t));
+    float* hlse = (float*)malloc(nl * sizeof(float));
+    if (hout == NULL || hlse == NULL) return 1;
+    if (!cuda_ok(cudaMemcpy(hout, dout, nq * sizeof(uint16_t), cudaMemcpyDeviceToHost), "cudaMemcpy") ||
+        !cuda_ok(cudaMemcpy(hlse, dlse, nl * sizeof(float), cudaMemcpyDeviceToHost), "cudaMemcpy"))
+      return 1;
+    if (!write_file(dir, "paged_q.bf16", hq, nq * 2) || !write_file(dir, "paged_kp.bf16", hk, npool * 2) ||
+        !write_file(dir, "paged_vp.bf16", hv, npool * 2) || !write_file(dir, "paged_out.bf16", hout, nq * 2) ||
+        !write_file(dir, "paged_lse.f32", hlse, nl * 4))
+      return 1;
+    cudaFree(dq); cudaFree(dk); cudaFree(dv); cudaFree(dout); cudaFree(dlse); cudaFree(dlens); cudaFree(dtable);
+    free(hq); free(hk); free(hv); free(hout); free(hlse);
+  }
   attn_release_workspace();
-  printf("c_abi_client: prefill, decode and packed RoPE prefill ran through the C ABI\n");
+  printf("c_abi_client: prefill, decode, packed RoPE prefill, multi-token and paged decode ran through the C ABI\n");
   return 0;
 }

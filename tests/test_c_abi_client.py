@@ -89,3 +89,22 @@ def test_c_client_matches_oracle(tmp_path):
         got = kout[a:e].transpose(1, 0, 2)
         assert np.all(np.abs(got - want) <= np.abs(want) * 2.0 ** -7 + 1e-30)
         assert np.mean(got != want) < 1e-2
+    # multi-token decode: B=2, Hq=8, Hkv=2, Lq=4, Lmax=200, D=128, kv_lens 200, 9
+    q = _bf16(f("multi_q.bf16"), (2, 8, 4, 128))
+    kc, vc = _bf16(f("multi_kc.bf16"), (2, 2, 200, 128)), _bf16(f("multi_vc.bf16"), (2, 2, 200, 128))
+    out, lse = _bf16(f("multi_out.bf16"), (2, 8, 4, 128)), _f32(f("multi_lse.f32"), (2, 8, 4))
+    O_ref, lse_ref = oracle.decode_multi(q, kc, vc, [200, 9], 128 ** -0.5)
+    assert_attn_close(out, lse, O_ref, lse_ref, "C client multi-token decode")
+    # paged decode: B=2, Hq=8, Hkv=2, D=64, 16-key pages, pool of 12, kv_lens 100, 37; the cache the pages describe
+    q = _bf16(f("paged_q.bf16"), (2, 8, 64))
+    kp, vp = _bf16(f("paged_kp.bf16"), (12, 2, 16, 64)), _bf16(f("paged_vp.bf16"), (12, 2, 16, 64))
+    table = [[11, 3, 7, 0, 9, 5, 1], [6, 10, 2]]
+    kc = torch.zeros((2, 2, 112, 64), dtype=torch.bfloat16)
+    vc = torch.zeros((2, 2, 112, 64), dtype=torch.bfloat16)
+    for b, pages in enumerate(table):
+        for i, pg in enumerate(pages):
+            kc[b, :, 16 * i:16 * (i + 1)] = kp[pg]
+            vc[b, :, 16 * i:16 * (i + 1)] = vp[pg]
+    out, lse = _bf16(f("paged_out.bf16"), (2, 8, 64)), _f32(f("paged_lse.f32"), (2, 8))
+    O_ref, lse_ref = oracle.decode(q, kc, vc, [100, 37], 0.125)
+    assert_attn_close(out, lse, O_ref, lse_ref, "C client paged decode")

@@ -193,6 +193,10 @@ def test_decode_million_key_cache_sampled():
 def test_decode_paged_matches_contiguous_and_oracle(B, Hq, Hkv, Lmax, D, page_size):
     q, kc, vc, lens = make_decode(B, Hq, Hkv, Lmax, D, seed=900 + page_size, kv_range=(1, Lmax))
     kp, vp, table = make_pages(kc, vc, page_size, seed=901)
+    # entries past a sequence's last page hold -1, as serving engines pad block tables: never read, never flagged
+    for b in range(B):
+        table[b, (int(lens[b]) + page_size - 1) // page_size:] = -1
+    AB.attn_get_device_status()
     dev = torch.device("cuda:0")
     scale = D ** -0.5
     for chunk in (0, 7):
@@ -208,9 +212,9 @@ def test_decode_paged_matches_contiguous_and_oracle(B, Hq, Hkv, Lmax, D, page_si
 
 
 def test_decode_paged_bad_page_id_is_flagged():
-    q, kc, vc, lens = make_decode(2, 8, 2, 64, 128, seed=77)
+    q, kc, vc, lens = make_decode(2, 8, 2, 64, 128, seed=77, kv_lens=[64, 50])
     kp, vp, table = make_pages(kc, vc, 16, seed=78, fill_unused=0.0)
-    table[1, 2] = kp.shape[0] + 5  # outside the pool
+    table[1, 2] = kp.shape[0] + 5  # outside the pool, on a page that holds keys 32..47 of sequence 1
     dev = torch.device("cuda:0")
     AB.attn_decode_paged(q.to(dev), kp.to(dev), vp.to(dev), table.to(dev), lens.to(dev))
     assert AB.attn_get_device_status() == AB.ATTN_ERR_DEVICE_BOUNDS
