@@ -237,9 +237,12 @@ int attn_decode_ex(const attn_decode_params* p);
  *   kv_lens         DEVICE int32 [B], at most max_pages * page_size (clamped
  *                   and flagged otherwise, as in attn_decode)
  *   page_size       keys per page, 8 .. 65536 (any value, not only powers of 2)
- *   max_pages       columns of block_table; num_pages rows of the pool.  A page
- *                   id outside [0, num_pages) is flagged ATTN_ERR_DEVICE_BOUNDS
- *                   in the device status word and page 0 is read instead.
+ *   max_pages       columns of block_table; num_pages rows of the pool.  Only
+ *                   the entries of pages that hold keys of a sequence (the
+ *                   first ceil(kv_len / page_size)) are read; the rest may hold
+ *                   anything (e.g. -1 padding).  A page id read outside
+ *                   [0, num_pages) is flagged ATTN_ERR_DEVICE_BOUNDS in the
+ *                   device status word and page 0 is read instead.
  *   other fields    as attn_decode_params (q, out, lse, B, Hq, Hkv, D, scale,
  *                   out_dtype, chunk, stream); same workspace as attn_decode_ex.
  */
