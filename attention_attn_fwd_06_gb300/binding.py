@@ -179,20 +179,26 @@ def _stream_handle(stream, device):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
-def _need(t, name, dtype, ndim):
+def _need(t, name, dtype, ndim, shape=None, device=None):
+    """Check a tensor argument; ``shape`` and ``device``, when given, must match exactly (outputs are written
+    by the kernels over their full extent, so a smaller buffer must never reach the library)."""
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
     if t.dim() != ndim:
         raise ValueError(f"{name} must have {ndim} dims, got shape {tuple(t.shape)}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} must be on {device}, got {t.device}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
 
 
-def _set_rope(p, rope, D, device):
+def _set_rope(p, rope, D, device, k_shape=None):
     """rope = (cos, sin, style) or (cos, sin, style, k_out): fp32 device tables [max_pos, D/2], "half" or
     "interleaved", and for prefill an optional bf16 tensor shaped like k receiving the rotated keys (None: off)."""
     if rope is None:
@@ -200,7 +206,9 @@ def _set_rope(p, rope, D, device):
     cos, sin, style = rope[:3]
     k_out = rope[3] if len(rope) > 3 else None
     if k_out is not None:
-        _need(k_out, "rope k_out", torch.bfloat16, k_out.dim())
+        if k_shape is None:
+            raise ValueError("rope k_out is taken by prefill calls only")
+        _need(k_out, "rope k_out", torch.bfloat16, len(k_shape), k_shape, device)
         p.rope.k_out = _ptr(k_out)
     for t, name in ((cos, "rope cos"), (sin, "rope sin")):
         _need(t, name, torch.float32, 2)
@@ -222,19 +230,19 @@ def attn_fwd(q, k, v, out=None, lse=None, causal=True, scale=None, out_dtype=tor
     ``rope = (cos, sin, style)`` rotates q and k inside the call (fp32 device tables [max_pos, D/2];
     style "half" or "interleaved"); every call of this module takes the same argument."""
     _need(q, "q", torch.bfloat16, 4)
-    _need(k, "k", torch.bfloat16, 4)
-    _need(v, "v", torch.bfloat16, 4)
+    _need(k, "k", torch.bfloat16, 4, device=q.device)
+    _need(v, "v", torch.bfloat16, 4, device=q.device)
     B, Hq, Lq, D = q.shape
     Hkv, Lkv = k.shape[1], k.shape[2]
     if tuple(k.shape) != (B, Hkv, Lkv, D) or tuple(v.shape) != tuple(k.shape):
         raise ValueError(f"k/v shapes {tuple(k.shape)} {tuple(v.shape)} do not match q {tuple(q.shape)}")
     if out is None:
         out = torch.empty((B, Hq, Lq, D), dtype=out_dtype, device=q.device)
-    _need(out, "out", out_dtype, 4)
+    _need(out, "out", out_dtype, 4, (B, Hq, Lq, D), q.device)
     if lse is None and want_lse:
         lse = torch.empty((B, Hq, Lq), dtype=torch.float32, device=q.device)
     if lse is not None:
-        _need(lse, "lse", torch.float32, 3)
+        _need(lse, "lse", torch.float32, 3, (B, Hq, Lq), q.device)
     p = attn_fwd_params()
     p.q, p.k, p.v, p.out, p.lse = (_ptr(t) for t in (q, k, v, out, lse))
     p.B, p.Hq, p.Hkv, p.Lq, p.Lkv, p.D = B, Hq, Hkv, Lq, Lkv, D
@@ -242,7 +250,7 @@ def attn_fwd(q, k, v, out=None, lse=None, causal=True, scale=None, out_dtype=tor
     p.causal = int(bool(causal))
     p.out_dtype = ATTN_DTYPE_F32 if out_dtype == torch.float32 else ATTN_DTYPE_BF16
     p.stream = _stream_handle(stream, q.device)
-    _set_rope(p, rope, D, q.device)
+    _set_rope(p, rope, D, q.device, tuple(k.shape))
     _check(load().attn_fwd_ex(ctypes.byref(p)), "attn_fwd")
     return out, lse
 
@@ -251,10 +259,10 @@ def attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqle
                     causal=True, scale=None, out_dtype=torch.bfloat16, want_lse=True, stream=None, rope=None):
     """Packed prefill: q [total_q,Hq,D], k/v [total_k,Hkv,D] bf16, cu_seqlens int32 [B+1] on the device."""
     _need(q, "q", torch.bfloat16, 3)
-    _need(k, "k", torch.bfloat16, 3)
-    _need(v, "v", torch.bfloat16, 3)
-    _need(cu_seqlens_q, "cu_seqlens_q", torch.int32, 1)
-    _need(cu_seqlens_k, "cu_seqlens_k", torch.int32, 1)
+    _need(k, "k", torch.bfloat16, 3, device=q.device)
+    _need(v, "v", torch.bfloat16, 3, device=q.device)
+    _need(cu_seqlens_q, "cu_seqlens_q", torch.int32, 1, device=q.device)
+    _need(cu_seqlens_k, "cu_seqlens_k", torch.int32, 1, device=q.device)
     total_q, Hq, D = q.shape
     total_k, Hkv = k.shape[0], k.shape[1]
     B = cu_seqlens_q.shape[0] - 1
@@ -262,11 +270,11 @@ def attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqle
         raise ValueError("cu_seqlens_q and cu_seqlens_k must have the same length")
     if out is None:
         out = torch.empty((total_q, Hq, D), dtype=out_dtype, device=q.device)
-    _need(out, "out", out_dtype, 3)
+    _need(out, "out", out_dtype, 3, (total_q, Hq, D), q.device)
     if lse is None and want_lse:
         lse = torch.empty((total_q, Hq), dtype=torch.float32, device=q.device)
     if lse is not None:
-        _need(lse, "lse", torch.float32, 2)
+        _need(lse, "lse", torch.float32, 2, (total_q, Hq), q.device)
     p = attn_fwd_params()
     p.q, p.k, p.v, p.out, p.lse = (_ptr(t) for t in (q, k, v, out, lse))
     p.B, p.Hq, p.Hkv, p.Lq, p.Lkv, p.D = B, Hq, Hkv, int(max_seqlen_q), int(max_seqlen_k), D
@@ -276,7 +284,7 @@ def attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqle
     p.cu_seqlens_q, p.cu_seqlens_k = _ptr(cu_seqlens_q), _ptr(cu_seqlens_k)
     p.total_q, p.total_k = total_q, total_k
     p.stream = _stream_handle(stream, q.device)
-    _set_rope(p, rope, D, q.device)
+    _set_rope(p, rope, D, q.device, tuple(k.shape))
     _check(load().attn_fwd_ex(ctypes.byref(p)), "attn_fwd_ex")
     return out, lse
 
@@ -285,9 +293,9 @@ def attn_decode(q, kcache, vcache, kv_lens, out=None, lse=None, scale=None, chun
                 out_dtype=torch.bfloat16, want_lse=True, stream=None, rope=None):
     """Decode: q [B,Hq,D], caches [B,Hkv,Lmax,D] bf16, kv_lens int32 [B] -> (out [B,Hq,D], lse [B,Hq])."""
     _need(q, "q", torch.bfloat16, 3)
-    _need(kcache, "kcache", torch.bfloat16, 4)
-    _need(vcache, "vcache", torch.bfloat16, 4)
-    _need(kv_lens, "kv_lens", torch.int32, 1)
+    _need(kcache, "kcache", torch.bfloat16, 4, device=q.device)
+    _need(vcache, "vcache", torch.bfloat16, 4, device=q.device)
+    _need(kv_lens, "kv_lens", torch.int32, 1, device=q.device)
     B, Hq, D = q.shape
     Hkv, Lmax = kcache.shape[1], kcache.shape[2]
     if tuple(kcache.shape) != (B, Hkv, Lmax, D) or tuple(vcache.shape) != tuple(kcache.shape):
@@ -296,11 +304,11 @@ def attn_decode(q, kcache, vcache, kv_lens, out=None, lse=None, scale=None, chun
         raise ValueError("kv_lens must have B entries")
     if out is None:
         out = torch.empty((B, Hq, D), dtype=out_dtype, device=q.device)
-    _need(out, "out", out_dtype, 3)
+    _need(out, "out", out_dtype, 3, (B, Hq, D), q.device)
     if lse is None and want_lse:
         lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
     if lse is not None:
-        _need(lse, "lse", torch.float32, 2)
+        _need(lse, "lse", torch.float32, 2, (B, Hq), q.device)
     p = attn_decode_params()
     p.q, p.kcache, p.vcache, p.kv_lens, p.out, p.lse = (_ptr(t) for t in (q, kcache, vcache, kv_lens, out, lse))
     p.B, p.Hq, p.Hkv, p.Lmax, p.D = B, Hq, Hkv, Lmax, D
@@ -317,10 +325,10 @@ def attn_decode_paged(q, kpages, vpages, block_table, kv_lens, out=None, lse=Non
                       out_dtype=torch.bfloat16, want_lse=True, stream=None, rope=None):
     """Decode over a paged cache: pages [num_pages,Hkv,page_size,D] bf16, block_table int32 [B,max_pages]."""
     _need(q, "q", torch.bfloat16, 3)
-    _need(kpages, "kpages", torch.bfloat16, 4)
-    _need(vpages, "vpages", torch.bfloat16, 4)
-    _need(block_table, "block_table", torch.int32, 2)
-    _need(kv_lens, "kv_lens", torch.int32, 1)
+    _need(kpages, "kpages", torch.bfloat16, 4, device=q.device)
+    _need(vpages, "vpages", torch.bfloat16, 4, device=q.device)
+    _need(block_table, "block_table", torch.int32, 2, device=q.device)
+    _need(kv_lens, "kv_lens", torch.int32, 1, device=q.device)
     B, Hq, D = q.shape
     num_pages, Hkv, page_size = kpages.shape[0], kpages.shape[1], kpages.shape[2]
     if tuple(kpages.shape) != (num_pages, Hkv, page_size, D) or tuple(vpages.shape) != tuple(kpages.shape):
@@ -329,11 +337,11 @@ def attn_decode_paged(q, kpages, vpages, block_table, kv_lens, out=None, lse=Non
         raise ValueError("block_table and kv_lens must have B rows")
     if out is None:
         out = torch.empty((B, Hq, D), dtype=out_dtype, device=q.device)
-    _need(out, "out", out_dtype, 3)
+    _need(out, "out", out_dtype, 3, (B, Hq, D), q.device)
     if lse is None and want_lse:
         lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
     if lse is not None:
-        _need(lse, "lse", torch.float32, 2)
+        _need(lse, "lse", torch.float32, 2, (B, Hq), q.device)
     p = attn_decode_paged_params()
     p.q, p.kpages, p.vpages = _ptr(q), _ptr(kpages), _ptr(vpages)
     p.block_table, p.kv_lens, p.out, p.lse = _ptr(block_table), _ptr(kv_lens), _ptr(out), _ptr(lse)
@@ -353,9 +361,9 @@ def attn_decode_multi(q, kcache, vcache, kv_lens, out=None, lse=None, scale=None
     """Multi-token decode: q [B,Hq,Lq,D], caches [B,Hkv,Lmax,D] bf16, kv_lens int32 [B] counting the new tokens'
     own keys -> (out [B,Hq,Lq,D], lse [B,Hq,Lq])."""
     _need(q, "q", torch.bfloat16, 4)
-    _need(kcache, "kcache", torch.bfloat16, 4)
-    _need(vcache, "vcache", torch.bfloat16, 4)
-    _need(kv_lens, "kv_lens", torch.int32, 1)
+    _need(kcache, "kcache", torch.bfloat16, 4, device=q.device)
+    _need(vcache, "vcache", torch.bfloat16, 4, device=q.device)
+    _need(kv_lens, "kv_lens", torch.int32, 1, device=q.device)
     B, Hq, Lq, D = q.shape
     Hkv, Lmax = kcache.shape[1], kcache.shape[2]
     if tuple(kcache.shape) != (B, Hkv, Lmax, D) or tuple(vcache.shape) != tuple(kcache.shape):
@@ -364,11 +372,11 @@ def attn_decode_multi(q, kcache, vcache, kv_lens, out=None, lse=None, scale=None
         raise ValueError("kv_lens must have B entries")
     if out is None:
         out = torch.empty((B, Hq, Lq, D), dtype=out_dtype, device=q.device)
-    _need(out, "out", out_dtype, 4)
+    _need(out, "out", out_dtype, 4, (B, Hq, Lq, D), q.device)
     if lse is None and want_lse:
         lse = torch.empty((B, Hq, Lq), dtype=torch.float32, device=q.device)
     if lse is not None:
-        _need(lse, "lse", torch.float32, 3)
+        _need(lse, "lse", torch.float32, 3, (B, Hq, Lq), q.device)
     p = attn_decode_multi_params()
     p.q, p.kcache, p.vcache, p.kv_lens, p.out, p.lse = (_ptr(t) for t in (q, kcache, vcache, kv_lens, out, lse))
     p.B, p.Hq, p.Hkv, p.Lq, p.Lmax, p.D = B, Hq, Hkv, Lq, Lmax, D
@@ -392,9 +400,9 @@ def attn_decode_noalloc(q, kcache, vcache, kv_lens, out, lse=None, scale=None, c
     one-time address lookup and should not be inside a stream capture.
     """
     _need(q, "q", torch.bfloat16, 3)
-    _need(kcache, "kcache", torch.bfloat16, 4)
-    _need(vcache, "vcache", torch.bfloat16, 4)
-    _need(kv_lens, "kv_lens", torch.int32, 1)
+    _need(kcache, "kcache", torch.bfloat16, 4, device=q.device)
+    _need(vcache, "vcache", torch.bfloat16, 4, device=q.device)
+    _need(kv_lens, "kv_lens", torch.int32, 1, device=q.device)
     B, Hq, D = q.shape
     Hkv, Lmax = kcache.shape[1], kcache.shape[2]
     if tuple(kcache.shape) != (B, Hkv, Lmax, D) or tuple(vcache.shape) != tuple(kcache.shape):
@@ -403,9 +411,9 @@ def attn_decode_noalloc(q, kcache, vcache, kv_lens, out, lse=None, scale=None, c
         raise ValueError("kv_lens must have B entries")
     if out.dtype not in (torch.bfloat16, torch.float32):
         raise TypeError("out must be bf16 or fp32")
-    _need(out, "out", out.dtype, 3)
+    _need(out, "out", out.dtype, 3, (B, Hq, D), q.device)
     if lse is not None:
-        _need(lse, "lse", torch.float32, 2)
+        _need(lse, "lse", torch.float32, 2, (B, Hq), q.device)
     p = attn_decode_params()
     p.q, p.kcache, p.vcache, p.kv_lens, p.out, p.lse = (_ptr(t) for t in (q, kcache, vcache, kv_lens, out, lse))
     p.B, p.Hq, p.Hkv, p.Lmax, p.D = B, Hq, Hkv, Lmax, D

@@ -328,7 +328,15 @@ int attn_decode_noalloc(const attn_decode_params* p) {
     return ATTN_ERR_CUDA;
   }
   if (g_noalloc_ptr[dev] == nullptr) {
-    // One-time set-up on this device (it is current): resolve the scratch array's device address.
+    // One-time set-up on this device (it is current).  Its memset and synchronise would invalidate a stream
+    // capture in progress, so a first call made inside one is refused before anything touches the device.
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(static_cast<cudaStream_t>(p->stream), &cap) != cudaSuccess) {
+      cudaGetLastError();
+      return ATTN_ERR_CUDA;
+    }
+    if (cap != cudaStreamCaptureStatusNone) return ATTN_ERR_INVALID_ARG;
+    // Resolve the scratch array's device address.
     float* ptr = nullptr;
     if (cudaGetSymbolAddress(reinterpret_cast<void**>(&ptr), g_noalloc_scratch) != cudaSuccess || ptr == nullptr) {
       cudaGetLastError();

@@ -103,7 +103,9 @@ struct MultiArgs {
   int GP;              // query heads per kv head
   int R;               // GP * Lq real rows of the tile
   int q_box_bytes;     // bytes one Q load brings (all column blocks)
-  float scale_log2;    // scale * log2(e)
+  float scale_log2;    // |scale| * log2(e), or 1 when scale == 0 (then `uniform` is set)
+  uint32_t idesc_s;    // instruction descriptor of the S MMAs: negates Q when scale < 0, so S * scale_log2 keeps the sign
+  int uniform;         // scale == 0: every visible logit is 0 (uniform weights), masked ones -inf
   int out_f32;
   unsigned* status;
   RopeArgs rope;       // style != 0: the softmax threads rotate the Q tile's rows before the S MMAs
@@ -403,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t koff = (kk >> 2) * C::BLOCK_BYTES + (kk & 3) * 32;
           tc::mma_ss(tbase + C::tm_s(buf), tc::smem_desc_sw128(q_addr + koff, 16, 1024),
-                     tc::smem_desc_sw128(k_addr + koff, 16, 1024), C::IDESC_S, kk > 0);
+                     tc::smem_desc_sw128(k_addr + koff, 16, 1024), a.idesc_s, kk > 0);
         }
         tc::mma_commit(&s_full[buf]);
         tc::mma_commit(&k_empty[kslot]);
@@ -522,15 +524,27 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         const bool last = (tt == pc.T - 1);
         const int ks = last ? pc.n - BN : tt * BN;  // key of column 0
-        if (last || ks + BN - 1 > pc.n - a.Lq) {
+        // The mask acts on the scaled logits (scale, then mask): the factor is positive (a negative scale negates
+        // Q in the S MMA), so a raw -inf stays -inf once scaled; with scale == 0 every visible logit is 0.
+        if (last || ks + BN - 1 > pc.n - a.Lq || a.uniform) {
           const int lo_key = last ? (pc.T - 1) * BN : 0;  // earlier keys belong to the previous tile
+          if (a.uniform) {
 #pragma unroll
-          for (int cc = 0; cc < 4; ++cc)
+            for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              const int key = ks + cc * 32 + e;
-              if (key < lo_key || key > horizon) sr[cc][e] = __float_as_uint(-INFINITY);
-            }
+              for (int e = 0; e < 32; ++e) {
+                const int key = ks + cc * 32 + e;
+                sr[cc][e] = (key < lo_key || key > horizon) ? __float_as_uint(-INFINITY) : 0u;
+              }
+          } else {
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+              for (int e = 0; e < 32; ++e) {
+                const int key = ks + cc * 32 + e;
+                if (key < lo_key || key > horizon) sr[cc][e] = __float_as_uint(-INFINITY);
+              }
+          }
         }
         float mx[4];
 #pragma unroll
@@ -806,7 +820,10 @@ cudaError_t launch_d(const DecodeMultiLaunch& p) {
   a.GP = GP;
   a.R = R;
   a.q_box_bytes = qbox * 128 * C::NDB;
-  a.scale_log2 = p.scale * kLog2e;
+  // a positive factor on the logits: a negative scale negates Q in the S MMA (exact); scale == 0 is uniform weights
+  a.uniform = (p.scale == 0.f) ? 1 : 0;
+  a.scale_log2 = a.uniform ? 1.f : fabsf(p.scale) * kLog2e;
+  a.idesc_s = C::IDESC_S | (p.scale < 0.f ? tc::kIdescNegateA : 0u);
   a.out_f32 = p.out_f32;
   a.status = p.status;
   a.rope = p.rope;

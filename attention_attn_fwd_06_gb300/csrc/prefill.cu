@@ -117,7 +117,9 @@ struct PrefillArgs {
   int varlen;
   int causal;
   int out_f32;
-  float scale_log2;  // scale * log2(e)
+  float scale_log2;  // |scale| * log2(e), or 1 when scale == 0 (then `uniform` is set)
+  uint32_t idesc_s;  // instruction descriptor of the S MMAs: negates Q when scale < 0, so S * scale_log2 keeps the sign
+  int uniform;       // scale == 0: every visible logit is 0 (uniform weights), masked ones -inf
   int ns;            // work items per (sequence, head)
   int single;        // 1: an item is one tile pair; 0: an item is the tile pairs np-1-s and s
   int total_items;   // B * Hq * ns
@@ -328,7 +330,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t koff = ((kk >> 2) * C::BLOCK_BYTES + (kk & 3) * 32) >> 4;
-          tc::mma_ss(tbase + C::tm_s(t), tc::desc64(qa + koff, kHi), tc::desc64(ka + koff, kHi), C::IDESC_S, kk > 0);
+          tc::mma_ss(tbase + C::tm_s(t), tc::desc64(qa + koff, kHi), tc::desc64(ka + koff, kHi), a.idesc_s, kk > 0);
         }
         tc::mma_commit(&s_full[t]);
       };
@@ -444,15 +446,26 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
           for (int cc = 0; cc < 4; ++cc) tc::tmem_ld32(s_addr + cc * 32, sr[cc]);
           tc::tmem_ld_wait();
 
+          // The mask acts on the scaled logits (scale, then mask): with scale > 0 -- the host makes the factor
+          // positive by negating Q in the S MMA when scale < 0 -- a raw -inf stays -inf once scaled.  With
+          // scale == 0 every visible logit is 0, so those tiles set visible scores to 0 and masked ones to -inf.
           const int kbase = j * BN;
           const bool need_mask = (kbase + BN > jb.Lkv_s) || (a.causal && kbase + BN - 1 > q0 + jb.off);
-          if (need_mask) {
+          if (need_mask || a.uniform) {
             const int lim = a.causal ? min(jb.Lkv_s - 1, horizon) : (jb.Lkv_s - 1);
+            if (a.uniform) {
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc)
+              for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
-              for (int i = 0; i < 32; ++i)
-                if (kbase + cc * 32 + i > lim) sr[cc][i] = __float_as_uint(-INFINITY);
+                for (int i = 0; i < 32; ++i)
+                  sr[cc][i] = (kbase + cc * 32 + i > lim) ? __float_as_uint(-INFINITY) : 0u;
+            } else {
+#pragma unroll
+              for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                  if (kbase + cc * 32 + i > lim) sr[cc][i] = __float_as_uint(-INFINITY);
+            }
           }
           // row max with three-input max (two new values per instruction), four independent chains
           float mx[4];
@@ -644,7 +657,11 @@ cudaError_t launch_d(const PrefillLaunch& p) {
   a.varlen = varlen ? 1 : 0;
   a.causal = p.causal;
   a.out_f32 = p.out_f32;
-  a.scale_log2 = p.scale * kLog2e;
+  // S * scale in log2 units with a positive factor: a negative scale negates Q inside the S MMA instead (exact),
+  // and scale == 0 runs the uniform-weight form (factor 1 on logits the mask pass sets to 0 or -inf)
+  a.uniform = (p.scale == 0.f) ? 1 : 0;
+  a.scale_log2 = a.uniform ? 1.f : fabsf(p.scale) * kLog2e;
+  a.idesc_s = C::IDESC_S | (p.scale < 0.f ? tc::kIdescNegateA : 0u);
   const int npairs = (p.Lq + NQ * BM - 1) / (NQ * BM);
   // Dense inputs: persistent CTAs (one per SM) over equal-cost items -- two mirrored tile pairs when causal,
   // one tile pair otherwise -- so a CTA's start-up is paid once.  Packed sequences differ in cost: one CTA per

@@ -62,12 +62,15 @@ __device__ __forceinline__ uint64_t desc64(uint32_t lo, uint32_t hi) { return ((
 
 // Instruction descriptor for kind::f16 with bf16 A and B and an fp32 accumulator.
 //   bits 4-5 D format (1 = f32), 7-9 A format (1 = bf16), 10-12 B format (1 = bf16),
-//   bit 15 A major (0 = K-major), bit 16 B major (0 = K-major, 1 = MN-major),
+//   bit 13 negate A, bit 15 A major (0 = K-major), bit 16 B major (0 = K-major, 1 = MN-major),
 //   bits 17-22 N >> 3, bits 24-28 M >> 4.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool b_mn_major) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) |
          ((uint32_t)(M >> 4) << 24);
 }
+// The same MMA with A negated: D (+)= (-A) B.  Negating a bf16 value is exact and round-to-nearest is symmetric,
+// so the fp32 result is exactly the negation of the plain product.
+constexpr uint32_t kIdescNegateA = 1u << 13;
 
 // ---------------------------------------------------------------- MMAs (one thread issues)
 // D[tmem] (+)= A[smem] * B[smem]

@@ -112,8 +112,10 @@ typedef struct attn_rope {
  *   v    bf16 [B, Hkv, Lkv, D]  contiguous
  *   out  bf16 [B, Hq,  Lq,  D]  written
  *   lse  fp32 [B, Hq,  Lq]      written; may be NULL (then not written)
- *   scale   multiplies the logits (pass 1/sqrt(D) for the standard chain); must be
- *           finite (NaN or +-inf: ATTN_ERR_INVALID_ARG)
+ *   scale   multiplies the logits (pass 1/sqrt(D) for the standard chain), before
+ *           the mask is added; any finite value, zero (uniform weights over the
+ *           visible keys) and negative values included (NaN or +-inf:
+ *           ATTN_ERR_INVALID_ARG).  Every entry point treats scale this way.
  *   causal  0 = no mask, 1 = bottom-right-aligned causal mask
  *
  * Runs on the tensor cores (tcgen05 MMAs with TMEM accumulators, TMA-fed
@@ -364,7 +366,8 @@ void attn_release_workspace(void);
  * routine.  The first call on a device looks up the buffer's device address
  * (cudaGetSymbolAddress, once per device, with that device current) and
  * zeroes the counter area (cudaMemset, then a device synchronise); make that
- * first call outside any stream capture.  The kernel leaves the counters at
+ * first call outside any stream capture (a first call on a capturing stream
+ * returns ATTN_ERR_INVALID_ARG and leaves the capture untouched).  The kernel leaves the counters at
  * zero after every call, and every partial is written before it is read in
  * the same call.  All calls share the one buffer and it keeps the last call's
  * contents: two calls that can overlap on the GPU (different streams with no

@@ -239,3 +239,41 @@ def test_decode_rope_validation(lib):
     m.B, m.Hq, m.Hkv, m.Lq, m.Lmax, m.D, m.scale = 1, 4, 4, 2, 128, 128, 0.1
     m.rope.cos, m.rope.sin, m.rope.max_pos, m.rope.style = FAKE, FAKE, 127, B.ATTN_ROPE_HALF
     assert lib.attn_decode_multi(ctypes.byref(m)) == B.ATTN_ERR_INVALID_ARG
+
+
+def test_any_finite_scale_passes_validation(lib):
+    # The scale multiplies the logits before the mask is added, and every finite value means something: 0 gives
+    # uniform weights over the visible keys, a negative value reverses the order of the logits.  Validation lets
+    # them through; here, with no sm_103 device, the calls then fail for want of one (never INVALID_ARG).
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present (the fake pointers must not reach a kernel)")
+    for sc in (0.0, -0.0, -0.088, -3.5, 1e-30, -1e30):
+        assert fwd(lib, scale=sc) in (B.ATTN_ERR_UNSUPPORTED, B.ATTN_ERR_CUDA), sc
+        assert dec(lib, scale=sc) in (B.ATTN_ERR_UNSUPPORTED, B.ATTN_ERR_CUDA), sc
+        assert multi(lib, scale=sc) in (B.ATTN_ERR_UNSUPPORTED, B.ATTN_ERR_CUDA), sc
+
+
+def test_binding_refuses_wrong_output_shapes_and_devices():
+    # Outputs are written over their full extent by the kernels: the binding compares every caller-supplied
+    # buffer's shape and device with what the call will write, before any pointer reaches the library.
+    import torch
+
+    good = torch.empty(2, 3, 4)
+    with pytest.raises(ValueError, match="shape"):
+        B._need(torch.empty(2, 3, 5), "out", torch.float32, 3, (2, 3, 4))
+    with pytest.raises(ValueError, match="dims"):
+        B._need(torch.empty(2, 3), "out", torch.float32, 3, (2, 3, 4))
+    with pytest.raises(TypeError):
+        B._need(good, "out", torch.bfloat16, 3, (2, 3, 4))
+    with pytest.raises(ValueError, match="CUDA"):  # right shape, but not on a GPU
+        B._need(good, "out", torch.float32, 3, (2, 3, 4))
+    p = B.attn_fwd_params()
+    tab = torch.empty(8, 32)
+    with pytest.raises(ValueError, match="shape"):  # rotated keys must be shaped like k
+        B._set_rope(p, (tab, tab, "half", torch.empty(1, 2, 16, 64, dtype=torch.bfloat16)), 64,
+                    torch.device("cpu"), (1, 2, 17, 64))
+    with pytest.raises(ValueError, match="prefill"):  # decode calls take no k_out
+        B._set_rope(p, (tab, tab, "half", torch.empty(1, 2, 16, 64, dtype=torch.bfloat16)), 64,
+                    torch.device("cpu"))

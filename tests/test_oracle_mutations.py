@@ -96,6 +96,22 @@ def _multi_with_mask(mask_of):
     return bad
 
 
+def _head_mask_before_scale(Qh, Kh, Vh, scale, causal, visible=None):
+    # the mask applied to the raw scores, then the scale: right for scale > 0 only (-inf * 0 is NaN, and a
+    # negative scale turns masked keys into +inf)
+    Lq, Lkv = Qh.shape[0], Kh.shape[0]
+    if visible is None:
+        visible = OA.visible_mask(Lq, Lkv, causal)
+    with np.errstate(invalid="ignore"):
+        S = scale * np.where(visible, Qh @ Kh.T, -np.inf)
+        P, m, l = OA.softmax_two_pass(S, np.ones_like(visible))
+    return P @ Vh, OA.log_sum_exp(m, l)
+
+
+def _scores_abs_scale(Qh, Kh, scale):
+    return abs(scale) * (Qh @ Kh.T)
+
+
 MUTATIONS = {
     "scale_dropped": ("scores", lambda Qh, Kh, scale: Qh @ Kh.T),
     "logit_sign": ("scores", lambda Qh, Kh, scale: -scale * (Qh @ Kh.T)),
@@ -121,6 +137,8 @@ MUTATIONS = {
     "rope_keys_not_rotated": ("_rope_q_k", _rope_keys_not_rotated),
     "rope_unrounded": ("_rope_q_k", _rope_unrounded),
     "varlen_keys_at_query_offsets": ("attention_varlen", _varlen_keys_at_query_offsets),
+    "mask_before_scale": ("attention_head", _head_mask_before_scale),
+    "scale_sign_dropped": ("scores", _scores_abs_scale),
 }
 
 

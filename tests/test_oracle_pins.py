@@ -467,6 +467,63 @@ def pin_rope_rows_and_varlen_agree_with_dense():
         np.testing.assert_allclose(Ovr, Od[0, 1, rows], atol=1e-13)
 
 
+def pin_scale_zero_is_uniform_average():
+    """scale 0: every visible logit is 0, so O is the plain mean of the visible V rows and lse = ln(count).
+
+    A closed form that needs no exponential: it pins where the scale is applied (before the mask is added --
+    a mask applied to raw scores and then multiplied by 0 would give NaN) and the count of visible keys under
+    the bottom-right causal alignment, for square, Lq < Lkv, Lq > Lkv (empty first rows), decode and multi-token
+    decode alike."""
+    for n, (Lq, Lkv, causal) in enumerate([(7, 7, True), (4, 9, True), (9, 5, True), (6, 8, False)]):
+        q, k, v = _qkv(700 + n, 1, 4, 2, Lq, Lkv, 5)
+        O, lse = OA.attention(q, k, v, 0.0, causal)
+        for h in range(4):
+            hk = h // 2
+            for i in range(Lq):
+                cnt = min(Lkv, i + (Lkv - Lq) + 1) if causal else Lkv
+                if cnt <= 0:
+                    assert lse[0, h, i] == -np.inf and not O[0, h, i].any()
+                    continue
+                np.testing.assert_allclose(O[0, h, i], v[0, hk, :cnt].mean(axis=0), atol=1e-14)
+                assert abs(lse[0, h, i] - math.log(cnt)) < 1e-14
+    r = _rng(710)
+    qd, kc, vc = r.standard_normal((2, 4, 6)), r.standard_normal((2, 2, 12, 6)), r.standard_normal((2, 2, 12, 6))
+    lens = [12, 5]
+    Od, ld = OA.decode(qd, kc, vc, lens, 0.0)
+    qm = r.standard_normal((2, 4, 3, 6))
+    Om, lm = OA.decode_multi(qm, kc, vc, lens, 0.0)
+    for b, nb in enumerate(lens):
+        for h in range(4):
+            np.testing.assert_allclose(Od[b, h], vc[b, h // 2, :nb].mean(axis=0), atol=1e-14)
+            assert abs(ld[b, h] - math.log(nb)) < 1e-14
+            for t in range(3):
+                cnt = nb - 3 + t + 1
+                np.testing.assert_allclose(Om[b, h, t], vc[b, h // 2, :cnt].mean(axis=0), atol=1e-14)
+                assert abs(lm[b, h, t] - math.log(cnt)) < 1e-14
+
+
+def pin_negative_scale():
+    """A negative scale against the literal loops, and scale -s with q equal to scale s with -q."""
+    for n, (Lq, Lkv, causal) in enumerate([(6, 6, True), (3, 8, True), (5, 7, False)]):
+        q, k, v = _qkv(720 + n, 1, 2, 1, Lq, Lkv, 4)
+        O, lse = OA.attention(q, k, v, -0.61, causal)
+        Ob, lseb = attention_loops(q, k, v, -0.61, causal)
+        np.testing.assert_allclose(O, np.array(Ob), rtol=0, atol=1e-12)
+        np.testing.assert_allclose(lse, np.array(lseb), rtol=0, atol=1e-12)
+        O2, l2 = OA.attention(-q, k, v, 0.61, causal)
+        np.testing.assert_allclose(O, O2, atol=1e-14)
+        np.testing.assert_allclose(lse, l2, atol=1e-14)
+    # decode: the smallest logit now dominates -- the key most aligned with q gets the least weight
+    r = _rng(730)
+    qd = r.standard_normal((1, 1, 4))
+    kc = np.zeros((1, 1, 3, 4))
+    kc[0, 0, 0] = 40 * qd[0, 0] / np.linalg.norm(qd[0, 0])  # aligned with q: largest raw score
+    kc[0, 0, 1] = -40 * qd[0, 0] / np.linalg.norm(qd[0, 0])  # opposite: smallest raw score
+    vc = r.standard_normal((1, 1, 3, 4))
+    O, _ = OA.decode(qd, kc, vc, [3], -1.0)
+    np.testing.assert_allclose(O[0, 0], vc[0, 0, 1], atol=1e-12)
+
+
 PINS = [
     pin_brute_force,
     pin_rows_sum_to_one,
@@ -496,6 +553,8 @@ PINS = [
     pin_rope_decode_is_last_prefill_row,
     pin_rope_multi_tokens_are_prefill_rows,
     pin_rope_rows_and_varlen_agree_with_dense,
+    pin_scale_zero_is_uniform_average,
+    pin_negative_scale,
 ]
 
 
