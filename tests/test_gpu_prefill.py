@@ -6,9 +6,10 @@ in both directions (bottom-right causal alignment, rows that see no key), a
 single query, a single key, no keys at all, fp32 output and logits large
 enough to trigger the O rescale.  The prefill workloads run at full size in
 the bench's launch configuration and are checked on sampled rows that the
-oracle computes one by one, as is a shape with more work items than SMs (every
-persistent CTA walks several jobs) and one 65,536-token sequence at each head
-dim.
+oracle computes one by one, plus every row of one whole head (of the longest
+sequence, for the packed workload); so are a shape with more work items than
+SMs (every persistent CTA walks several jobs) and one 65,536-token sequence at
+each head dim.
 """
 import numpy as np
 import pytest
@@ -135,8 +136,15 @@ def _sample_rows(rng, L, n):
     return np.array(sorted(rows))
 
 
+def _every_row(L, step=1024):
+    return [np.arange(r0, min(L, r0 + step)) for r0 in range(0, L, step)]
+
+
 @pytest.mark.parametrize("name", ["prefill_causal", "prefill_noncausal_d64"])
 def test_prefill_workload_sampled(name):
+    # Sampled rows of three heads per batch entry, and then EVERY row of one whole head (the last batch entry's
+    # last head: every (query tile, key tile) pair of that head, the diagonal and the last tiles included),
+    # element by element against the oracle in blocks of rows.
     w = WORKLOADS[name]
     q, k, v = make_prefill(w.B, w.Hq, w.Hkv, w.L, w.L, w.D, w.seed)
     O, lse = run(q, k, v, w.causal)
@@ -147,6 +155,10 @@ def test_prefill_workload_sampled(name):
             rows = _sample_rows(rng, w.L, 48)
             O_ref, lse_ref = oracle.attention_rows(q, k, v, w.scale, w.causal, b, int(h), rows)
             assert_attn_close(O[b, h, rows], lse[b, h, rows], O_ref, lse_ref, f"{name} b={b} h={h}")
+    b, h = w.B - 1, w.Hq - 1
+    for rows in _every_row(w.L):
+        O_ref, lse_ref = oracle.attention_rows(q, k, v, w.scale, w.causal, b, h, rows)
+        assert_attn_close(O[b, h, rows], lse[b, h, rows], O_ref, lse_ref, f"{name} full head b={b} h={h}")
 
 
 @pytest.mark.parametrize("D,causal", [(128, True), (64, False)])
@@ -182,6 +194,13 @@ def test_prefill_ragged_workload_sampled():
         O_ref, lse_ref = oracle.attention_varlen_rows(q, k, v, cul, cul, w.scale, True, s, h, rows)
         idx = torch.as_tensor(cul[s] + rows)
         assert_attn_close(out[idx, h], lse[idx, h], O_ref, lse_ref, f"seq {s} (len {lens[s]}) h={h}")
+    # every row of one head of the longest sequence (the last query head: the last kv head's group)
+    s = int(np.argmax(lens))
+    h = w.Hq - 1
+    for rows in _every_row(lens[s]):
+        O_ref, lse_ref = oracle.attention_varlen_rows(q, k, v, cul, cul, w.scale, True, s, h, rows)
+        idx = torch.as_tensor(cul[s] + rows)
+        assert_attn_close(out[idx, h], lse[idx, h], O_ref, lse_ref, f"longest seq {s} (len {lens[s]}) full head")
 
 
 @pytest.mark.parametrize("D,causal", [(128, False), (128, True), (64, False)])
