@@ -43,6 +43,7 @@
 //    is created.
 #include <cfloat>
 #include <cmath>
+#include <type_traits>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -56,6 +57,42 @@ constexpr float kLn2 = 0.6931471805599453f;
 // (warp merge, output or partial, publish, a possible merge of the row) takes about as long as streaming three
 // 64-key stages (a sweep of 64 to 256 on the 8 x 4096 GQA workload put the shortest calls at 192 and above).
 constexpr int kRowCost = 192;
+#ifndef ATTN_DECODE_TAPER_MILLI
+#define ATTN_DECODE_TAPER_MILLI 200
+#endif
+// Slices taper with the CTA index: CTA c of g starts at cost position F(c / g) * Wc with
+// F(x) = x + (a/2)(x - x^2), so the first CTA takes (1 + a/2) times the mean slice and the last (1 - a/2) times.
+// All CTAs issue their first copies together, memory serves them roughly in launch order, and each CTA then streams
+// at about the same rate: per-CTA traces of the 8 x 4096 GQA workload put the last CTAs' first data ~2.5 us after
+// the first CTAs' and, with equal slices, their finish ~3.5 us later.  a = 0.2 (thousandths below).
+constexpr float kTaper = ATTN_DECODE_TAPER_MILLI * 1e-3f;
+
+// First cost position of slice c of g over [0, Wc) with taper a (g >= 1; c >= g gives Wc).  Integer base plus a
+// small fp32 correction; non-decreasing in c for a < 2, and every CTA evaluates the same function, so the slices
+// tile [0, Wc).  Callers use a = 0 unless slices average at least 64 positions, so no slice is empty.
+__device__ __forceinline__ long long slice_start(long long c, long long g, long long Wc, float a) {
+  if (c >= g) return Wc;
+  const long long base = (Wc * c) / g;
+  if (a == 0.f) return base;
+  const float x = (float)c / (float)g;
+  return base + (long long)((float)Wc * (0.5f * a) * (x - x * x));
+}
+
+// The slice holding cost position pos (0 <= pos < Wc): the largest c with slice_start(c) <= pos.  The inverse of F in
+// fp32 gives a first guess; integer steps make it exact.
+__device__ __forceinline__ long long slice_of(long long pos, long long g, long long Wc, float a) {
+  const float y = (float)pos / (float)Wc;
+  float x = y;
+  if (a > 0.f) {
+    const float h = 1.f + 0.5f * a;
+    x = (h - sqrtf(fmaxf(h * h - 2.f * a * y, 0.f))) / a;
+  }
+  long long c = (long long)(x * (float)g);
+  c = c < 0 ? 0 : (c >= g ? g - 1 : c);
+  while (c > 0 && slice_start(c, g, Wc, a) > pos) --c;
+  while (c + 1 < g && slice_start(c + 1, g, Wc, a) <= pos) ++c;
+  return c;
+}
 
 template <int D, int GP>
 struct DecodeCfg {
@@ -83,8 +120,7 @@ struct DecodeCfg {
   static constexpr int ROPE_BYTES = 4 * D;                     // cos and sin rows (D/2 fp32 each) of the q position
   static constexpr int OFF_Q = OFF_V + NS * TILE_BYTES;
   static constexpr int OFF_R = OFF_Q + NS * Q_BYTES;          // rope rows per stage
-  static constexpr int OFF_O = OFF_R + NS * ROPE_BYTES;       // obuf[2][GP][D] fp32 (merge; also combine weights)
-  static constexpr int OFF_BAR = OFF_O + 2 * GP * D * 4;      // full[NS], empty[NS]
+  static constexpr int OFF_BAR = OFF_R + NS * ROPE_BYTES;     // full[NS], empty[NS]
   static constexpr int OFF_INFO = OFF_BAR + 2 * NS * 8;       // StageInfo[NS]
   static constexpr int OFF_P = OFF_INFO + NS * 32;            // pbuf[NW][32]
   static constexpr int OFF_A = OFF_P + NW * 32 * 4;           // abuf[NW][GP]
@@ -93,6 +129,8 @@ struct DecodeCfg {
   static constexpr int OFF_LENS = OFF_L + NW * GP * 4;        // lens[LENS_CACHE]
   static constexpr int OFF_MISC = OFF_LENS + LENS_CACHE * 4;  // abort flag, last-partial flag
   static constexpr int SMEM = OFF_MISC + 16;
+  static_assert(NW * GP * D * 4 <= TILE_BYTES, "the piece-end merge parks every warp's O in one K tile");
+  static_assert(KPI * NW * ITER == SK && (KPI * D * 2) % 16 == 0, "a warp's first key group: whole 16-byte rows");
   static_assert(MINB * (SMEM + 1024) <= 228 * 1024, "MINB CTAs per SM");
 };
 
@@ -109,12 +147,18 @@ struct StageInfo {
 
 __device__ __forceinline__ int clamp_len(int len, int Lmax) { return len < 0 ? 0 : (len > Lmax ? Lmax : len); }
 
-template <typename T>
-__device__ __forceinline__ void store_out(void* out, size_t idx, float v, int out_f32) {
-  if (out_f32)
-    reinterpret_cast<float*>(out)[idx] = v;
-  else
-    reinterpret_cast<__nv_bfloat16*>(out)[idx] = __float2bfloat16_rn(v);
+// Four consecutive outputs starting at element idx (a multiple of 4), as fp32 or bf16.
+__device__ __forceinline__ void store_out4(void* out, size_t idx, float4 v, int out_f32) {
+  if (out_f32) {
+    *reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + idx) = v;
+  } else {
+    __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(v.z, v.w);
+    uint2 w2;
+    w2.x = *reinterpret_cast<uint32_t*>(&lo);
+    w2.y = *reinterpret_cast<uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(out) + idx) = w2;
+  }
 }
 
 template <int D, int GP>
@@ -126,7 +170,6 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS, DecodeCfg<D, GP>::M
   __nv_bfloat16* Vs = reinterpret_cast<__nv_bfloat16*>(smem + C::OFF_V);
   uint8_t* Qs = smem + C::OFF_Q;
   float* Rs = reinterpret_cast<float*>(smem + C::OFF_R);
-  float* obuf = reinterpret_cast<float*>(smem + C::OFF_O);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* empty = full + C::NS;
   StageInfo* info = reinterpret_cast<StageInfo*>(smem + C::OFF_INFO);
@@ -154,7 +197,6 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS, DecodeCfg<D, GP>::M
   }
   // The producer's first kv_lens load is issued before the barrier, so its latency overlaps the set-up.
   const int len_first = (warp == C::NW && lane < p.B) ? p.kv_lens[lane] : 0;
-  for (int i = threadIdx.x; i < 2 * GP * D; i += blockDim.x) obuf[i] = 0.f;
   __syncthreads();
 
   if (warp == C::NW) {
@@ -191,9 +233,9 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS, DecodeCfg<D, GP>::M
     // its keys the last len positions, so a slice that takes on a row start also takes fewer keys.  Slices
     // that fall inside a row's cost-only head take no keys of that row.
     const long long Wc = W + (long long)kRowCost * nonempty * Hg;
-    const long long per = (Wc + geff - 1) / geff;
-    const long long lo = (long long)cta * per;
-    const long long hi = min(lo + per, Wc);
+    const float taper = (Wc >= 64 * geff) ? kTaper : 0.f;
+    const long long lo = slice_start(cta, geff, Wc, taper);
+    const long long hi = slice_start(cta + 1, geff, Wc, taper);
 
     int t = 0;  // stages issued
     bool ok = true;
@@ -252,17 +294,37 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS, DecodeCfg<D, GP>::M
       return __shfl_sync(0xffffffffu, okw, 0) != 0;
     };
 
-    auto emit = [&](int b, int hg, int kb, int ke, int np, int slot, int cta_lo, int lo_odd) -> bool {
-      // stream keys [kb, ke) of row (b, hg); ke == kb emits a single key-less stage
+    // Stream keys [kb, ke) of row (b, hg), whose keys sit at cost positions [ks, ks + len) (first_in_slice: the
+    // piece starts this CTA's slice); ke == kb emits one key-less stage (a sequence with no keys).
+    auto emit = [&](int b, int hg, int kb, int ke, long long ks, bool first_in_slice) -> bool {
       const int hkv = hg / ngroups;
       const int hq0 = hkv * group + (hg - hkv * ngroups) * GP;
       const __nv_bfloat16* qg = reinterpret_cast<const __nv_bfloat16*>(p.q) + ((size_t)b * p.Hq + hq0) * D;
       const int nkeys = ke - kb;
       const int nst = nkeys > 0 ? (nkeys + C::SK - 1) / C::SK : 1;
+      int np = 0, slot = 0, cta_lo = 0, lo_odd = 0;  // the piece's merge bookkeeping
       for (int u = 0; u < nst; ++u, ++t) {
         const int slot_r = t % C::NS;
         if (t >= C::NS && !wait_empty(slot_r)) return false;
         const int nk = nkeys > 0 ? min(C::SK, nkeys - u * C::SK) : 0;
+        const uint32_t kv_bytes = 2u * (uint32_t)nk * D * 2;
+        if (u == 0) {
+          // The piece's first K/V copies go out before anything else: their bytes are expected without an
+          // arrival, then the bookkeeping below, the stage record and the arrival (with q's bytes) follow, so the
+          // record is written before the phase can complete.
+          if (nk > 0) {
+            if (lane == 0) mbar_expect_tx(&full[slot_r], kv_bytes);
+            copy_keys(b, hkv, kb, nk, Ks + slot_r * C::TILE_ELEMS, Vs + slot_r * C::TILE_ELEMS, &full[slot_r]);
+            // which CTAs hold a piece of this row, and this piece's partial slot
+            const int len = seq_len(b);
+            const long long c_lo = slice_of(ks, geff, Wc, taper);
+            const long long c_hi = slice_of(ks + len - 1, geff, Wc, taper);
+            np = (int)(c_hi - c_lo + 1);
+            cta_lo = (int)c_lo;
+            slot = 2 * cta + (first_in_slice ? 0 : 1);
+            lo_odd = (ks != slice_start(c_lo, geff, Wc, taper)) ? 1 : 0;
+          }
+        }
         if (lane == 0) {
           StageInfo si;
           si.b = b;
@@ -276,7 +338,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS, DecodeCfg<D, GP>::M
           info[slot_r] = si;
           // the first stage of a piece carries q, and with RoPE the table rows of its position (kv_len - 1)
           const bool rope_rows = (u == 0) && rope_on && nkeys > 0;
-          mbar_arrive_expect_tx(&full[slot_r], 2u * (uint32_t)nk * D * 2 + (u == 0 ? (uint32_t)C::Q_BYTES : 0u) +
+          mbar_arrive_expect_tx(&full[slot_r], (u == 0 ? (uint32_t)C::Q_BYTES : kv_bytes) +
                                                    (rope_rows ? (uint32_t)C::ROPE_BYTES : 0u));
           if (u == 0) bulk_g2s(Qs + slot_r * C::Q_BYTES, qg, C::Q_BYTES, &full[slot_r]);
           if (rope_rows) {
@@ -286,7 +348,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS, DecodeCfg<D, GP>::M
             bulk_g2s(rdst + D / 2, p.rope.sin + pos * (D / 2), D * 2, &full[slot_r]);
           }
         }
-        if (nk > 0)
+        if (u > 0 && nk > 0)
           copy_keys(b, hkv, kb + u * C::SK, nk, Ks + slot_r * C::TILE_ELEMS, Vs + slot_r * C::TILE_ELEMS, &full[slot_r]);
       }
       return true;
@@ -309,14 +371,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS, DecodeCfg<D, GP>::M
       while (ok && pos < hi) {
         const long long ks = rs + kRowCost;  // its keys: cost positions [ks, ks + len)
         const long long a = max(pos, ks), e = min(hi, ks + len);
-        if (a < e) {
-          const long long cta_lo = ks / per;
-          const long long cta_hi = (ks + len - 1) / per;
-          const int np = (int)(cta_hi - cta_lo + 1);
-          const int slot = 2 * cta + (a == lo ? 0 : 1);
-          const int lo_odd = (ks != cta_lo * per) ? 1 : 0;
-          ok = emit(b, hg, (int)(a - ks), (int)(e - ks), np, slot, (int)cta_lo, lo_odd);
-        }
+        if (a < e) ok = emit(b, hg, (int)(a - ks), (int)(e - ks), ks, a == lo);
         pos = rs + rcost;
         // next row (skip sequences with no keys)
         rs += rcost;
@@ -334,7 +389,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS, DecodeCfg<D, GP>::M
     if (nonempty < p.B) {
       for (long long e = cta; ok && e < (long long)p.B * Hg; e += gridDim.x) {
         const int b = (int)(e / Hg);
-        if (seq_len(b) == 0) ok = emit(b, (int)(e - (long long)b * Hg), 0, 0, 0, 0, 0, 0);
+        if (seq_len(b) == 0) ok = emit(b, (int)(e - (long long)b * Hg), 0, 0, 0, false);
       }
     }
     if (ok) {
@@ -363,20 +418,25 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS, DecodeCfg<D, GP>::M
   const float qscale = p.scale * kLog2e;
   float* pw = pbuf + warp * 32;
   float* aw = abuf + warp * GP;
+  // A slot is handed back to the producer once every warp is done with it (the test hook withholds CTA 0's
+  // release of its second stage: the producer's bounded wait for that slot then runs out and the CTA winds down,
+  // with no fault).
+  auto release = [&](int slot, int t) {
+    if (lane == 0 && !(p.fault_skip_arrive && cta == 0 && t == 1)) mbar_arrive(&empty[slot]);
+  };
 
-  float2 qf[GP][4];     // scaled q, dims 8*sub .. 8*sub+7 as 4 pairs, per head
-  float2 o[GP][4];      // O accumulator, same dims
-  float m = -INFINITY;  // running max (log2 units) of this lane's head, uniform over the lanes sharing it
-  float l = 0.f;        // this lane's share of the running sum
-
-  for (int t = 0;; ++t) {
-    const int slot = t % C::NS;
+  int t = 0;  // stages consumed
+  while (true) {
+    // ---------------- one row piece; its first stage carries q ----------------
+    int slot = t % C::NS;
     if (!mbar_wait(&full[slot], (t / C::NS) & 1, p.status, abort_flag)) break;
-    const StageInfo si = info[slot];
+    StageInfo si = info[slot];
     if (si.b < 0) break;
-    const __nv_bfloat16* Kt = Ks + slot * C::TILE_ELEMS;
-    const __nv_bfloat16* Vt = Vs + slot * C::TILE_ELEMS;
-    if (si.flags & 1) {
+    float2 qf[GP][4];     // scaled q, dims 8*sub .. 8*sub+7 as 4 pairs, per head
+    float2 o[GP][4];      // O accumulator, same dims
+    float m = -INFINITY;  // running max (log2 units) of this lane's head, uniform over the lanes sharing it
+    float l = 0.f;        // this lane's share of the running sum
+    {
       const __nv_bfloat16* qsm = reinterpret_cast<const __nv_bfloat16*>(Qs + slot * C::Q_BYTES);
       const float* rc = Rs + slot * (C::ROPE_BYTES / 4);  // cos row of the q position; sin row at + D/2
 #pragma unroll
@@ -423,123 +483,130 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS, DecodeCfg<D, GP>::M
           o[g][j] = make_float2(0.f, 0.f);
         }
       }
-      m = -INFINITY;
-      l = 0.f;
     }
-    const int nk = si.nk;
-
+    bool alive = true;
+    while (true) {
+      const __nv_bfloat16* Kt = Ks + slot * C::TILE_ELEMS;
+      const __nv_bfloat16* Vt = Vs + slot * C::TILE_ELEMS;
+      const int nk = si.nk;
 #pragma unroll 1
-    for (int it = 0; it < C::ITER; ++it) {
-      // key groups of KPI keys go round-robin over the warps, so a short last stage of a piece still spreads
-      const int kb = (it * C::NW + warp) * C::KPI;
-      if (kb >= nk) break;  // warp-uniform
+      for (int it = 0; it < C::ITER; ++it) {
+        // key groups of KPI keys go round-robin over the warps, so a short last stage of a piece still spreads
+        const int kb = (it * C::NW + warp) * C::KPI;
+        if (kb >= nk) break;  // warp-uniform
 
-      // Load this iteration's K and V rows up front so the V latency hides behind the reductions.
-      uint4 kr[C::R], vr[C::R];
+        // Load this iteration's K and V rows up front so the V latency hides behind the reductions.
+        uint4 kr[C::R], vr[C::R];
 #pragma unroll
-      for (int r = 0; r < C::R; ++r) {
-        const int key = kb + r * C::RPW + rw;
-        kr[r] = make_uint4(0, 0, 0, 0);
-        vr[r] = make_uint4(0, 0, 0, 0);
-        if (key < nk) {
-          kr[r] = lds128(Kt + key * D + 8 * sub);
-          vr[r] = lds128(Vt + key * D + 8 * sub);
-        }
-      }
-      // S = (scale*log2e) q . k for R rows x GP heads, partial over this lane's 8 dims (packed fp32x2 FMAs)
-      float acc[C::VPL];
-#pragma unroll
-      for (int r = 0; r < C::R; ++r) {
-        const uint32_t w4[4] = {kr[r].x, kr[r].y, kr[r].z, kr[r].w};
-        float2 kf[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) bf16x2_to_f32(w4[j], kf[j].x, kf[j].y);
-#pragma unroll
-        for (int g = 0; g < GP; ++g) {
-          float2 s2 = __ffma2_rn(qf[g][0], kf[0], make_float2(0.f, 0.f));
-#pragma unroll
-          for (int j = 1; j < 4; ++j) s2 = __ffma2_rn(qf[g][j], kf[j], s2);
-          acc[r * GP + g] = s2.x + s2.y;
-        }
-      }
-      // Reduce-scatter over the LPR lanes of a row: afterwards lane `sub` holds
-      // the full score of value index `sub` = (row r = sub / GP, head sub % GP).
-#pragma unroll
-      for (int mask = C::LPR / 2, n = C::VPL; mask >= 1; mask >>= 1, n >>= 1) {
-        const bool up = (sub & mask) != 0;
-#pragma unroll
-        for (int i = 0; i < n / 2; ++i) {
-          const float send = up ? acc[i] : acc[i + n / 2];
-          const float keep = up ? acc[i + n / 2] : acc[i];
-          acc[i] = keep + __shfl_xor_sync(0xffffffffu, send, mask);
-        }
-      }
-      const int my_key = kb + (sub / GP) * C::RPW + rw;
-      const float s = (my_key < nk) ? acc[0] : -INFINITY;
-
-      // online softmax for head (sub % GP): max over the lanes that share it
-      float tmax = s;
-#pragma unroll
-      for (int mask = GP; mask < 32; mask <<= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, mask));
-      const float m_new = fmaxf(m, tmax);
-      const float alpha = (m_new == -INFINITY) ? 1.f : ex2_approx(m - m_new);
-      const float pv = (s == -INFINITY) ? 0.f : ex2_approx(s - m_new);
-      l = fmaf(l, alpha, pv);
-      m = m_new;
-
-      pw[lane] = pv;
-      if (rw == 0 && sub < GP) aw[sub] = alpha;
-      __syncwarp();
-      if (__any_sync(0xffffffffu, alpha < 1.f)) {
-#pragma unroll
-        for (int g = 0; g < GP; ++g) {
-          const float2 a2 = make_float2(aw[g], aw[g]);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) o[g][j] = __fmul2_rn(o[g][j], a2);
-        }
-      }
-      // O += P V over the same R rows
-#pragma unroll
-      for (int r = 0; r < C::R; ++r) {
-        const uint32_t w4[4] = {vr[r].x, vr[r].y, vr[r].z, vr[r].w};
-        float2 vf[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) bf16x2_to_f32(w4[j], vf[j].x, vf[j].y);
-        const float* pr = pw + rw * C::LPR + r * GP;
-        float pg[GP];
-        if constexpr (GP % 4 == 0) {
-#pragma unroll
-          for (int g4 = 0; g4 < GP / 4; ++g4) {
-            const float4 p4 = reinterpret_cast<const float4*>(pr)[g4];
-            pg[4 * g4] = p4.x;
-            pg[4 * g4 + 1] = p4.y;
-            pg[4 * g4 + 2] = p4.z;
-            pg[4 * g4 + 3] = p4.w;
+        for (int r = 0; r < C::R; ++r) {
+          const int key = kb + r * C::RPW + rw;
+          kr[r] = make_uint4(0, 0, 0, 0);
+          vr[r] = make_uint4(0, 0, 0, 0);
+          if (key < nk) {
+            kr[r] = lds128(Kt + key * D + 8 * sub);
+            vr[r] = lds128(Vt + key * D + 8 * sub);
           }
-        } else {
-#pragma unroll
-          for (int g = 0; g < GP; ++g) pg[g] = pr[g];
         }
+        // S = (scale*log2e) q . k for R rows x GP heads, partial over this lane's 8 dims (packed fp32x2 FMAs)
+        float acc[C::VPL];
 #pragma unroll
-        for (int g = 0; g < GP; ++g) {
-          const float2 p2 = make_float2(pg[g], pg[g]);
+        for (int r = 0; r < C::R; ++r) {
+          const uint32_t w4[4] = {kr[r].x, kr[r].y, kr[r].z, kr[r].w};
+          float2 kf[4];
 #pragma unroll
-          for (int j = 0; j < 4; ++j) o[g][j] = __ffma2_rn(p2, vf[j], o[g][j]);
+          for (int j = 0; j < 4; ++j) bf16x2_to_f32(w4[j], kf[j].x, kf[j].y);
+#pragma unroll
+          for (int g = 0; g < GP; ++g) {
+            float2 s2 = __ffma2_rn(qf[g][0], kf[0], make_float2(0.f, 0.f));
+#pragma unroll
+            for (int j = 1; j < 4; ++j) s2 = __ffma2_rn(qf[g][j], kf[j], s2);
+            acc[r * GP + g] = s2.x + s2.y;
+          }
         }
+        // Reduce-scatter over the LPR lanes of a row: afterwards lane `sub` holds
+        // the full score of value index `sub` = (row r = sub / GP, head sub % GP).
+#pragma unroll
+        for (int mask = C::LPR / 2, n = C::VPL; mask >= 1; mask >>= 1, n >>= 1) {
+          const bool up = (sub & mask) != 0;
+#pragma unroll
+          for (int i = 0; i < n / 2; ++i) {
+            const float send = up ? acc[i] : acc[i + n / 2];
+            const float keep = up ? acc[i + n / 2] : acc[i];
+            acc[i] = keep + __shfl_xor_sync(0xffffffffu, send, mask);
+          }
+        }
+        const int my_key = kb + (sub / GP) * C::RPW + rw;
+        const float s = (my_key < nk) ? acc[0] : -INFINITY;
+
+        // online softmax for head (sub % GP): max over the lanes that share it
+        float tmax = s;
+#pragma unroll
+        for (int mask = GP; mask < 32; mask <<= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, mask));
+        const float m_new = fmaxf(m, tmax);
+        const float alpha = (m_new == -INFINITY) ? 1.f : ex2_approx(m - m_new);
+        const float pv = (s == -INFINITY) ? 0.f : ex2_approx(s - m_new);
+        l = fmaf(l, alpha, pv);
+        m = m_new;
+
+        pw[lane] = pv;
+        if (rw == 0 && sub < GP) aw[sub] = alpha;
+        __syncwarp();
+        if (__any_sync(0xffffffffu, alpha < 1.f)) {
+#pragma unroll
+          for (int g = 0; g < GP; ++g) {
+            const float2 a2 = make_float2(aw[g], aw[g]);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) o[g][j] = __fmul2_rn(o[g][j], a2);
+          }
+        }
+        // O += P V over the same R rows
+#pragma unroll
+        for (int r = 0; r < C::R; ++r) {
+          const uint32_t w4[4] = {vr[r].x, vr[r].y, vr[r].z, vr[r].w};
+          float2 vf[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) bf16x2_to_f32(w4[j], vf[j].x, vf[j].y);
+          const float* pr = pw + rw * C::LPR + r * GP;
+          float pg[GP];
+          if constexpr (GP % 4 == 0) {
+#pragma unroll
+            for (int g4 = 0; g4 < GP / 4; ++g4) {
+              const float4 p4 = reinterpret_cast<const float4*>(pr)[g4];
+              pg[4 * g4] = p4.x;
+              pg[4 * g4 + 1] = p4.y;
+              pg[4 * g4 + 2] = p4.z;
+              pg[4 * g4 + 3] = p4.w;
+            }
+          } else {
+#pragma unroll
+            for (int g = 0; g < GP; ++g) pg[g] = pr[g];
+          }
+#pragma unroll
+          for (int g = 0; g < GP; ++g) {
+            const float2 p2 = make_float2(pg[g], pg[g]);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) o[g][j] = __ffma2_rn(p2, vf[j], o[g][j]);
+          }
+        }
+        __syncwarp();
       }
       __syncwarp();
+      if (si.flags & 2) break;  // the piece's last stage: its slot is released after the merge below
+      release(slot, t);
+      ++t;
+      slot = t % C::NS;
+      if (!mbar_wait(&full[slot], (t / C::NS) & 1, p.status, abort_flag)) {
+        alive = false;
+        break;
+      }
+      si = info[slot];
     }
-    __syncwarp();
-    // this slot's K, V and q are no longer read (the test hook withholds CTA 0's release of its second stage: the
-    // producer's bounded wait for that slot then runs out and the CTA winds down, with no fault)
-    if (lane == 0 && !(p.fault_skip_arrive && cta == 0 && t == 1)) mbar_arrive(&empty[slot]);
-    if (!(si.flags & 2)) continue;
+    if (!alive) break;
 
     // ---------------- end of a row piece: merge the consumer warps ----------------
     float lsum = l;
 #pragma unroll
     for (int mask = GP; mask < 32; mask <<= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, mask);
-    // (o is folded in place: the next piece's first stage re-initialises it)
 #pragma unroll
     for (int mask = C::LPR; mask < 32; mask <<= 1)
 #pragma unroll
@@ -549,66 +616,67 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS, DecodeCfg<D, GP>::M
           o[g][j].x += __shfl_xor_sync(0xffffffffu, o[g][j].x, mask);
           o[g][j].y += __shfl_xor_sync(0xffffffffu, o[g][j].y, mask);
         }
+    // Each warp parks its O (not yet rescaled) in the K tile of the stage it just finished, scratch until the slot
+    // is released below.  With up to 4 heads per CTA a warp's O fits in the K rows of its own first key group,
+    // which no other warp reads, so it needs no barrier first; with 8 the warps wait for each other and share the
+    // tile.
+    constexpr bool kOwnRows = 2 * GP <= C::KPI;
+    constexpr int kScrStride = kOwnRows ? C::KPI * D / 2 : GP * D;  // floats between the warps' regions
+    float* scr = reinterpret_cast<float*>(Ks + slot * C::TILE_ELEMS);
+    if constexpr (!kOwnRows) named_bar_sync(1, nct);
+    if (rw == 0) {
+#pragma unroll
+      for (int g = 0; g < GP; ++g) {
+        float4* dst = reinterpret_cast<float4*>(scr + warp * kScrStride + g * D + 8 * sub);
+        dst[0] = make_float4(o[g][0].x, o[g][0].y, o[g][1].x, o[g][1].y);
+        dst[1] = make_float4(o[g][2].x, o[g][2].y, o[g][3].x, o[g][3].y);
+      }
+    }
     if (rw == 0 && sub < GP) {
       mbuf[warp * GP + sub] = m;
       lbuf[warp * GP + sub] = lsum;
     }
     named_bar_sync(1, nct);
-    // Warp w adds its rescaled O into buffer w % 2 on turn w / 2: two warps at a time, in a fixed order (bitwise
-    // reproducible); both buffers are zero on entry.
-#pragma unroll 1
-    for (int turn = 0; turn < (C::NW + 1) / 2; ++turn) {
-      if ((warp >> 1) == turn && rw == 0) {
-        float* buf = obuf + (warp & 1) * GP * D;
-#pragma unroll
-        for (int g = 0; g < GP; ++g) {
-          float M = -INFINITY;
-#pragma unroll
-          for (int w2 = 0; w2 < C::NW; ++w2) M = fmaxf(M, mbuf[w2 * GP + g]);
-          const float mw = mbuf[warp * GP + g];
-          const float e = (mw == -INFINITY) ? 0.f : ex2_approx(mw - M);
-          float* dst = buf + g * D + 8 * sub;
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            dst[2 * j] = fmaf(e, o[g][j].x, dst[2 * j]);
-            dst[2 * j + 1] = fmaf(e, o[g][j].y, dst[2 * j + 1]);
-          }
-        }
-      }
-      named_bar_sync(1, nct);
-    }
     const int hkv = si.hg / ngroups;
     const int hq0 = hkv * group + (si.hg - hkv * ngroups) * GP;
-    for (int idx = ctid; idx < GP * D; idx += nct) {
-      const int g = idx / D;
-      const int d = idx - g * D;
+    // Output pass over runs of 4 columns: M = max over the warps, each warp's O and sum weighted by 2^(m_w - M) in
+    // warp order (bitwise reproducible).  A row held by one CTA is written; otherwise it is this CTA's partial.
+    for (int e = ctid; e < GP * D / 4; e += nct) {
+      const int g = (4 * e) / D;
+      const int d = 4 * e - g * D;
       float M = -INFINITY;
 #pragma unroll
-      for (int w = 0; w < C::NW; ++w) M = fmaxf(M, mbuf[w * GP + g]);
+      for (int w2 = 0; w2 < C::NW; ++w2) M = fmaxf(M, mbuf[w2 * GP + g]);
       float L = 0.f;
+      float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-      for (int w = 0; w < C::NW; ++w) {
-        const float mw = mbuf[w * GP + g];
-        L = fmaf((mw == -INFINITY) ? 0.f : ex2_approx(mw - M), lbuf[w * GP + g], L);
+      for (int w2 = 0; w2 < C::NW; ++w2) {
+        const float mw = mbuf[w2 * GP + g];
+        const float wt = (mw == -INFINITY) ? 0.f : ex2_approx(mw - M);
+        L = fmaf(wt, lbuf[w2 * GP + g], L);
+        const float4 v = reinterpret_cast<const float4*>(scr + w2 * kScrStride + g * D)[d / 4];
+        O = make_float4(fmaf(wt, v.x, O.x), fmaf(wt, v.y, O.y), fmaf(wt, v.z, O.z), fmaf(wt, v.w, O.w));
       }
-      const float O = obuf[idx] + obuf[GP * D + idx];
-      obuf[idx] = 0.f;
-      obuf[GP * D + idx] = 0.f;
       const size_t bh = (size_t)si.b * p.Hq + hq0 + g;
       if (si.np <= 1) {
         const bool empty_seq = (si.np == 0);
-        store_out<float>(p.out, bh * D + d, empty_seq ? 0.f : O / L, p.out_f32);
+        const float inv = empty_seq ? 0.f : 1.f / L;
+        store_out4(p.out, bh * D + d, make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv), p.out_f32);
         if (d == 0 && p.lse != nullptr) p.lse[bh] = empty_seq ? -INFINITY : (M + log2f(L)) * kLn2;
       } else {
         const size_t prow = (size_t)si.slot * GP + g;
-        p.part_o[prow * D + d] = O;
+        reinterpret_cast<float4*>(p.part_o + prow * D)[d / 4] = O;
         if (d == 0) reinterpret_cast<float2*>(p.part_ml)[prow] = make_float2(M, L);
       }
     }
+    fence_proxy_async_smem();  // the scratch stores come before the copy that refills the slot
+    // every warp is done with the scratch; for a partial, the barrier also orders every thread's partial stores
+    // before thread 0's release fence and atomic below
+    named_bar_sync(1, nct);
+    release(slot, t);
+    ++t;
     if (si.np > 1) {
-      // Publish the partial (the barrier orders every thread's stores before thread 0's release
-      // fence and atomic); the CTA that lands a row's last partial merges them all.
-      named_bar_sync(1, nct);
+      // Publish the partial; the CTA that lands a row's last partial merges them all.
       if (ctid == 0) {
         const unsigned ctr = 2u + (unsigned)(si.b * Hg + si.hg);
         // release: the CTA's partial (ordered before this by the barrier) is visible before the count;
@@ -622,8 +690,8 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS, DecodeCfg<D, GP>::M
       if (*last_flag) {
         // Merge the row's partials: each thread takes a run of 4 columns of one head and folds every partial of
         // the row into it in slot order with a running max (a fixed order: bitwise reproducible), the loads of
-        // four partials in flight at a time.  Partial slots of the row: CTA c holds slot 2c (+1 for the first
-        // CTA when the row starts inside its slice).
+        // up to eight partials in flight at a time.  Partial slots of the row: CTA c holds slot 2c (+1 for the
+        // first CTA when the row starts inside its slice).
         constexpr int RUNS = GP * D / 4;
         const float2* ml_base = reinterpret_cast<const float2*>(p.part_ml);
         for (int e = ctid; e < RUNS; e += nct) {
@@ -631,7 +699,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS, DecodeCfg<D, GP>::M
           const int d = e * 4 - g * D;
           float M = -INFINITY, L = 0.f;
           float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-          auto fold = [&](float2 ml, float4 o) {
+          auto fold = [&](float2 ml, float4 ov) {
             if (ml.x > M) {  // new running max: rescale what was folded so far (nothing while M is -inf)
               const float sc = (M == -INFINITY) ? 0.f : ex2_approx(M - ml.x);
               acc = make_float4(acc.x * sc, acc.y * sc, acc.z * sc, acc.w * sc);
@@ -639,45 +707,35 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS, DecodeCfg<D, GP>::M
               M = ml.x;
             }
             const float w = (ml.x == -INFINITY) ? 0.f : ex2_approx(ml.x - M);
-            acc = make_float4(fmaf(w, o.x, acc.x), fmaf(w, o.y, acc.y), fmaf(w, o.z, acc.z), fmaf(w, o.w, acc.w));
+            acc = make_float4(fmaf(w, ov.x, acc.x), fmaf(w, ov.y, acc.y), fmaf(w, ov.z, acc.z), fmaf(w, ov.w, acc.w));
             L = fmaf(w, ml.y, L);
           };
           auto slot_of = [&](int i) { return 2 * (si.cta_lo + i) + (i == 0 ? si.lo_odd : 0); };
-          int i = 0;
-          for (; i + 3 < si.np; i += 4) {
-            float2 ml[4];
-            float4 o[4];
+          auto batch = [&](int i, auto n_c) {
+            constexpr int N = decltype(n_c)::value;
+            float2 ml[N];
+            float4 ov[N];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
+            for (int u = 0; u < N; ++u) {
               const size_t prow = (size_t)slot_of(i + u) * GP + g;
               ml[u] = __ldcg(ml_base + prow);
-              o[u] = __ldcg(reinterpret_cast<const float4*>(p.part_o + prow * D + d));
+              ov[u] = __ldcg(reinterpret_cast<const float4*>(p.part_o + prow * D + d));
             }
 #pragma unroll
-            for (int u = 0; u < 4; ++u) fold(ml[u], o[u]);
-          }
-          for (; i < si.np; ++i) {
-            const size_t prow = (size_t)slot_of(i) * GP + g;
-            fold(__ldcg(ml_base + prow), __ldcg(reinterpret_cast<const float4*>(p.part_o + prow * D + d)));
-          }
+            for (int u = 0; u < N; ++u) fold(ml[u], ov[u]);
+          };
+          int i = 0;
+          for (; i + 7 < si.np; i += 8) batch(i, std::integral_constant<int, 8>{});
+          for (; i + 1 < si.np; i += 2) batch(i, std::integral_constant<int, 2>{});
+          if (i < si.np) batch(i, std::integral_constant<int, 1>{});
           const float inv = 1.f / L;  // L > 0: the row has keys
           const size_t bh = (size_t)si.b * p.Hq + hq0 + g;
-          if (p.out_f32) {
-            *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + bh * D + d) =
-                make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-          } else {
-            __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
-            __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
-            uint2 w2;
-            w2.x = *reinterpret_cast<uint32_t*>(&lo);
-            w2.y = *reinterpret_cast<uint32_t*>(&hi);
-            *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.out) + bh * D + d) = w2;
-          }
+          store_out4(p.out, bh * D + d, make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv), p.out_f32);
           if (d == 0 && p.lse != nullptr) p.lse[bh] = (M + log2f(L)) * kLn2;
         }
       }
     }
-    named_bar_sync(1, nct);  // mbuf/lbuf/obuf/last_flag are reused by the next piece
+    named_bar_sync(1, nct);  // mbuf/lbuf/last_flag are reused by the next piece
   }
 }
 
