@@ -53,45 +53,72 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-// Cost, in keys, charged to every row with keys when the key space is split: the piece-end work of a row
-// (warp merge, output or partial, publish, a possible merge of the row) takes about as long as streaming three
-// 64-key stages (a sweep of 64 to 256 on the 8 x 4096 GQA workload put the shortest calls at 192 and above).
-constexpr int kRowCost = 192;
-#ifndef ATTN_DECODE_TAPER_MILLI
-#define ATTN_DECODE_TAPER_MILLI 200
+// Tuning constants (compile-time overridable), each set by sweeps of graph-replayed steps of the 8 x 4096 GQA,
+// paged and 131k-key decode workloads:
+//  * ROW_COST: keys charged to every row with keys when the key space is split -- its piece-end work (warp
+//    merge, output or partial, publish, a possible merge of the row) takes about as long as streaming three
+//    64-key stages (64 and 256 were slower; 96 and 128 within 1 %);
+//  * STAGE_BYTES: K and V bytes per ring stage for 2 or 4 heads per CTA (16 KB stages: within 1 %, paged slower);
+//  * RANK_W0: the slice weights by launch rank below (8 and 7: within 1 %; equal slices: 5 % slower).
+#ifndef ATTN_DECODE_ROW_COST
+#define ATTN_DECODE_ROW_COST 192
 #endif
-// Slices taper with the CTA index: CTA c of g starts at cost position F(c / g) * Wc with
-// F(x) = x + (a/2)(x - x^2), so the first CTA takes (1 + a/2) times the mean slice and the last (1 - a/2) times.
-// All CTAs issue their first copies together, memory serves them roughly in launch order, and each CTA then streams
-// at about the same rate: per-CTA traces of the 8 x 4096 GQA workload put the last CTAs' first data ~2.5 us after
-// the first CTAs' and, with equal slices, their finish ~3.5 us later.  a = 0.2 (thousandths below).
-constexpr float kTaper = ATTN_DECODE_TAPER_MILLI * 1e-3f;
-
-// First cost position of slice c of g over [0, Wc) with taper a (g >= 1; c >= g gives Wc).  Integer base plus a
-// small fp32 correction; non-decreasing in c for a < 2, and every CTA evaluates the same function, so the slices
-// tile [0, Wc).  Callers use a = 0 unless slices average at least 64 positions, so no slice is empty.
-__device__ __forceinline__ long long slice_start(long long c, long long g, long long Wc, float a) {
-  if (c >= g) return Wc;
-  const long long base = (Wc * c) / g;
-  if (a == 0.f) return base;
-  const float x = (float)c / (float)g;
-  return base + (long long)((float)Wc * (0.5f * a) * (x - x * x));
-}
-
-// The slice holding cost position pos (0 <= pos < Wc): the largest c with slice_start(c) <= pos.  The inverse of F in
-// fp32 gives a first guess; integer steps make it exact.
-__device__ __forceinline__ long long slice_of(long long pos, long long g, long long Wc, float a) {
-  const float y = (float)pos / (float)Wc;
-  float x = y;
-  if (a > 0.f) {
-    const float h = 1.f + 0.5f * a;
-    x = (h - sqrtf(fmaxf(h * h - 2.f * a * y, 0.f))) / a;
+constexpr int kRowCost = ATTN_DECODE_ROW_COST;
+#ifndef ATTN_DECODE_STAGE_BYTES
+#define ATTN_DECODE_STAGE_BYTES 32768
+#endif
+#ifndef ATTN_DECODE_RANK_W0
+#define ATTN_DECODE_RANK_W0 10
+#endif
+// Slices are weighted by the CTA's launch rank on its SM.  The persistent grid is `ranks` CTAs per SM launched in
+// rank-major order (CTA c has rank c / n, n = CTAs per rank), and per-CTA traces of the 8 x 4096 GQA workload show
+// the CTAs sharing an SM streaming at about 1.0 : 0.9 : 0.8 of each other's rate by rank, so equal slices finish
+// ~3.5 us apart.  Rank r takes weight W0 - r (10 : 9 : 8 by default).
+struct SliceMap {
+  long long Wc;     // cost positions to split
+  long long g;      // slices
+  long long n;      // slices per rank (0: equal slices)
+  int ranks;
+  long long total;  // sum of the weights of all slices
+  __device__ long long weight(int r) const { return ATTN_DECODE_RANK_W0 - r; }
+  // weights of the slices before slice c
+  __device__ long long cum(long long c) const {
+    if (n == 0) return c;
+    const long long r = c / n;
+    long long s = 0;
+    for (int q = 0; q < r; ++q) s += n * weight(q);
+    return s + (c - r * n) * weight((int)r);
   }
-  long long c = (long long)(x * (float)g);
-  c = c < 0 ? 0 : (c >= g ? g - 1 : c);
-  while (c > 0 && slice_start(c, g, Wc, a) > pos) --c;
-  while (c + 1 < g && slice_start(c + 1, g, Wc, a) <= pos) ++c;
-  return c;
+  // first cost position of slice c (c >= g: Wc); exact integer arithmetic, non-decreasing in c
+  __device__ long long start(long long c) const { return c >= g ? Wc : (Wc * cum(c)) / total; }
+  // the slice holding cost position pos (0 <= pos < Wc): the largest c with start(c) <= pos
+  __device__ long long of(long long pos) const {
+    const long long y = (pos * total) / Wc;  // the weight units before pos
+    long long c;
+    if (n == 0) {
+      c = y;
+    } else {
+      long long s = 0;
+      int r = 0;
+      while (r + 1 < ranks && s + n * weight(r) <= y) s += n * weight(r++);
+      c = r * n + (y - s) / weight(r);
+    }
+    c = c < 0 ? 0 : (c >= g ? g - 1 : c);
+    while (c > 0 && start(c) > pos) --c;
+    while (c + 1 < g && start(c + 1) <= pos) ++c;
+    return c;
+  }
+};
+
+__device__ __forceinline__ SliceMap make_slice_map(long long Wc, long long g, int ranks) {
+  SliceMap m;
+  m.Wc = Wc;
+  m.g = g;
+  m.ranks = ranks;
+  // rank weights only for the full persistent grid with enough positions per slice; otherwise equal slices
+  m.n = (ranks > 1 && g == (long long)gridDim.x && g % ranks == 0 && Wc >= 64 * g) ? g / ranks : 0;
+  m.total = m.cum(g);
+  return m;
 }
 
 template <int D, int GP>
@@ -102,13 +129,15 @@ struct DecodeCfg {
   static constexpr int KPI = RPW * R;                         // keys per warp iteration
   static constexpr int VPL = R * GP;                          // partial sums per lane before folding
   static_assert(VPL == LPR, "the fold must leave exactly one score per lane");
-  static constexpr int SK = 32768 / (D * 4);                  // keys per stage (16 KB of K + 16 KB of V)
+  // bytes of K and V per stage (GP = 2 or 4: smaller stages, more of them, with the same bytes in flight)
+  static constexpr int STAGE_BYTES = (GP == 2 || GP == 4) ? ATTN_DECODE_STAGE_BYTES : 32768;
+  static constexpr int SK = STAGE_BYTES / (D * 4);            // keys per stage
   static constexpr int NW = (SK / KPI) < 4 ? (SK / KPI) : 4;  // consumer warps
   static constexpr int KPW = SK / NW;                         // keys per consumer warp per stage
   static constexpr int ITER = KPW / KPI;
   static_assert(ITER * KPI * NW == SK, "stage must split evenly over the consumer warps");
   static constexpr int MINB = (GP >= 8) ? 2 : 3;             // resident CTAs per SM (register budget)
-  static constexpr int NS = (MINB == 3) ? 2 : 3;              // ring stages
+  static constexpr int NS = ((MINB == 3) ? 2 : 3) * 32768 / STAGE_BYTES;  // ring stages (64 or 96 KB of K and V)
   static constexpr int THREADS = 32 * (NW + 1);
   static constexpr int LENS_CACHE = (GP >= 8) ? 64 : 512;    // kv_lens kept in shared memory for the walk
   static constexpr int TILE_ELEMS = SK * D;
@@ -233,9 +262,9 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS, DecodeCfg<D, GP>::M
     // its keys the last len positions, so a slice that takes on a row start also takes fewer keys.  Slices
     // that fall inside a row's cost-only head take no keys of that row.
     const long long Wc = W + (long long)kRowCost * nonempty * Hg;
-    const float taper = (Wc >= 64 * geff) ? kTaper : 0.f;
-    const long long lo = slice_start(cta, geff, Wc, taper);
-    const long long hi = slice_start(cta + 1, geff, Wc, taper);
+    const SliceMap sm = make_slice_map(Wc, geff, C::MINB);
+    const long long lo = sm.start(cta);
+    const long long hi = sm.start(cta + 1);
 
     int t = 0;  // stages issued
     bool ok = true;
@@ -301,12 +330,14 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS, DecodeCfg<D, GP>::M
       const int hq0 = hkv * group + (hg - hkv * ngroups) * GP;
       const __nv_bfloat16* qg = reinterpret_cast<const __nv_bfloat16*>(p.q) + ((size_t)b * p.Hq + hq0) * D;
       const int nkeys = ke - kb;
-      const int nst = nkeys > 0 ? (nkeys + C::SK - 1) / C::SK : 1;
+      const int first = C::SK;  // keys of the piece's first stage
+      const int nst = nkeys > 0 ? (nkeys <= first ? 1 : 1 + (nkeys - first + C::SK - 1) / C::SK) : 1;
       int np = 0, slot = 0, cta_lo = 0, lo_odd = 0;  // the piece's merge bookkeeping
       for (int u = 0; u < nst; ++u, ++t) {
         const int slot_r = t % C::NS;
         if (t >= C::NS && !wait_empty(slot_r)) return false;
-        const int nk = nkeys > 0 ? min(C::SK, nkeys - u * C::SK) : 0;
+        const int k0 = (u == 0) ? 0 : first + (u - 1) * C::SK;  // the stage's first key within the piece
+        const int nk = nkeys > 0 ? min(u == 0 ? first : C::SK, nkeys - k0) : 0;
         const uint32_t kv_bytes = 2u * (uint32_t)nk * D * 2;
         if (u == 0) {
           // The piece's first K/V copies go out before anything else: their bytes are expected without an
@@ -317,12 +348,12 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS, DecodeCfg<D, GP>::M
             copy_keys(b, hkv, kb, nk, Ks + slot_r * C::TILE_ELEMS, Vs + slot_r * C::TILE_ELEMS, &full[slot_r]);
             // which CTAs hold a piece of this row, and this piece's partial slot
             const int len = seq_len(b);
-            const long long c_lo = slice_of(ks, geff, Wc, taper);
-            const long long c_hi = slice_of(ks + len - 1, geff, Wc, taper);
+            const long long c_lo = sm.of(ks);
+            const long long c_hi = sm.of(ks + len - 1);
             np = (int)(c_hi - c_lo + 1);
             cta_lo = (int)c_lo;
             slot = 2 * cta + (first_in_slice ? 0 : 1);
-            lo_odd = (ks != slice_start(c_lo, geff, Wc, taper)) ? 1 : 0;
+            lo_odd = (ks != sm.start(c_lo)) ? 1 : 0;
           }
         }
         if (lane == 0) {
@@ -349,7 +380,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS, DecodeCfg<D, GP>::M
           }
         }
         if (u > 0 && nk > 0)
-          copy_keys(b, hkv, kb + u * C::SK, nk, Ks + slot_r * C::TILE_ELEMS, Vs + slot_r * C::TILE_ELEMS, &full[slot_r]);
+          copy_keys(b, hkv, kb + k0, nk, Ks + slot_r * C::TILE_ELEMS, Vs + slot_r * C::TILE_ELEMS, &full[slot_r]);
       }
       return true;
     };
