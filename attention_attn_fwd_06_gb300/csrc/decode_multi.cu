@@ -74,7 +74,7 @@ struct MCfg {
   static constexpr int OFF_BAR = OFF_V + NS * TILE_BYTES;
   // barriers: q_full, q_empty, k_full[NS], v_full[NS], k_empty[NS], v_empty[NS], s_full[2], p_full[2],
   // o_done[2], drain, q_ready
-  static constexpr int NBAR = 2 + 4 * NS + 2 + 2 + 2 + 1 + 1;
+  static constexpr int NBAR = 2 + 4 * NS + 2 + 2 + 2 + 1 + 1 + 1;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // tmem address, abort flag, last-partial flag
   static constexpr int SMEM_USED = OFF_MISC + 16;
   static constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // slack to align the base to 1024
@@ -283,6 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* o_done = p_full + 2;        // [2] P V of even / odd tiles completed
   uint64_t* drain = o_done + 2;
   uint64_t* q_ready = drain + 1;        // with RoPE: the piece's Q rows are rotated (128 arrivals)
+  uint64_t* merge_bar = q_ready + 1;    // an item's partials copied into the idle K/V ring for its merge
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   volatile int* last_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
@@ -665,10 +666,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       named_bar_sync(1, kSoftmaxThreads);
       if (*last_flag) {
         // Merge: the 128 threads split the item's rows into 32-column chunks; each thread folds the partials of
-        // its chunks in slot order with a running max (fixed order: bitwise reproducible), two partials' loads
-        // in flight at a time.
+        // its chunks in slot order with a running max (fixed order: bitwise reproducible).  When this is the
+        // CTA's last piece the K/V ring is idle (every load landed and every MMA reading it completed before
+        // this epilogue), so the partials come into it with one round of bulk copies; otherwise two partials'
+        // loads are in flight at a time.
         constexpr int CPR = D / 32;  // chunks per row
-        for (int e = stid; e < a.R * CPR; e += kSoftmaxThreads) {
+        const uint32_t pbytes = (uint32_t)a.R * D * 4;  // one partial's O
+        const uint32_t mlbytes = (uint32_t)a.R * 8;     // its (m, l) rows
+        Walk peek = walk;
+        Piece pn;
+        const bool in_smem = (a.R % 2 == 0) && !walk_next(peek, a, pn) &&
+                             (size_t)pc.np * (pbytes + mlbytes) <= (size_t)2 * C::NS * C::TILE_BYTES;
+        const float* sm_o = reinterpret_cast<const float*>(Ks);                                // [np][R][D]
+        const float2* sm_ml = reinterpret_cast<const float2*>(Ks + (size_t)pc.np * pbytes);  // [np][R]
+        bool merge_ok = true;
+        if (in_smem) {
+          if (stid == 0) {
+            mbar_arrive_expect_tx(merge_bar, (uint32_t)pc.np * (pbytes + mlbytes));
+            for (int i = 0; i < pc.np; ++i) {
+              const size_t prow = (size_t)slot_of(pc, i) * a.R;
+              bulk_g2s(Ks + (size_t)i * pbytes, a.part_o + prow * D, pbytes, merge_bar);
+              bulk_g2s(Ks + (size_t)pc.np * pbytes + (size_t)i * mlbytes, a.part_ml + prow * 2, mlbytes, merge_bar);
+            }
+          }
+          merge_ok = mbar_wait(merge_bar, 0, a.status, abort_flag);  // at most one such merge per CTA
+          // after a failed wait the copies may still be landing: let them, before shared memory is released
+          if (!merge_ok) mbar_wait(merge_bar, 0, a.status, nullptr);
+        }
+        for (int e = stid; merge_ok && e < a.R * CPR; e += kSoftmaxThreads) {
           const int r = e / CPR;
           const int ch = e - r * CPR;
           float M = -INFINITY, L = 0.f;
@@ -695,6 +720,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             L = fmaf(w, ml.y, L);
           };
           int i = 0;
+          if (in_smem) {
+            for (; i < pc.np; ++i) {
+              const float4* s0 = reinterpret_cast<const float4*>(sm_o + ((size_t)i * a.R + r) * D + ch * 32);
+              float4 o0[8];
+#pragma unroll
+              for (int j = 0; j < 8; ++j) o0[j] = s0[j];
+              fold(sm_ml[(size_t)i * a.R + r], o0);
+            }
+          }
           for (; i + 1 < pc.np; i += 2) {
             const size_t p0 = (size_t)slot_of(pc, i) * a.R + r;
             const size_t p1 = (size_t)slot_of(pc, i + 1) * a.R + r;
