@@ -47,6 +47,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "slice_map.h"
 
 namespace attn {
 namespace {
@@ -59,7 +60,7 @@ constexpr float kLn2 = 0.6931471805599453f;
 //    merge, output or partial, publish, a possible merge of the row) takes about as long as streaming three
 //    64-key stages (64 and 256 were slower; 96 and 128 within 1 %);
 //  * STAGE_BYTES: K and V bytes per ring stage for 2 or 4 heads per CTA (16 KB stages: within 1 %, paged slower);
-//  * RANK_W0: the slice weights by launch rank below (8 and 7: within 1 %; equal slices: 5 % slower).
+//  * RANK_W0: the slice weights by launch rank (slice_map.h; 8 and 7: within 1 %; equal slices: 5 % slower).
 #ifndef ATTN_DECODE_ROW_COST
 #define ATTN_DECODE_ROW_COST 192
 #endif
@@ -67,60 +68,6 @@ constexpr int kRowCost = ATTN_DECODE_ROW_COST;
 #ifndef ATTN_DECODE_STAGE_BYTES
 #define ATTN_DECODE_STAGE_BYTES 32768
 #endif
-#ifndef ATTN_DECODE_RANK_W0
-#define ATTN_DECODE_RANK_W0 10
-#endif
-// Slices are weighted by the CTA's launch rank on its SM.  The persistent grid is `ranks` CTAs per SM launched in
-// rank-major order (CTA c has rank c / n, n = CTAs per rank), and per-CTA traces of the 8 x 4096 GQA workload show
-// the CTAs sharing an SM streaming at about 1.0 : 0.9 : 0.8 of each other's rate by rank, so equal slices finish
-// ~3.5 us apart.  Rank r takes weight W0 - r (10 : 9 : 8 by default).
-struct SliceMap {
-  long long Wc;     // cost positions to split
-  long long g;      // slices
-  long long n;      // slices per rank (0: equal slices)
-  int ranks;
-  long long total;  // sum of the weights of all slices
-  __device__ long long weight(int r) const { return ATTN_DECODE_RANK_W0 - r; }
-  // weights of the slices before slice c
-  __device__ long long cum(long long c) const {
-    if (n == 0) return c;
-    const long long r = c / n;
-    long long s = 0;
-    for (int q = 0; q < r; ++q) s += n * weight(q);
-    return s + (c - r * n) * weight((int)r);
-  }
-  // first cost position of slice c (c >= g: Wc); exact integer arithmetic, non-decreasing in c
-  __device__ long long start(long long c) const { return c >= g ? Wc : (Wc * cum(c)) / total; }
-  // the slice holding cost position pos (0 <= pos < Wc): the largest c with start(c) <= pos
-  __device__ long long of(long long pos) const {
-    const long long y = (pos * total) / Wc;  // the weight units before pos
-    long long c;
-    if (n == 0) {
-      c = y;
-    } else {
-      long long s = 0;
-      int r = 0;
-      while (r + 1 < ranks && s + n * weight(r) <= y) s += n * weight(r++);
-      c = r * n + (y - s) / weight(r);
-    }
-    c = c < 0 ? 0 : (c >= g ? g - 1 : c);
-    while (c > 0 && start(c) > pos) --c;
-    while (c + 1 < g && start(c + 1) <= pos) ++c;
-    return c;
-  }
-};
-
-__device__ __forceinline__ SliceMap make_slice_map(long long Wc, long long g, int ranks) {
-  SliceMap m;
-  m.Wc = Wc;
-  m.g = g;
-  m.ranks = ranks;
-  // rank weights only for the full persistent grid with enough positions per slice; otherwise equal slices
-  m.n = (ranks > 1 && g == (long long)gridDim.x && g % ranks == 0 && Wc >= 64 * g) ? g / ranks : 0;
-  m.total = m.cum(g);
-  return m;
-}
-
 template <int D, int GP>
 struct DecodeCfg {
   static constexpr int LPR = D / 8;                           // lanes per K/V row (16 B each)
@@ -262,7 +209,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS, DecodeCfg<D, GP>::M
     // its keys the last len positions, so a slice that takes on a row start also takes fewer keys.  Slices
     // that fall inside a row's cost-only head take no keys of that row.
     const long long Wc = W + (long long)kRowCost * nonempty * Hg;
-    const SliceMap sm = make_slice_map(Wc, geff, C::MINB);
+    const SliceMap sm = make_slice_map(Wc, geff, C::MINB, gridDim.x);
     const long long lo = sm.start(cta);
     const long long hi = sm.start(cta + 1);
 
