@@ -108,6 +108,7 @@ struct DecodeCfg {
   static_assert(NW * GP * D * 4 <= TILE_BYTES, "the piece-end merge parks every warp's O in one K tile");
   static_assert(KPI * NW * ITER == SK && (KPI * D * 2) % 16 == 0, "a warp's first key group: whole 16-byte rows");
   static_assert(MINB * (SMEM + 1024) <= 228 * 1024, "MINB CTAs per SM");
+  static_assert(SK / 8 + 1 <= 32, "a stage spans at most 32 pages of the smallest page size (one lane each)");
 };
 
 struct StageInfo {
@@ -194,13 +195,13 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS, DecodeCfg<D, GP>::M
       nonempty += __shfl_xor_sync(0xffffffffu, nonempty, off);
     }
     __syncwarp();
-    // The whole producer warp walks the slice in lock-step (lane 0 issues copies and barrier operations;
-    // the other lanes fetch page-table windows for the paged layout).
+    // The whole producer warp walks the slice in lock-step (lane 0 issues the barrier operations and q copies,
+    // the lanes split a stage's K/V copies between them and fetch page-table windows for the paged layout).
     auto seq_len = [&](int b) -> int { return b < C::LENS_CACHE ? lens_s[b] : clamp_len(p.kv_lens[b], p.Lmax); };
     const long long W = wsum * Hg;
     // Slices of at least min_keys keys, but never fewer slices than rows with keys (a CTA per row of a short
     // problem rather than one CTA walking many rows); CTAs past the effective grid only handle empty sequences.
-    long long geff = (W + p.min_keys - 1) / p.min_keys;
+    long long geff = floor_div(W + p.min_keys - 1, p.min_keys);
     if (geff < (long long)nonempty * Hg) geff = (long long)nonempty * Hg;
     if (geff > (long long)gridDim.x) geff = gridDim.x;
     if (geff < 1) geff = 1;
@@ -216,52 +217,48 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS, DecodeCfg<D, GP>::M
     int t = 0;  // stages issued
     bool ok = true;
     const bool paged = p.block_table != nullptr;
-    // Paged layout: lane i holds the page id of page (win_base + i) of sequence win_b.
+    // Paged layout: lane i holds the block-table entry of page (win_base + i) of sequence win_b, as loaded (it is
+    // checked where a copy uses it, so the load's latency overlaps whatever the warp does before that).
     int win_b = -1, win_base = 0, my_page = 0;
-    auto load_window = [&](int b, int first_page) {
+    // Make the window hold pages [first, last] of sequence b (last - first < 32).
+    auto need_pages = [&](int b, int first, int last) {
+      if (b == win_b && first >= win_base && last < win_base + 32) return;
       win_b = b;
-      win_base = first_page;
-      const int pg = first_page + lane;
+      win_base = first;
+      const int pg = first + lane;
       my_page = 0;
-      // only pages that hold keys of the sequence are read (and checked): entries past its last page may hold
-      // anything, e.g. the -1 a serving engine pads its block table with
-      if (pg < p.max_pages && (long long)pg * p.page_size < seq_len(b)) {
-        const int id = p.block_table[(size_t)b * p.max_pages + pg];
-        if (id < 0 || id >= p.num_pages) {
-          record_status(p.status, ATTN_ERR_DEVICE_BOUNDS);  // out-of-pool page id: read page 0 instead
-        } else {
-          my_page = id;
-        }
-      }
-      __syncwarp();
+      // only pages that hold keys of the sequence are read: entries past its last page may hold anything, e.g.
+      // the -1 a serving engine pads its block table with
+      if (pg < p.max_pages && (long long)pg * p.page_size < seq_len(b))
+        my_page = p.block_table[(size_t)b * p.max_pages + pg];
     };
-    // Copy keys [k0, k0 + nk) of row (b, hkv) to shared memory at dst (K) and dstv (V).
+    // Copy keys [k0, k0 + nk) of row (b, hkv) to shared memory at dstk (K) and dstv (V).  Contiguous: lane 0 issues
+    // the K copy and lane 1 the V copy.  Paged: lane j issues the copies of the stage's page first + j, the part of
+    // it the stage holds (a stage of at most 128 keys over pages of at least 8 keys spans at most 17 pages).
     auto copy_keys = [&](int b, int hkv, int k0, int nk, __nv_bfloat16* dstk, __nv_bfloat16* dstv, uint64_t* bar) {
       if (!paged) {
-        if (lane == 0) {
+        if (lane < 2) {
           const size_t row0 = ((size_t)b * p.Hkv + hkv) * (size_t)p.Lmax + (size_t)k0;
-          const uint32_t bytes = (uint32_t)nk * D * 2;
-          bulk_g2s(dstk, reinterpret_cast<const __nv_bfloat16*>(p.kcache) + row0 * D, bytes, bar);
-          bulk_g2s(dstv, reinterpret_cast<const __nv_bfloat16*>(p.vcache) + row0 * D, bytes, bar);
+          const __nv_bfloat16* src = reinterpret_cast<const __nv_bfloat16*>(lane == 0 ? p.kcache : p.vcache);
+          bulk_g2s(lane == 0 ? dstk : dstv, src + row0 * D, (uint32_t)nk * D * 2, bar);
         }
         return;
       }
       const int ps = p.page_size;
       const int first = k0 / ps, last = (k0 + nk - 1) / ps;
-      if (b != win_b || first < win_base || last >= win_base + 32) load_window(b, first);
-      int k = k0, done = 0;
-      for (int pg = first; pg <= last; ++pg) {
-        const int page = __shfl_sync(0xffffffffu, my_page, pg - win_base);
-        const int off = k - pg * ps;
-        const int n = min(ps - off, nk - done);
-        if (lane == 0) {
-          const size_t row0 = ((size_t)page * p.Hkv + hkv) * (size_t)ps + (size_t)off;
-          const uint32_t bytes = (uint32_t)n * D * 2;
-          bulk_g2s(dstk + done * D, reinterpret_cast<const __nv_bfloat16*>(p.kcache) + row0 * D, bytes, bar);
-          bulk_g2s(dstv + done * D, reinterpret_cast<const __nv_bfloat16*>(p.vcache) + row0 * D, bytes, bar);
+      need_pages(b, first, last);
+      const int pg = first + lane;
+      int page = __shfl_sync(0xffffffffu, my_page, min(pg, last) - win_base);
+      if (pg <= last) {
+        if (page < 0 || page >= p.num_pages) {
+          record_status(p.status, ATTN_ERR_DEVICE_BOUNDS);  // out-of-pool page id: read page 0 instead
+          page = 0;
         }
-        k += n;
-        done += n;
+        const int kl = max(k0, pg * ps), kh = min(k0 + nk, (pg + 1) * ps);  // the stage's keys on this page
+        const size_t row0 = ((size_t)page * p.Hkv + hkv) * (size_t)ps + (size_t)(kl - pg * ps);
+        const uint32_t bytes = (uint32_t)(kh - kl) * D * 2;
+        bulk_g2s(dstk + (size_t)(kl - k0) * D, reinterpret_cast<const __nv_bfloat16*>(p.kcache) + row0 * D, bytes, bar);
+        bulk_g2s(dstv + (size_t)(kl - k0) * D, reinterpret_cast<const __nv_bfloat16*>(p.vcache) + row0 * D, bytes, bar);
       }
     };
     auto wait_empty = [&](int slot_r) -> bool {
@@ -287,21 +284,55 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS, DecodeCfg<D, GP>::M
         const int nk = nkeys > 0 ? min(u == 0 ? first : C::SK, nkeys - k0) : 0;
         const uint32_t kv_bytes = 2u * (uint32_t)nk * D * 2;
         if (u == 0) {
-          // The piece's first K/V copies go out before anything else: their bytes are expected without an
-          // arrival, then the bookkeeping below, the stage record and the arrival (with q's bytes) follow, so the
-          // record is written before the phase can complete.
-          if (nk > 0) {
-            if (lane == 0) mbar_expect_tx(&full[slot_r], kv_bytes);
-            copy_keys(b, hkv, kb, nk, Ks + slot_r * C::TILE_ELEMS, Vs + slot_r * C::TILE_ELEMS, &full[slot_r]);
-            // which CTAs hold a piece of this row, and this piece's partial slot
-            const int len = seq_len(b);
-            const long long c_lo = sm.of(ks);
-            const long long c_hi = sm.of(ks + len - 1);
-            np = (int)(c_hi - c_lo + 1);
-            cta_lo = (int)c_lo;
-            slot = 2 * cta + (first_in_slice ? 0 : 1);
-            lo_odd = (ks != sm.start(c_lo)) ? 1 : 0;
+          // The piece's first copies (K/V, q, and with RoPE the table rows of position kv_len - 1) go out before
+          // anything else: their bytes are expected without an arrival, then the bookkeeping below, the stage
+          // record and the arrival follow, so the record is written before the phase can complete.
+          const bool rope_rows = rope_on && nkeys > 0;
+          if (lane == 0) {
+            const uint32_t rope_bytes = rope_rows ? (uint32_t)C::ROPE_BYTES : 0u;
+            mbar_expect_tx(&full[slot_r], kv_bytes + (uint32_t)C::Q_BYTES + rope_bytes);
           }
+          // contiguous K/V go first; a paged stage first loads its block-table window, whose latency the q copy
+          // and the bookkeeping below cover, and issues its copies after them
+          __nv_bfloat16* const kdst = Ks + slot_r * C::TILE_ELEMS;
+          __nv_bfloat16* const vdst = Vs + slot_r * C::TILE_ELEMS;
+          if (nk > 0 && !paged) copy_keys(b, hkv, kb, nk, kdst, vdst, &full[slot_r]);
+          if (nk > 0 && paged) need_pages(b, kb / p.page_size, (kb + nk - 1) / p.page_size);
+          if (lane == 0) {
+            bulk_g2s(Qs + slot_r * C::Q_BYTES, qg, C::Q_BYTES, &full[slot_r]);
+            if (rope_rows) {
+              const size_t pos = (size_t)(seq_len(b) - 1);
+              float* rdst = Rs + slot_r * (C::ROPE_BYTES / 4);
+              bulk_g2s(rdst, p.rope.cos + pos * (D / 2), D * 2, &full[slot_r]);
+              bulk_g2s(rdst + D / 2, p.rope.sin + pos * (D / 2), D * 2, &full[slot_r]);
+            }
+          }
+          if (nk > 0) {
+            // Which CTAs hold a piece of this row, and this piece's partial slot.  This CTA's slice holds some of
+            // the row's keys [ks, ks + len), so the slices holding its first and last key, c_lo and c_hi, lie on
+            // either side of cta; the warp tests 32 slices at a time with starts_by (start is non-decreasing).
+            const long long last = ks + seq_len(b) - 1;
+            int c_lo = 0, c_hi = cta;
+            for (int top = cta;; top -= 32) {  // c_lo: the largest c <= cta with start(c) <= ks
+              const unsigned m = __ballot_sync(0xffffffffu, top - lane >= 0 && sm.starts_by(top - lane, ks));
+              if (m) {
+                c_lo = top - (__ffs(m) - 1);
+                break;
+              }
+            }
+            for (int bot = cta + 1;; bot += 32) {  // c_hi: the largest c with start(c) <= last
+              const unsigned m = __ballot_sync(0xffffffffu, bot + lane >= sm.g || !sm.starts_by(bot + lane, last));
+              if (m) {
+                c_hi = bot + (__ffs(m) - 1) - 1;
+                break;
+              }
+            }
+            np = c_hi - c_lo + 1;
+            cta_lo = c_lo;
+            slot = 2 * cta + (first_in_slice ? 0 : 1);
+            lo_odd = sm.starts_by(c_lo, ks - 1) ? 1 : 0;  // start(c_lo) < ks
+          }
+          if (nk > 0 && paged) copy_keys(b, hkv, kb, nk, kdst, vdst, &full[slot_r]);
         }
         if (lane == 0) {
           StageInfo si;
@@ -314,16 +345,10 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS, DecodeCfg<D, GP>::M
           si.cta_lo = cta_lo;
           si.lo_odd = lo_odd;
           info[slot_r] = si;
-          // the first stage of a piece carries q, and with RoPE the table rows of its position (kv_len - 1)
-          const bool rope_rows = (u == 0) && rope_on && nkeys > 0;
-          mbar_arrive_expect_tx(&full[slot_r], (u == 0 ? (uint32_t)C::Q_BYTES : kv_bytes) +
-                                                   (rope_rows ? (uint32_t)C::ROPE_BYTES : 0u));
-          if (u == 0) bulk_g2s(Qs + slot_r * C::Q_BYTES, qg, C::Q_BYTES, &full[slot_r]);
-          if (rope_rows) {
-            const size_t pos = (size_t)(seq_len(b) - 1);
-            float* rdst = Rs + slot_r * (C::ROPE_BYTES / 4);
-            bulk_g2s(rdst, p.rope.cos + pos * (D / 2), D * 2, &full[slot_r]);
-            bulk_g2s(rdst + D / 2, p.rope.sin + pos * (D / 2), D * 2, &full[slot_r]);
+          if (u == 0) {
+            mbar_arrive(&full[slot_r]);
+          } else {
+            mbar_arrive_expect_tx(&full[slot_r], kv_bytes);
           }
         }
         if (u > 0 && nk > 0)
@@ -343,7 +368,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS, DecodeCfg<D, GP>::M
         acc += (long long)Hg * rc;
       }
       long long rcost = (long long)len + kRowCost;
-      int hg = (int)((lo - acc) / rcost);
+      int hg = (int)floor_div(lo - acc, rcost);
       long long rs = acc + (long long)hg * rcost;  // cost interval of row (b, hg): [rs, rs + rcost)
       long long pos = lo;
       while (ok && pos < hi) {
@@ -366,7 +391,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS, DecodeCfg<D, GP>::M
     // Rows of sequences with no keys: O = 0, lse = -inf, one row per CTA in turn.
     if (nonempty < p.B) {
       for (long long e = cta; ok && e < (long long)p.B * Hg; e += gridDim.x) {
-        const int b = (int)(e / Hg);
+        const int b = (int)floor_div(e, Hg);
         if (seq_len(b) == 0) ok = emit(b, (int)(e - (long long)b * Hg), 0, 0, 0, false);
       }
     }

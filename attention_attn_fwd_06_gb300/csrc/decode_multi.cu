@@ -42,6 +42,7 @@
 #include <cmath>
 
 #include "common.cuh"
+#include "intdiv.h"
 #include "kernels.h"
 #include "rope.cuh"
 #include "tcgen05.cuh"
@@ -151,7 +152,7 @@ __device__ Walk walk_init(const MultiArgs& a, int lane) {
   for (int off = 16; off >= 1; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
   const long long W = part * a.Hkv;
   const long long G = gridDim.x;
-  w.per = (W + G - 1) / G;
+  w.per = floor_div(W + G - 1, G);
   if (w.per < 1) w.per = 1;
   w.lo = (long long)blockIdx.x * w.per;
   w.hi = min(w.lo + w.per, W);
@@ -189,7 +190,7 @@ __device__ Walk walk_init(const MultiArgs& a, int lane) {
       w.n = clamp_len(a.kv_lens[w.b], a.Lmax);
       w.T = tiles_of(w.n);
       const long long first = base + excl;  // first cost position of sequence w.b
-      w.hk = (int)((w.lo - first) / (w.T + kItemCost));
+      w.hk = (int)floor_div(w.lo - first, w.T + kItemCost);
       w.start = first + (long long)w.hk * (w.T + kItemCost);
       break;
     }
@@ -210,8 +211,8 @@ __device__ __forceinline__ bool walk_next(Walk& w, const MultiArgs& a, Piece& p)
       p.T = w.T;
       p.t0 = (int)(s - ts);
       p.t1 = (int)(e - ts);
-      const long long clo = ts / w.per;
-      const long long chi = (ts + w.T - 1) / w.per;
+      const long long clo = floor_div(ts, w.per);
+      const long long chi = floor_div(ts + w.T - 1, w.per);
       p.np = (int)(chi - clo + 1);
       p.cta_lo = (int)clo;
       p.lo_odd = (ts != clo * w.per) ? 1 : 0;

@@ -1,5 +1,6 @@
-// Host check of the decode grid's slice map (csrc/slice_map.h): for many sizes, the slices tile the cost space
-// in order with none empty, and of() inverts start() exactly.  Prints "ok" and returns 0, or the first failure.
+// Host check of the decode grid's slice map (csrc/slice_map.h): floor_div equals integer division over the
+// magnitudes the map uses; for many sizes, the slices tile the cost space in order with none empty, and of()
+// inverts start() exactly.  Prints "ok" and returns 0, or the first failure.
 #include <cstdio>
 #include <cstdlib>
 #include <random>
@@ -34,8 +35,25 @@ static int check(long long Wc, long long g, int ranks, long long grid, bool expe
   return 0;
 }
 
+static int check_floor_div(std::mt19937_64& rng) {
+  for (int i = 0; i < 2000000; ++i) {
+    const int abits = 1 + (int)(rng() % 63), bbits = 1 + (int)(rng() % 40);
+    const long long a = (long long)(rng() >> (64 - abits));
+    long long b = (long long)(rng() >> (64 - bbits));
+    if (b == 0) b = 1;
+    const long long want = a / b;
+    // near-exact multiples are where an estimate is most often off by one
+    const long long a2 = (want > 0 && want < (1LL << 62) / b) ? want * b - (long long)(rng() % 3) + 1 : a;
+    if (attn::floor_div(a, b) != want) return fail("floor_div", a, b, want);
+    if (a2 >= 0 && attn::floor_div(a2, b) != a2 / b)
+      return fail("floor_div near a multiple", a2, b, a2 / b);
+  }
+  return 0;
+}
+
 int main() {
   std::mt19937_64 rng(7);
+  if (check_floor_div(rng)) return 1;
   const long long grids[] = {456, 304, 444, 152};
   int bad = 0;
   for (long long grid : grids) {
