@@ -217,6 +217,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS, DecodeCfg<D, GP>::M
     int t = 0;  // stages issued
     bool ok = true;
     const bool paged = p.block_table != nullptr;
+    const uint64_t kv_policy = l2_policy_evict_first();  // K/V are read once
     // Paged layout: lane i holds the block-table entry of page (win_base + i) of sequence win_b, as loaded (it is
     // checked where a copy uses it, so the load's latency overlaps whatever the warp does before that).
     int win_b = -1, win_base = 0, my_page = 0;
@@ -240,7 +241,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS, DecodeCfg<D, GP>::M
         if (lane < 2) {
           const size_t row0 = ((size_t)b * p.Hkv + hkv) * (size_t)p.Lmax + (size_t)k0;
           const __nv_bfloat16* src = reinterpret_cast<const __nv_bfloat16*>(lane == 0 ? p.kcache : p.vcache);
-          bulk_g2s(lane == 0 ? dstk : dstv, src + row0 * D, (uint32_t)nk * D * 2, bar);
+          bulk_g2s_hint(lane == 0 ? dstk : dstv, src + row0 * D, (uint32_t)nk * D * 2, bar, kv_policy);
         }
         return;
       }
@@ -257,8 +258,10 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS, DecodeCfg<D, GP>::M
         const int kl = max(k0, pg * ps), kh = min(k0 + nk, (pg + 1) * ps);  // the stage's keys on this page
         const size_t row0 = ((size_t)page * p.Hkv + hkv) * (size_t)ps + (size_t)(kl - pg * ps);
         const uint32_t bytes = (uint32_t)(kh - kl) * D * 2;
-        bulk_g2s(dstk + (size_t)(kl - k0) * D, reinterpret_cast<const __nv_bfloat16*>(p.kcache) + row0 * D, bytes, bar);
-        bulk_g2s(dstv + (size_t)(kl - k0) * D, reinterpret_cast<const __nv_bfloat16*>(p.vcache) + row0 * D, bytes, bar);
+        bulk_g2s_hint(dstk + (size_t)(kl - k0) * D, reinterpret_cast<const __nv_bfloat16*>(p.kcache) + row0 * D, bytes,
+                      bar, kv_policy);
+        bulk_g2s_hint(dstv + (size_t)(kl - k0) * D, reinterpret_cast<const __nv_bfloat16*>(p.vcache) + row0 * D, bytes,
+                      bar, kv_policy);
       }
     };
     auto wait_empty = [&](int slot_r) -> bool {

@@ -323,6 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::tma_prefetch_desc(&tmq);
       tc::tma_prefetch_desc(&tmk);
       tc::tma_prefetch_desc(&tmv);
+      const uint64_t kv_policy = l2_policy_evict_first();  // K/V are read once
       int kv = 0;        // K/V tiles issued (ring position)
       int q_issued = 0;  // Q loads issued (one per piece)
       bool q_pending = false;
@@ -372,8 +373,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           mbar_arrive_expect_tx(&k_full[slot], C::TILE_BYTES);
           for (int db = 0; db < C::NDB; ++db)
-            tc::tma_load_3d(Ks + slot * C::TILE_BYTES + db * C::BLOCK_BYTES, &tmk, db * 64, krow, khead,
-                            &k_full[slot]);
+            tc::tma_load_3d_hint(Ks + slot * C::TILE_BYTES + db * C::BLOCK_BYTES, &tmk, db * 64, krow, khead,
+                                 &k_full[slot], kv_policy);
           if (kv >= C::NS && !wait_slot(&v_empty[slot], ((kv / C::NS) - 1) & 1)) {
             mbar_wait(&k_full[slot], (kv / C::NS) & 1, a.status, nullptr);  // K is in flight: let it land
             ok = false;
@@ -381,8 +382,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           mbar_arrive_expect_tx(&v_full[slot], C::TILE_BYTES);
           for (int db = 0; db < C::NDB; ++db)
-            tc::tma_load_3d(Vs + slot * C::TILE_BYTES + db * C::BLOCK_BYTES, &tmv, db * 64, krow, khead,
-                            &v_full[slot]);
+            tc::tma_load_3d_hint(Vs + slot * C::TILE_BYTES + db * C::BLOCK_BYTES, &tmv, db * 64, krow, khead,
+                                 &v_full[slot], kv_policy);
           ++kv;
         }
       }
