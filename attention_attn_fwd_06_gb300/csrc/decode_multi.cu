@@ -292,6 +292,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
+  if (warp == kWarpTMA && lane == 0) {
+    // the tensor maps are fetched while the set-up and the kv_lens read run
+    tc::tma_prefetch_desc(&tmq);
+    tc::tma_prefetch_desc(&tmk);
+    tc::tma_prefetch_desc(&tmv);
+  }
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::NBAR; ++i) {
       const bool many = ((&bars[i] >= p_full) && (&bars[i] < p_full + 2)) || &bars[i] == q_ready;
@@ -320,9 +326,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     // from inside the slot waits the moment the previous piece releases the buffer, so a piece boundary does
     // not drain the ring.
     if (lane == 0) {
-      tc::tma_prefetch_desc(&tmq);
-      tc::tma_prefetch_desc(&tmk);
-      tc::tma_prefetch_desc(&tmv);
       const uint64_t kv_policy = l2_policy_evict_first();  // K/V are read once
       int kv = 0;        // K/V tiles issued (ring position)
       int q_issued = 0;  // Q loads issued (one per piece)
