@@ -1,6 +1,6 @@
 // Host check of the decode grid's slice map (csrc/slice_map.h): floor_div equals integer division over the
-// magnitudes the map uses; for many sizes, the slices tile the cost space in order with none empty, and of()
-// inverts start() exactly.  Prints "ok" and returns 0, or the first failure.
+// magnitudes the map uses; for many sizes, the slices tile the cost space in order with none empty, of() inverts
+// start() exactly, and starts_by(c, pos) equals start(c) <= pos.  Prints "ok" and returns 0, or the first failure.
 #include <cstdio>
 #include <cstdlib>
 #include <random>
@@ -27,6 +27,13 @@ static int check(long long Wc, long long g, int ranks, long long grid, bool expe
     const long long x = pos(rng);
     const long long c = m.of(x);
     if (!(m.start(c) <= x && x < m.start(c + 1))) return fail("of()", Wc, g, x);
+    // starts_by (the division-free test the kernel's holder search uses) agrees with start() around c
+    for (long long d = -2; d <= 2; ++d) {
+      const long long cc = c + d;
+      if (cc < 0 || cc > g) continue;
+      for (long long px = x - 1; px <= x + 1; ++px)
+        if (m.starts_by(cc, px) != (m.start(cc) <= px)) return fail("starts_by", Wc, g, px);
+    }
   }
   if (m.n != 0) {  // the first rank's slices carry more than the last rank's
     const long long first = m.start(1) - m.start(0), last = m.start(g) - m.start(g - 1);
