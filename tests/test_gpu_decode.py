@@ -69,6 +69,21 @@ def test_decode_tiny_lengths_many_rows():
         assert_attn_close(O, lse, O_ref, lse_ref, f"chunk={chunk}")
 
 
+@pytest.mark.parametrize("B,Hq,Hkv", [
+    (40, 16, 4),   # more sequences than a warp has lanes: the length walk and the row search take two passes
+    (70, 16, 2),   # 8 heads per kv head: more sequences than the shared-memory length cache holds
+])
+def test_decode_many_sequences(B, Hq, Hkv):
+    g = torch.Generator().manual_seed(B)
+    lens = torch.randint(0, 300, (B,), generator=g, dtype=torch.int32)
+    lens[3] = 0  # an empty sequence among them
+    q, kc, vc, _ = make_decode(B, Hq, Hkv, 300, 128, seed=50 + B)
+    for chunk in (0, 7):
+        O, lse = run(q, kc, vc, lens, 0.088, chunk=chunk)
+        O_ref, lse_ref = oracle.decode(q, kc, vc, lens.tolist(), 0.088)
+        assert_attn_close(O, lse, O_ref, lse_ref, f"B={B} chunk={chunk}")
+
+
 def test_decode_all_sequences_empty():
     q, kc, vc, _ = make_decode(2, 8, 2, 64, 128, seed=4)
     O, lse = run(q, kc, vc, torch.zeros(2, dtype=torch.int32), 0.088)

@@ -68,6 +68,20 @@ def test_decode_multi_small(B, Hq, Hkv, Lq, Lmax, D, lens):
     assert_attn_close(O, lse, O_ref, lse_ref)
 
 
+def test_decode_multi_many_sequences():
+    # More sequences than a warp has lanes: the work walk's prefix sums take two passes of 32.
+    B = 45
+    g = torch.Generator().manual_seed(45)
+    lens = torch.randint(0, 400, (B,), generator=g, dtype=torch.int32).tolist()
+    lens[7] = 0
+    lens[30] = 2  # fewer keys than new tokens
+    q, kc, vc, _ = make_decode_multi(B, 16, 4, 4, 400, 128, seed=61)
+    kc, vc = poison_past_lens(kc, vc, lens)
+    O, lse = run(q, kc, vc, lens)
+    O_ref, lse_ref = oracle.decode_multi(q, kc, vc, lens, 128 ** -0.5)
+    assert_attn_close(O, lse, O_ref, lse_ref)
+
+
 def test_decode_multi_long_sequence_split_over_all_ctas():
     # One item of 64 tiles on a grid of one CTA per SM: every CTA holds a piece, the last one merges them all.
     q, kc, vc, _ = make_decode_multi(1, 4, 1, 8, 8192, 128, seed=23)
