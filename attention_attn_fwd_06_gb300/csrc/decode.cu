@@ -54,19 +54,24 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-// Tuning constants (compile-time overridable), each set by sweeps of graph-replayed steps of the 8 x 4096 GQA,
-// paged and 131k-key decode workloads:
+// Tuning constants (compile-time overridable), each set by sweeps of graph-replayed steps of the 8 x 4096 GQA
+// (contiguous, paged, RoPE) and 131k-key decode workloads:
+//  * STAGE_BYTES: K and V bytes per ring stage for 2 or 4 heads per CTA.  16 KB stages (a four-stage ring, the
+//    same bytes in flight as two 32 KB stages): 24.0 against 24.7 us on the GQA workload, 25.2 against 26.6 us
+//    paged, 24.4 against 25.6 us with RoPE, 203 against 208 us at 131k keys.  (Before the producer's bookkeeping
+//    was made cheap and its copies split across lanes, 16 KB stages were within 1 % and slower paged.)
 //  * ROW_COST: keys charged to every row with keys when the key space is split -- its piece-end work (warp
 //    merge, output or partial, publish, a possible merge of the row) takes about as long as streaming three
-//    64-key stages (64 and 256 were slower; 96 and 128 within 1 %);
-//  * STAGE_BYTES: K and V bytes per ring stage for 2 or 4 heads per CTA (16 KB stages: within 1 %, paged slower);
+//    32-key stages: with 16 KB stages 96 keys measured 23.9 / 24.7 / 24.4 / 202.5 us on those four workloads,
+//    128 keys 24.0 / 25.0 / 24.2 / 202.3 us, 64 keys 24.5 / 25.0 / 24.9 / 202.0 us, 192 keys 24.1 / 25.2 / 24.4 /
+//    203.0 us;
 //  * RANK_W0: the slice weights by launch rank (slice_map.h; 8 and 7: within 1 %; equal slices: 5 % slower).
 #ifndef ATTN_DECODE_ROW_COST
-#define ATTN_DECODE_ROW_COST 192
+#define ATTN_DECODE_ROW_COST 96
 #endif
 constexpr int kRowCost = ATTN_DECODE_ROW_COST;
 #ifndef ATTN_DECODE_STAGE_BYTES
-#define ATTN_DECODE_STAGE_BYTES 32768
+#define ATTN_DECODE_STAGE_BYTES 16384
 #endif
 template <int D, int GP>
 struct DecodeCfg {
