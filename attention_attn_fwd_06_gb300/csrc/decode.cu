@@ -25,9 +25,10 @@
 //    once and reuses it for every query of the step).
 //  * A producer warp walks the slice and streams K and V rows (contiguous
 //    cache, or pages of a paged cache through its block table) (and, on a row
-//    piece's first stage, its q vectors) into a shared-memory ring (2-3 stages)
-//    with 1-D bulk copies on the TMA engine (cp.async.bulk, mbarrier
-//    completion), running ahead of the consumers across row boundaries.
+//    piece's first stage, its q vectors) into a shared-memory ring (two to
+//    four stages, 64 or 96 KB of K and V) with 1-D bulk copies on the TMA
+//    engine (cp.async.bulk, mbarrier completion, an L2 evict-first policy for
+//    the K/V rows), running ahead of the consumers across row boundaries.
 //  * Consumer warps read 16-byte vectors of K/V from shared memory.  For a
 //    K row, D/8 lanes each hold 8 dims; the q.k partial sums of R rows x GP
 //    heads are folded across those lanes with a reduce-scatter of warp
