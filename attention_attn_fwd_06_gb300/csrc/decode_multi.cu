@@ -126,9 +126,14 @@ struct Piece {
 };
 
 // Cost, in tiles, charged to every item with keys when the tile space is split: its piece-end work
-// (epilogue or partial, publish, a possible merge) takes about as long as streaming two K/V tiles (a sweep of
-// 0 to 3 on the 8-token GQA workload put the shortest calls at 2 and 3).
-constexpr int kItemCost = 2;
+// (epilogue or partial, publish, a possible merge) takes about as long as streaming three K/V tiles.  Sweeps of
+// graph-replayed steps, 8-token GQA workload: 1 tile 25.9 us, 2 tiles 25.0-25.3 us, 3 tiles 24.6-24.8 us, 4 tiles
+// 25.1 us, 5 and 6 tiles 25.4-25.9 us (same box A/B of 2 and 3, twice: 25.0 / 25.1 against 24.7 / 24.7 us); the
+// 131k-key workload is within 0.5 % for 1 to 6.
+#ifndef ATTN_DMULTI_ITEM_COST
+#define ATTN_DMULTI_ITEM_COST 3
+#endif
+constexpr int kItemCost = ATTN_DMULTI_ITEM_COST;
 
 // Walks this CTA's share [lo, hi) of the flattened cost space.  Item (b, hk) occupies [start, start + kItemCost
 // + T): its tiles are the last T positions, so a share that takes on an item start also takes fewer tiles, and a
