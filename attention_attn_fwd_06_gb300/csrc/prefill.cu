@@ -66,7 +66,9 @@ struct Cfg {
   // D = 128: 12 warps with a register split -- warpgroup 0 holds the TMA and MMA warps (warps 2-3 idle) and
   // lowers its registers, the two softmax warpgroups (warps 4-7, 8-11) raise theirs, so the softmax threads
   // (128 scores, 64 packed P words and the row state each) keep everything in registers.  Measured on the
-  // causal 4k workload: 464 -> 444 us; at D = 64 the split was 1 % slower.
+  // causal 4k workload: 464 -> 444 us; at D = 64 the split was 1 % slower.  Of the splits 96 / 200, 104 / 192
+  // and 112 / 184, 104 / 192 is the one with no spills in either part and measured 0.7 % faster than 96 / 200
+  // (452 against 455.5 us, two same-box rounds); 56 / 224 starved the MMA warp (+20 %).
   static constexpr bool SPLIT = (D == 128);
   static constexpr int FIRST_SOFTMAX_WARP = SPLIT ? 4 : 2;
   static constexpr int THREADS = 32 * (FIRST_SOFTMAX_WARP + 4 * NQ);
@@ -74,8 +76,8 @@ struct Cfg {
   // the split.  Each SM sub-partition holds one warp of each warpgroup, so the split fits when one warp of
   // each, after the split, needs no more than the three took at launch; the inc then never waits for ever.
   static constexpr int LAUNCH_REGS = 168;
-  static constexpr int REGS_LOW = 96;
-  static constexpr int REGS_HIGH = 200;
+  static constexpr int REGS_LOW = 104;
+  static constexpr int REGS_HIGH = 192;
   static_assert(!SPLIT || (THREADS == 3 * 128 && REGS_LOW + NQ * REGS_HIGH <= 3 * LAUNCH_REGS &&
                            REGS_LOW % 8 == 0 && REGS_HIGH % 8 == 0 && REGS_LOW >= 24 && REGS_HIGH <= 256),
                 "register split must fit the launch allocation");
